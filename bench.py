@@ -1,0 +1,530 @@
+#!/usr/bin/env python
+"""Benchmark of the hot path: one full-graph training epoch of one graph partition.
+
+A step is one epoch on one partition through the C ABI: for every layer a halo
+pull from the stale-representation table, the forward aggregation and update,
+the push of the new local rows; the softmax-CE gradient; for every layer the
+backward update and (past the first layer) the backward aggregation with the
+halo-row gradients.  The metric is aggregated edge x feature per second: the
+sum over the step's aggregations of (entries x feature width), divided by the
+step time.
+
+Default workload: one partition of an R-MAT scale-24 graph (8,388,608 local +
+4,194,304 halo vertices, ~408M local entries with self loops), 3-layer GCN
+128 -> 256 -> 256 -> 172, bf16 storage with fp32 accumulation, stale tables of
+2^24 rows.  All inputs are synthetic and seeded (synth/).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+With N > 1 the script runs under torchrun, one partition per rank (weak
+scaling, no data-path collective); timing is the max over ranks.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.configs import PROFILE, TINY, WORKLOADS  # noqa: E402
+
+METRIC = "GCN layer fwd+bwd: edge·feat/s, epoch ms, % HBM roofline (SpMM) / % TC peak"
+UNIT = "edge*feat/s"
+SEED = 0
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+
+def rank_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(world: int, use_cuda: bool):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return dist
+
+
+def barrier(dist, use_cuda: bool):
+    if dist is None:
+        return
+    if use_cuda:
+        import torch
+
+        dist.barrier(device_ids=[torch.cuda.current_device()])
+    else:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, use_cuda: bool) -> float:
+    """Max of a host scalar over all ranks (identity for a single process)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float, use_cuda: bool) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def workload_by_name(name: str):
+    if name.endswith("-tiny"):
+        return TINY[name[:-5]]
+    if name in PROFILE:
+        return PROFILE[name]
+    return WORKLOADS[name]
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def edge_feat_per_step(part, w) -> int:
+    """Entries x feature width summed over the step's aggregations (forward on
+    every layer; backward, over the transpose, on every layer but the first)."""
+    fwd = sum(part.nnz * f for f in w.widths[:-1])
+    bwd = sum(part.nnz * f for f in w.widths[1:-1])
+    return int(fwd + bwd)
+
+
+def aggregation_bytes(part, w, elem: int):
+    """Compulsory bytes of each aggregation launch of one step, in launch order
+    (forward layers 0..L-1, then backward layers L-1..1): row pointers, column
+    ids, the normalisation vector, every input row once and every output row once."""
+    nL, nT, nnz = part.n_local, part.n_total, part.nnz
+    sage = w.agg == "sage"
+    fwd, bwd = [], []
+    for l in range(w.layers):
+        f = w.widths[l]
+        out_cols = 2 * f if sage else f
+        fwd.append(4 * (nL + 1) + 4 * nnz + 4 * (nL if sage else nT) + nT * f * elem + nL * out_cols * elem)
+    for l in range(w.layers - 1, 0, -1):
+        f = w.widths[l]
+        in_cols = 2 * f if sage else f
+        bwd.append(4 * (nT + 1) + 4 * nnz + 4 * (nL if sage else nT) + nL * in_cols * elem + nT * f * elem)
+    return fwd, bwd
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1939.4)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for name in ("aggregate.cu", "gnn_internal.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_aggregation_dense_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per aggregation launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"aggregate_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    src, traffic = None, None
+    for line in open(p):
+        if line.startswith("kernel_source_sha1:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_step_aggregations:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash() or traffic is None:
+        return None
+    return traffic
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.remove(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(part, w, target_s: float, seed: int, batch_rows: int = 4096, max_batches: int = 64):
+    """Time the oracle on row samples of one epoch until about target_s seconds of
+    oracle work; returns (edge_feat, seconds, description).
+
+    A batch holds, for every layer, the forward aggregation + update + update
+    backward of `batch_rows` random local rows and, past the first layer, the
+    backward aggregation of a proportional number of random transpose rows.
+    Input preparation (generator calls, widening, the sampled sub-transpose) is
+    not timed."""
+    import oracle
+
+    bf = w.dtype == "bf16"
+    nL, nT = part.n_local, part.n_total
+    sage = w.agg == "sage"
+    wts = oracle.sage_invcnt(part) if sage else oracle.gcn_dinv(part)
+    rows_t = min(nT, max(1, batch_rows * nT // max(nL, 1)))
+    deg = np.diff(part.rowptr)
+    # sampled transpose rows for every batch, and the block entries they hold
+    U_all = synth.sample_rows(nT, rows_t * max_batches, seed + 77)
+    rng = np.random.default_rng(seed)
+    U_all = U_all[rng.permutation(U_all.shape[0])]
+    sel = np.zeros(nT, bool)
+    sel[U_all] = True
+    keep = sel[part.colidx]
+    row_of = np.repeat(np.arange(nL), deg)
+    cnt = np.bincount(row_of[keep], minlength=nL)
+    sub = synth.Partition(np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32), part.colidx[keep], nL,
+                          part.n_halo, part.deg, part.local_ids, part.halo_ids, part.n_table)
+    T = oracle.transpose(sub)
+    del keep, row_of
+    ef, secs, batches = 0, 0.0, 0
+    while batches < max_batches and secs < target_s:
+        b = batches
+        for l in range(w.layers):
+            f_in, f_out = w.widths[l], w.widths[l + 1]
+            K = 2 * f_in if sage else f_in
+            rows = synth.sample_rows(nL, batch_rows, seed + 1000 * b + l)
+            parts = [part.colidx[part.rowptr[r]:part.rowptr[r + 1]] for r in rows]
+            cols = np.unique(np.concatenate(parts + [rows.astype(np.int32)]).astype(np.int64))
+            hmap = -np.ones(nT, np.int64)
+            hmap[cols] = np.arange(cols.shape[0])
+            Hs = oracle.widen(synth.features(0, f_in, f_in, SEED, 900 + l, bf16=bf, ids=cols), bf)
+            W = synth.glorot(K, f_out, SEED, synth.STREAM_WEIGHT + l).astype(np.float64)
+            G = oracle.widen(synth.features(rows.shape[0], f_out, f_out, SEED, 950 + l, bf16=bf), bf)
+            relu = l < w.layers - 1
+            t0 = time.perf_counter()
+            Z = oracle.aggregate(part, Hs, f_in, w.agg, rows=rows, hmap=hmap, weights=wts)
+            Ho = oracle.update(Z, W, relu)
+            oracle.update_backward(G, Ho, Z, W, relu, want_dz=l > 0)
+            secs += time.perf_counter() - t0
+            ef += int(deg[rows].sum()) * f_in
+            del Hs, hmap, Z, Ho, G
+            if l == 0:
+                continue
+            U = U_all[b * rows_t:(b + 1) * rows_t]
+            V = np.unique(np.concatenate([T[1][T[0][u]:T[0][u + 1]] for u in U] + [np.zeros(0, np.int32)]))
+            V = V.astype(np.int64)
+            vmap = -np.ones(nL, np.int64)
+            vmap[V] = np.arange(V.shape[0])
+            width = 2 * f_in if sage else f_in
+            dZ = oracle.widen(synth.features(0, width, width, SEED, 980 + l, bf16=bf, ids=V), bf)
+            t0 = time.perf_counter()
+            oracle.aggregate_backward(part, T, dZ, f_in, w.agg, rows=U, dmap=vmap, weights=wts)
+            secs += time.perf_counter() - t0
+            ef += int(np.diff(T[0])[U].sum()) * f_in
+            del dZ, vmap
+        batches += 1
+    desc = (f"{batches} batches; each: {batch_rows} random local rows per layer (forward aggregation + update + "
+            f"update backward) and {rows_t} random transpose rows per layer past the first (backward aggregation); "
+            f"double precision, {oracle.num_threads()} OpenMP threads; input preparation not timed")
+    return ef, secs, desc
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def fill_table(tab, n_rows, f, bf, seed, stream, dist, chunk=1 << 20):
+    """Generate a table on the host in chunks and copy it to the device view."""
+    import torch
+
+    ld = tab.stride(0)
+    buf = tab.as_strided((n_rows, ld), (ld, 1))
+    for r0 in range(0, n_rows, chunk):
+        n = min(chunk, n_rows - r0)
+        ids = np.arange(r0, r0 + n, dtype=np.int64)
+        h = synth.features(0, f, ld, seed, stream, dist, bf16=bf, ids=ids)
+        t = torch.from_numpy(h.view(np.int16) if bf else h)
+        if bf:
+            t = t.view(torch.bfloat16)
+        buf[r0:r0 + n].copy_(t, non_blocking=False)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from sparse_aggregation_dense_gb300 import PartitionModel, gnn
+
+    torch.cuda.set_device(local_rank)
+    dist = init_dist(world, True)
+    w = workload_by_name(args.workload)
+    bf = w.dtype == "bf16"
+    tdt = torch.bfloat16 if bf else torch.float32
+    t_gen = time.time()
+    part = w.make(SEED + rank)
+    t_gen = time.time() - t_gen
+    t_create = time.time()
+    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda")
+    torch.cuda.synchronize()
+    t_create = time.time() - t_create
+    for l in range(w.layers):
+        stream = synth.STREAM_FEATURES if l == 0 else synth.STREAM_TABLE + l
+        m.tables[l] = torch.empty((part.n_table, m.H[l].stride(0)), dtype=tdt, device="cuda")[:, :w.widths[l]]
+        fill_table(m.tables[l], part.n_table, w.widths[l], bf, SEED, stream, w.feat_dist if l == 0 else "normal")
+    lid = torch.from_numpy(part.local_ids).cuda()
+    m.H[0][:part.n_local] = m.tables[0][lid]
+    for l in range(w.layers):
+        K = (2 if w.agg == "sage" else 1) * w.widths[l]
+        m.W[l].copy_(torch.from_numpy(synth.glorot(K, w.widths[l + 1], SEED, synth.STREAM_WEIGHT + l)))
+    y = synth.labels(part.n_local, w.widths[-1], SEED, ids=part.local_ids)
+    m.labels.copy_(torch.from_numpy(y))
+    torch.cuda.synchronize()
+
+    ef = edge_feat_per_step(part, w)
+    for _ in range(args.warmup):
+        m.step()
+    m.check_errors()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gnn.profile_read(m.graph)  # clear
+    gnn.profile_enable(m.graph, True)
+    launches0 = gnn.launch_count()
+    barrier(dist, True)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            m.step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, True)
+    launches = gnn.launch_count() - launches0
+    gnn.profile_enable(m.graph, False)
+    prof = gnn.profile_read(m.graph)
+    m.check_errors()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(dist, ms_local, True)
+    total_ef = sum_over_ranks(dist, float(ef), True)
+    value = total_ef / (ms / 1e3)
+
+    # dominant kernel: the aggregation (forward + backward launches)
+    hbm, bf16_tf, peak_kind = measured_peaks()
+    fwd_b, bwd_b = aggregation_bytes(part, w, 2 if bf else 4)
+    alg_bytes = (sum(fwd_b) + sum(bwd_b)) * args.steps
+    agg_ms = prof["agg_fwd"][0] + prof["agg_bwd"][0]
+    agg_launches = prof["agg_fwd"][1] + prof["agg_bwd"][1]
+    achieved = alg_bytes / (agg_ms / 1e3) / 1e9 if agg_ms > 0 else 0.0
+    traffic = ncu_traffic(w.name)
+    breakdown = {k: round(v[0] / args.steps, 3) for k, v in prof.items()}
+    breakdown["other"] = round(ms_local - sum(v[0] for v in prof.values()) / args.steps, 3)
+
+    # end to end through the C ABI from pinned host buffers
+    nL = part.n_local
+    ld0 = m.H[0].stride(0)
+    x_host = synth.features(0, w.widths[0], ld0, SEED, synth.STREAM_FEATURES, w.feat_dist, bf16=bf,
+                            ids=part.local_ids)
+    x_pin = torch.from_numpy(x_host.view(np.int16) if bf else x_host).pin_memory()
+    if bf:
+        x_pin = x_pin.view(torch.bfloat16)
+    y_pin = torch.from_numpy(y).pin_memory()
+    loss_pin = torch.empty(1, dtype=torch.float32).pin_memory()
+    dw_pin = [torch.empty(d.shape, dtype=torch.float32).pin_memory() for d in m.dW]
+    h0 = m.H[0].as_strided((part.n_total, ld0), (ld0, 1))[:nL]
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(dist, True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        h0.copy_(x_pin, non_blocking=True)
+        m.labels.copy_(y_pin, non_blocking=True)
+        m.step()
+        loss_pin.copy_(m.loss, non_blocking=True)
+        for d, hp in zip(m.dW, dw_pin):
+            hp.copy_(d, non_blocking=True)
+        stream.synchronize()  # the host reads the step's result
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, True)
+    h2d = int(x_pin.numel() * x_pin.element_size() + y_pin.numel() * 4)
+    d2h = int(4 + sum(d.numel() * 4 for d in m.dW))
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cef, csec, desc = oracle_sample(part, w, args.cpu_seconds, SEED)
+        import oracle
+
+        cpu = {"value": cef / csec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+               "seconds": round(csec, 2)}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded generators, shapes of the pages' workloads)",
+        "config": {
+            "workload": w.name,
+            "description": w.description,
+            "n_local": part.n_local, "n_halo": part.n_halo, "nnz": part.nnz, "n_table": part.n_table,
+            "widths": w.widths, "agg": w.agg,
+            "edge_feat_per_step": ef,
+            "parallelism": f"one partition per GPU x{world} (no data-path collective)",
+            "l2": "inputs larger than L2 (no flush): tables and activations are tens of GB",
+            "seed": SEED,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "aggregation (CSR SpMM + heavy-row fix-up), forward and backward launches",
+            "achieved": achieved,
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": achieved / hbm if hbm else None,
+            "traffic": traffic,
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+            "algorithmic_bytes_per_step": sum(fwd_b) + sum(bwd_b),
+            "launch_groups": agg_launches,
+            "ms_per_step": round(agg_ms / args.steps, 3),
+        },
+        "breakdown_ms_per_step": breakdown,
+        "cpu_baseline": cpu,
+        "e2e": {"value": total_ef / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "setup_s": {"generate": round(t_gen, 1), "graph_create_and_alloc": round(t_create, 1)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    w = workload_by_name(args.workload)
+    part = w.make(SEED)
+    ef_total, secs = 0, 0.0
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        ef, s, desc = oracle_sample(part, w, args.ref_seconds, SEED + 7 * i, max_batches=16)
+        if i >= args.warmup:
+            ef_total += ef
+            secs += s
+    value = ef_total / secs
+    ms_full = edge_feat_per_step(part, w) / value * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_full, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded generators, shapes of the pages' workloads)",
+        "config": {"workload": w.name, "description": w.description, "n_local": part.n_local,
+                   "n_halo": part.n_halo, "nnz": part.nnz, "widths": w.widths, "agg": w.agg,
+                   "note": "ms_per_step extrapolated per edge from the sampled rows"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="rmat16m")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work timed for cpu_baseline")
+    ap.add_argument("--ref-seconds", type=float, default=3.0, help="oracle work per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours" and not args.workload.endswith("-tiny"):
+        args.warmup = 3
+    rank, world, local_rank = rank_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

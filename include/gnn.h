@@ -1,0 +1,218 @@
+/*
+ * gnn.h - C ABI of libgnn: one graph partition's full-graph GCN / GraphSAGE
+ * layer, forward and backward, on one GB300 GPU (sm_103a).
+ *
+ * The method (sources named by page title):
+ *  - "Reducing Communication in Graph Neural Network Training" (CAGNET), GNN
+ *    section: a layer computes H^(l) = sigma(A^T H^(l-1) W^l) where A holds the
+ *    graph with self loops, normalised as D^-1/2 (A + I) D^-1/2 with D the
+ *    modified degrees; the hot operations are the SpMM and the dense GEMM, and
+ *    the backward uses the same primitives.
+ *  - Sylvie (arxiv 2303.01277), Graph Engine and Alg. 1 / Alg. 2: each GPU
+ *    holds one partition; its HALO vertices (neighbours owned by another
+ *    partition) are received every layer; the feature gradients of HALO
+ *    vertices (J) are sent back in the backward pass.
+ *  - "Distributed Graph Neural Network Training with Periodic Stale
+ *    Representation Synchronization" (DIGEST), system design, Fig. 1(c): halo
+ *    rows are pulled from a table of stale representations (H_out <- H~_out)
+ *    and the fresh local rows are pushed back (H_in -> H~_in).
+ *
+ * Conventions shared by every call
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; host pointers are named as such.  The caller owns
+ *    every buffer it passes; a gnn_graph owns what it allocated.
+ *  - Matrices are row-major with a leading dimension `ld` in ELEMENTS.  Each
+ *    row must start on a 16-byte boundary: base pointers 16-byte aligned and
+ *    ld a multiple of 4 (fp32) or 8 (bf16).  A call writes columns [0, f) of
+ *    the rows it produces; for the aggregation outputs (Z, dH) the columns up
+ *    to the next 16-byte boundary are written as zeros too.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call except gnn_graph_create, gnn_graph_destroy and
+ *    gnn_get_error is asynchronous on that stream.
+ *  - Host-checkable argument errors (NULL pointers, negative or inconsistent
+ *    sizes, bad leading dimensions or alignment, unsupported widths) are
+ *    returned synchronously and nothing is launched.  Data errors found on the
+ *    device (an id outside the table, a repeated push id) set the graph's
+ *    device error word; the offending row is not written and no out-of-bounds
+ *    access happens; gnn_get_error reports them.
+ *  - Floating point: fp32 data accumulates in fp32; bf16 data (activations,
+ *    aggregations, activation gradients) accumulates in fp32 and is stored
+ *    rounded to nearest even.  dW is always fp32.  No float atomics are used:
+ *    every result is bitwise reproducible run to run.
+ */
+#ifndef GNN_H
+#define GNN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gnn_graph gnn_graph; /* opaque, owned by the library */
+
+typedef enum {
+    GNN_OK = 0,
+    GNN_EINVAL = 1,       /* bad argument (checked on the host) */
+    GNN_ENOMEM = 2,       /* device allocation failed */
+    GNN_ECUDA = 3,        /* a CUDA runtime call failed */
+    GNN_EUNSUPPORTED = 4, /* valid but unsupported shape / dtype */
+    GNN_EINDEX = 5        /* bad index data found on the device */
+} gnn_status;
+
+typedef enum { GNN_F32 = 0, GNN_BF16 = 1 } gnn_dtype;
+
+typedef enum {
+    GNN_AGG_GCN_SYM = 0,  /* Z[v] = sum_u dinv[v] dinv[u] H[u]  (A_hat = D^-1/2 (A+I) D^-1/2) */
+    GNN_AGG_SAGE_MEAN = 1 /* Z[v] = [ H[v] | mean of H[u] over u in N(v), u != v ] */
+} gnn_agg;
+
+/* Create the partition's graph (CAGNET GNN section: A with self loops and its
+ * transpose kept apart; Sylvie Graph Engine: block rows of the local vertices,
+ * columns = local vertices then HALO vertices).
+ *   rowptr  device int32[n_local + 1], rowptr[0] = 0, non-decreasing, rowptr[n_local] = nnz
+ *   colidx  device int32[nnz], every entry in [0, n_local + n_halo); row v lists
+ *           the vertices whose rows v aggregates; self loops are stored by the
+ *           caller (they are part of A + I).  Order within a row is free.
+ *   deg     device float[n_local + n_halo] degrees of A + I (global), or NULL:
+ *           then a local vertex's degree is its row length and a halo
+ *           vertex's degree is 1 + the number of times its column occurs.
+ *           Degree 0 gives a normalisation factor of 0.  (GCN only; ignored
+ *           for GraphSAGE, whose mean counts the entries u != v of row v.)
+ * The graph copies the CSR, validates it on the device, computes the
+ * normalisation, builds the transpose (entries of a transpose row ordered by
+ * ascending source row) and the load-balance schedules.  Synchronous: returns
+ * after the stream's work is done.  Errors: GNN_EINVAL (sizes, NULL),
+ * GNN_EINDEX (CSR fails validation), GNN_ENOMEM, GNN_ECUDA.  On error *out is
+ * set to NULL. */
+gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, int64_t n_halo,
+                            int64_t nnz, const float *deg, gnn_agg agg, void *stream, gnn_graph **out);
+
+/* Free everything the graph owns.  Synchronises the device first.  NULL
+ * returns GNN_EINVAL. */
+gnn_status gnn_graph_destroy(gnn_graph *g);
+
+/* Pull (DIGEST Fig. 1c, H_out <- H~_out; Sylvie Alg. 1 halo receive):
+ *   H[n_local + i, 0:f] = table[halo_ids[i], 0:f]   for i < n_halo.
+ *   table     device, n_table x ld_table, dtype
+ *   halo_ids  device int64[n_halo]; repeats allowed; an id outside
+ *             [0, n_table) sets GNN_EINDEX on the device and leaves that row.
+ *   H         device, (n_local + n_halo) x ld_h, dtype; only halo rows written.
+ * Bit-exact copy. */
+gnn_status gnn_halo_pull(gnn_graph *g, const void *table, int64_t ld_table, int64_t n_table,
+                         const int64_t *halo_ids, void *H, int64_t ld_h, int64_t f, gnn_dtype dtype,
+                         void *stream);
+
+/* Push (DIGEST Fig. 1c, H_in -> H~_in):
+ *   table[local_ids[v], 0:f] = H[v, 0:f]   for v < n_local.
+ *   H         device, n_local x ld_h (rows beyond n_local are not read)
+ *   local_ids device int64[n_local]; the partition's vertex sets do not
+ *             overlap (DIGEST complexity analysis), so a repeated id is an
+ *             error: every row carrying it is left unwritten and GNN_EINDEX is
+ *             set on the device; likewise for ids outside [0, n_table).
+ * Bit-exact copy.  Uses a graph-owned claim array of n_table words (grown on
+ * first use with a larger table; that call synchronises). */
+gnn_status gnn_halo_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, const int64_t *local_ids,
+                         void *table, int64_t ld_table, int64_t n_table, gnn_dtype dtype, void *stream);
+
+/* Column where the mean half of a GraphSAGE aggregation starts:
+ * f rounded up to 4 (fp32) or 8 (bf16) elements.  The aggregation width K' of
+ * a layer is f_in (GCN) or 2 * gnn_sage_half_offset(f_in) (GraphSAGE). */
+int64_t gnn_sage_half_offset(int64_t f, gnn_dtype dtype);
+
+/* Forward layer (CAGNET GNN section; aggregation first, then the update):
+ *   Z     = A_hat_block H           (GCN)   or [H_local | mean] (GraphSAGE)
+ *   H_out = relu ? max(Z W, 0) : Z W
+ *   H      device (n_local + n_halo) x ld_h, dtype: local rows then halo rows
+ *   W      device float[K x f_out] row-major, K = f_in (GCN) or 2 f_in
+ *          (GraphSAGE: rows 0..f_in-1 multiply the self half, f_in..2f_in-1 the
+ *          mean half).  The bf16 path rounds W to bf16 for the tensor cores.
+ *   Z      device n_local x ld_z, dtype (written; kept for the backward).
+ *          GraphSAGE: self half at column 0, mean half at
+ *          gnn_sage_half_offset(f_in), padding columns zero.  ld_z >= K'.
+ *   H_out  device n_local x ld_out, dtype.
+ * No bias (none in sigma(A^T H W)). */
+gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
+                             int64_t f_out, int relu, void *Z, int64_t ld_z, void *H_out, int64_t ld_out,
+                             gnn_dtype dtype, void *stream);
+
+/* Backward layer, by the chain rule of the forward above:
+ *   dY = relu ? G * 1[H_out > 0] : G      (ReLU'(0) = 0)
+ *   dW = Z^T dY                           device float[K x f_out], overwritten
+ *   dZ = dY W^T                           device n_local x ld_dz, dtype (work
+ *                                         buffer, same layout as Z); needed
+ *                                         only when dH != NULL
+ *   dH = A_hat_block^T dZ                 (GCN)
+ *   dH[u] = [u local] dZ_self[u] + sum over v with u in N(v), u != v of
+ *           dZ_mean[v] / |N(v) \ {v}|     (GraphSAGE)
+ *   G      device n_local x ld_g, dtype
+ *   H_out  device n_local x ld_out, dtype (read only when relu)
+ *   dH     device (n_local or n_local + n_halo) x ld_dh, dtype, or NULL to skip
+ *          the transposed aggregation (first layer).  want_halo_grad != 0 also
+ *          writes the n_halo halo rows (Sylvie Alg. 2: the HALO gradients J
+ *          that are sent back to their owners).
+ * dW is summed over rows in a fixed order (deterministic). */
+gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                              const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out, int relu,
+                              float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
+                              gnn_dtype dtype, void *stream);
+
+/* Training-harness helper (not a layer step): mean softmax cross-entropy over
+ * n rows of C logits with integer labels.
+ *   logits  device n x ld, dtype;  labels device int32[n] in [0, C)
+ *   G       device n x ld_g, dtype: (softmax - onehot) / n
+ *   row_loss device float[n] work buffer;  loss device float[1]: the mean,
+ *   summed in a fixed order.  A label outside [0, C) gives GNN_EINDEX from
+ *   the call's return only when checkable; on the device it yields a NaN loss. */
+gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
+                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream);
+
+/* Synchronise the device, then return and clear the graph's device error word
+ * (GNN_OK or GNN_EINDEX); GNN_ECUDA if the synchronisation itself failed. */
+gnn_status gnn_get_error(gnn_graph *g);
+
+/* Sizes of a graph (host outputs, any may be NULL). */
+gnn_status gnn_graph_sizes(const gnn_graph *g, int64_t *n_local, int64_t *n_halo, int64_t *nnz);
+
+/* Copy the transpose built by gnn_graph_create into caller device buffers
+ * (asynchronous on stream): rowptrT int32[n_local + n_halo + 1],
+ * colidxT int32[nnz] (source rows, ascending within each row) and
+ * permT int32[nnz] (the block entry each transpose entry came from).  Any of
+ * the three may be NULL to skip it. */
+gnn_status gnn_graph_copy_transpose(const gnn_graph *g, int32_t *rowptrT, int32_t *colidxT, int32_t *permT,
+                                    void *stream);
+
+/* Event timing of the library's kernel groups, for profiling (off by default).
+ * When enabled on a graph, every call on it records a CUDA event pair around
+ * each group it launches, on the call's stream:
+ *   GNN_PROF_AGG_FWD   the forward aggregation (SpMM kernel and its heavy-row fix-up)
+ *   GNN_PROF_AGG_BWD   the backward aggregation over the transpose
+ *   GNN_PROF_UPD_FWD   the forward dense update (GEMM + ReLU)
+ *   GNN_PROF_UPD_BWD   the backward dense update (dZ and dW)
+ *   GNN_PROF_PULL, GNN_PROF_PUSH  the table copies
+ * gnn_profile_read synchronises the device, writes the summed milliseconds and
+ * the number of recorded groups per kind (arrays of GNN_PROF_COUNT entries,
+ * host memory) and clears the records. */
+typedef enum {
+    GNN_PROF_AGG_FWD = 0,
+    GNN_PROF_AGG_BWD = 1,
+    GNN_PROF_UPD_FWD = 2,
+    GNN_PROF_UPD_BWD = 3,
+    GNN_PROF_PULL = 4,
+    GNN_PROF_PUSH = 5,
+    GNN_PROF_COUNT = 6
+} gnn_prof_kind;
+gnn_status gnn_profile_enable(gnn_graph *g, int on);
+gnn_status gnn_profile_read(gnn_graph *g, double *ms, int64_t *count);
+
+/* Number of kernels libgnn has launched in this process so far (all graphs). */
+int64_t gnn_launch_count(void);
+
+/* Static text for a status code. */
+const char *gnn_status_string(gnn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GNN_H */

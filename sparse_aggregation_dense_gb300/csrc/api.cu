@@ -1,0 +1,432 @@
+// api.cu - the C ABI (include/gnn.h): argument checks, graph lifetime and the
+// order of the kernels of each call.
+#include <atomic>
+#include <cstdlib>
+#include <new>
+
+#include "gnn_internal.cuh"
+
+using namespace gnn;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool dtype_ok(gnn_dtype t) { return t == GNN_F32 || t == GNN_BF16; }
+
+// a row-major operand of `rows` rows whose rows start on 16-byte boundaries
+inline bool operand_ok(const void *p, int64_t rows, int64_t ld, int64_t f, gnn_dtype t) {
+    if (rows == 0) return true;
+    if (!p || !aligned16(p)) return false;
+    if (ld < f || ld % elems_per_16b(t) != 0) return false;
+    return true;
+}
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// Wp = W laid out on the rows of the aggregation (GraphSAGE padding rows zero);
+// the bf16 path rounds W to bf16 (nearest even), the precision its products use.
+__global__ void pack_w_kernel(const float *__restrict__ W, int64_t K, int64_t N, int64_t f_in, int64_t half, int sage,
+                              int64_t Kp, float *__restrict__ Wp, int64_t ldw, int to_bf16) {
+    int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= Kp * ldw) return;
+    int64_t kp = x / ldw, j = x % ldw;
+    int64_t k = -1;
+    if (!sage) k = kp < K ? kp : -1;
+    else if (kp < f_in) k = kp;
+    else if (kp >= half && kp < half + f_in) k = f_in + (kp - half);
+    float w = (k >= 0 && j < N) ? W[k * N + j] : 0.f;
+    Wp[x] = to_bf16 ? __bfloat162float(__float2bfloat16_rn(w)) : w;
+}
+
+__global__ void unpack_dw_kernel(const float *__restrict__ dWp, int64_t N, int64_t f_in, int64_t half,
+                                 float *__restrict__ dW) {
+    int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= 2 * f_in * N) return;
+    int64_t k = x / N, j = x % N;
+    int64_t kp = k < f_in ? k : half + (k - f_in);
+    dW[x] = dWp[kp * N + j];
+}
+
+}  // namespace
+
+namespace gnn {
+
+static std::atomic<int64_t> g_launches{0};
+
+bool force_simt_update() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("GNN_UPDATE_SIMT");
+        v = (e && e[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+void count_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+gnn_status ensure_workspace(gnn_graph *g, size_t bytes, cudaStream_t s) {
+    if (bytes <= g->ws_bytes) return GNN_OK;
+    if (g->ws) GNN_CUDA_TRY(cudaFreeAsync(g->ws, s));
+    g->ws = nullptr;
+    g->ws_bytes = 0;
+    size_t want = bytes + bytes / 4;
+    GNN_CUDA_TRY(cudaMallocAsync(&g->ws, want, s));
+    g->ws_bytes = want;
+    return GNN_OK;
+}
+
+}  // namespace gnn
+
+namespace {
+
+// Records an event pair around a group of launches when profiling is on.
+struct ProfScope {
+    gnn_graph *g;
+    int kind;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr, b = nullptr;
+    ProfScope(gnn_graph *g_, int kind_, cudaStream_t s_) : g(g_), kind(kind_), s(s_) {
+        if (!g->prof_on) return;
+        if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+            a = b = nullptr;
+            return;
+        }
+        cudaEventRecord(a, s);
+    }
+    ~ProfScope() {
+        if (!a) return;
+        cudaEventRecord(b, s);
+        g->prof.push_back({kind, a, b});
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+int64_t gnn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+gnn_status gnn_profile_enable(gnn_graph *g, int on) {
+    if (!g) return GNN_EINVAL;
+    g->prof_on = on != 0;
+    return GNN_OK;
+}
+
+gnn_status gnn_profile_read(gnn_graph *g, double *ms, int64_t *count) {
+    if (!g || !ms || !count) return GNN_EINVAL;
+    for (int k = 0; k < GNN_PROF_COUNT; ++k) {
+        ms[k] = 0.0;
+        count[k] = 0;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return GNN_ECUDA;
+    for (auto &r : g->prof) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess && r.kind >= 0 && r.kind < GNN_PROF_COUNT) {
+            ms[r.kind] += t;
+            count[r.kind] += 1;
+        }
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g->prof.clear();
+    return GNN_OK;
+}
+
+const char *gnn_status_string(gnn_status s) {
+    switch (s) {
+        case GNN_OK: return "ok";
+        case GNN_EINVAL: return "invalid argument";
+        case GNN_ENOMEM: return "out of device memory";
+        case GNN_ECUDA: return "CUDA runtime error";
+        case GNN_EUNSUPPORTED: return "unsupported shape or type";
+        case GNN_EINDEX: return "bad index data on the device";
+    }
+    return "unknown status";
+}
+
+int64_t gnn_sage_half_offset(int64_t f, gnn_dtype dtype) {
+    return round_up(f, dtype == GNN_BF16 ? 8 : 4);
+}
+
+static void destroy_graph(gnn_graph *g) {
+    if (!g) return;
+    for (auto &r : g->prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    cudaFree(g->rowptr);
+    cudaFree(g->colidx);
+    cudaFree(g->rowptrT);
+    cudaFree(g->colidxT);
+    cudaFree(g->permT);
+    cudaFree(g->colw);
+    cudaFree(g->err);
+    cudaFree(g->ws);
+    cudaFree(g->claim);
+    free_schedule(&g->fwd);
+    free_schedule(&g->bwd);
+    delete g;
+}
+
+gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, int64_t n_halo,
+                            int64_t nnz, const float *deg, gnn_agg agg, void *stream, gnn_graph **out) {
+    if (!out) return GNN_EINVAL;
+    *out = nullptr;
+    if (n_local < 0 || n_halo < 0 || nnz < 0 || !rowptr) return GNN_EINVAL;
+    if (nnz > 0 && !colidx) return GNN_EINVAL;
+    if (agg != GNN_AGG_GCN_SYM && agg != GNN_AGG_SAGE_MEAN) return GNN_EINVAL;
+    if (n_local + n_halo >= ((int64_t)1 << 31) || nnz >= ((int64_t)1 << 31)) return GNN_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    gnn_graph *g = new (std::nothrow) gnn_graph();
+    if (!g) return GNN_ENOMEM;
+    cudaGetDevice(&g->device);
+    g->n_local = n_local;
+    g->n_halo = n_halo;
+    g->nnz = nnz;
+    g->agg = agg;
+    const int64_t nT = n_local + n_halo;
+    gnn_status st = GNN_OK;
+    auto fail = [&](gnn_status e) {
+        cudaStreamSynchronize(s);
+        destroy_graph(g);
+        return e;
+    };
+#define TRY_CUDA(x)                                          \
+    do {                                                     \
+        cudaError_t e_ = (x);                                \
+        if (e_ != cudaSuccess) return fail(cuda_status(e_)); \
+    } while (0)
+#define TRY(x)                         \
+    do {                               \
+        st = (x);                      \
+        if (st != GNN_OK) return fail(st); \
+    } while (0)
+    TRY_CUDA(cudaMalloc((void **)&g->err, sizeof(int)));
+    TRY_CUDA(cudaMemsetAsync(g->err, 0, sizeof(int), s));
+    TRY_CUDA(cudaMalloc((void **)&g->rowptr, (size_t)(n_local + 1) * sizeof(int32_t)));
+    TRY_CUDA(cudaMalloc((void **)&g->colidx, (size_t)(nnz > 0 ? nnz : 1) * sizeof(int32_t)));
+    TRY_CUDA(cudaMemcpyAsync(g->rowptr, rowptr, (size_t)(n_local + 1) * sizeof(int32_t), cudaMemcpyDefault, s));
+    if (nnz > 0)
+        TRY_CUDA(cudaMemcpyAsync(g->colidx, colidx, (size_t)nnz * sizeof(int32_t), cudaMemcpyDefault, s));
+    TRY(launch_validate_csr(g->rowptr, g->colidx, n_local, nT, nnz, g->err, s));
+    int bad = 0;
+    TRY_CUDA(cudaMemcpyAsync(&bad, g->err, sizeof(int), cudaMemcpyDeviceToHost, s));
+    TRY_CUDA(cudaStreamSynchronize(s));
+    if (bad) return fail(GNN_EINDEX);
+    // normalisation
+    if (agg == GNN_AGG_GCN_SYM) {
+        TRY_CUDA(cudaMalloc((void **)&g->colw, (size_t)(nT > 0 ? nT : 1) * sizeof(float)));
+        TRY(launch_gcn_dinv(g->rowptr, g->colidx, n_local, n_halo, nnz, deg, g->colw, s));
+    } else {
+        TRY_CUDA(cudaMalloc((void **)&g->colw, (size_t)(n_local > 0 ? n_local : 1) * sizeof(float)));
+        TRY(launch_sage_invcnt(g->rowptr, g->colidx, n_local, g->colw, s));
+    }
+    // transpose
+    TRY_CUDA(cudaMalloc((void **)&g->rowptrT, (size_t)(nT + 1) * sizeof(int32_t)));
+    TRY_CUDA(cudaMalloc((void **)&g->colidxT, (size_t)(nnz > 0 ? nnz : 1) * sizeof(int32_t)));
+    TRY_CUDA(cudaMalloc((void **)&g->permT, (size_t)(nnz > 0 ? nnz : 1) * sizeof(int32_t)));
+    TRY(csr_transpose(g->rowptr, g->colidx, n_local, nT, nnz, g->rowptrT, g->colidxT, g->permT, s));
+    // schedules
+    TRY(build_schedule(g->rowptr, n_local, &g->fwd, s));
+    TRY(build_schedule(g->rowptrT, nT, &g->bwd, s));
+    TRY_CUDA(cudaStreamSynchronize(s));
+    TRY_CUDA(cudaGetLastError());
+#undef TRY
+#undef TRY_CUDA
+    *out = g;
+    return GNN_OK;
+}
+
+gnn_status gnn_graph_destroy(gnn_graph *g) {
+    if (!g) return GNN_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    destroy_graph(g);
+    return e == cudaSuccess ? GNN_OK : GNN_ECUDA;
+}
+
+gnn_status gnn_graph_sizes(const gnn_graph *g, int64_t *n_local, int64_t *n_halo, int64_t *nnz) {
+    if (!g) return GNN_EINVAL;
+    if (n_local) *n_local = g->n_local;
+    if (n_halo) *n_halo = g->n_halo;
+    if (nnz) *nnz = g->nnz;
+    return GNN_OK;
+}
+
+gnn_status gnn_graph_copy_transpose(const gnn_graph *g, int32_t *rowptrT, int32_t *colidxT, int32_t *permT,
+                                    void *stream) {
+    if (!g) return GNN_EINVAL;
+    cudaStream_t s = as_stream(stream);
+    const size_t nT1 = (size_t)(g->n_local + g->n_halo + 1) * sizeof(int32_t);
+    const size_t nz = (size_t)g->nnz * sizeof(int32_t);
+    if (rowptrT) GNN_CUDA_TRY(cudaMemcpyAsync(rowptrT, g->rowptrT, nT1, cudaMemcpyDeviceToDevice, s));
+    if (colidxT && nz) GNN_CUDA_TRY(cudaMemcpyAsync(colidxT, g->colidxT, nz, cudaMemcpyDeviceToDevice, s));
+    if (permT && nz) GNN_CUDA_TRY(cudaMemcpyAsync(permT, g->permT, nz, cudaMemcpyDeviceToDevice, s));
+    return GNN_OK;
+}
+
+gnn_status gnn_get_error(gnn_graph *g) {
+    if (!g) return GNN_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GNN_ECUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, g->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GNN_ECUDA;
+    if (cudaMemset(g->err, 0, sizeof(int)) != cudaSuccess) return GNN_ECUDA;
+    return v ? GNN_EINDEX : GNN_OK;
+}
+
+gnn_status gnn_halo_pull(gnn_graph *g, const void *table, int64_t ld_table, int64_t n_table, const int64_t *halo_ids,
+                         void *H, int64_t ld_h, int64_t f, gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f <= 0 || n_table < 0) return GNN_EINVAL;
+    if (g->n_halo == 0) return GNN_OK;
+    if (!halo_ids || !operand_ok(table, n_table > 0 ? 1 : 0, ld_table, f, dtype) ||
+        !operand_ok(H, g->n_local + g->n_halo, ld_h, f, dtype))
+        return GNN_EINVAL;
+    ProfScope prof(g, GNN_PROF_PULL, as_stream(stream));
+    return launch_pull(table, ld_table, n_table, halo_ids, g->n_halo, H, ld_h, g->n_local, f, elem_size(dtype), g->err,
+                       as_stream(stream));
+}
+
+gnn_status gnn_halo_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, const int64_t *local_ids, void *table,
+                         int64_t ld_table, int64_t n_table, gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f <= 0 || n_table < 0) return GNN_EINVAL;
+    if (g->n_local == 0) return GNN_OK;
+    if (!local_ids || !operand_ok(H, g->n_local, ld_h, f, dtype) ||
+        !operand_ok(table, n_table > 0 ? 1 : 0, ld_table, f, dtype))
+        return GNN_EINVAL;
+    gnn_status st = ensure_claim(g, n_table);  // a first push to a larger table allocates (synchronising)
+    if (st != GNN_OK) return st;
+    ProfScope prof(g, GNN_PROF_PUSH, as_stream(stream));
+    return launch_push(g, H, ld_h, g->n_local, f, local_ids, table, ld_table, n_table, elem_size(dtype),
+                       as_stream(stream));
+}
+
+gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W, int64_t f_out,
+                             int relu, void *Z, int64_t ld_z, void *H_out, int64_t ld_out, gnn_dtype dtype,
+                             void *stream) {
+    if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W) return GNN_EINVAL;
+    const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    const int64_t half = gnn_sage_half_offset(f_in, dtype);
+    const int64_t K = sage ? 2 * f_in : f_in;
+    const int64_t Kp = sage ? 2 * half : f_in;
+    if (!operand_ok(H, nT, ld_h, f_in, dtype) || !operand_ok(Z, nL, ld_z, Kp, dtype) ||
+        !operand_ok(H_out, nL, ld_out, f_out, dtype))
+        return GNN_EINVAL;
+    if (f_in * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    if (nL == 0) return GNN_OK;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const bool use_tc = dtype == GNN_BF16 && update_fwd_tc_supported(Kp, f_out) && !force_simt_update();
+    const size_t wp_bytes = align_up((size_t)Kp * ldw * sizeof(float));
+    const size_t wt_bytes = use_tc ? align_up(update_tc_wt_bytes(Kp, f_out)) : 0;
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->fwd, f_in));
+    gnn_status st = ensure_workspace(g, wp_bytes + wt_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    float *Wp = static_cast<float *>(g->ws);
+    void *wt = static_cast<char *>(g->ws) + wp_bytes;
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(g->ws) + wp_bytes + wt_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(Kp * ldw, 256), 256, 0, s>>>(W, K, f_out, f_in, half, sage, Kp, Wp, ldw,
+                                                                      dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    AggParams p{};
+    p.rowptr = g->rowptr;
+    p.colidx = g->colidx;
+    p.n_rows = nL;
+    p.X = H;
+    p.ldx = ld_h;
+    p.f = f_in;
+    p.colw = g->colw;
+    p.mode = sage ? AGG_SAGE_FWD : AGG_GCN;
+    p.out = Z;
+    p.ldo = ld_z;
+    p.out_off = sage ? half : 0;
+    {
+        ProfScope prof(g, GNN_PROF_AGG_FWD, s);
+        st = launch_aggregate(p, g->fwd, dtype, partial, s);
+    }
+    if (st != GNN_OK) return st;
+    ProfScope prof(g, GNN_PROF_UPD_FWD, s);
+    if (use_tc) return launch_update_fwd_tc(Z, ld_z, nL, Kp, Wp, ldw, f_out, relu, H_out, ld_out, wt, g->err, s);
+    return launch_update_fwd(Z, ld_z, nL, Kp, Wp, ldw, f_out, relu, H_out, ld_out, dtype, s);
+}
+
+gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                              const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out, int relu,
+                              float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
+                              gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W || !dW) return GNN_EINVAL;
+    const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    const int64_t half = gnn_sage_half_offset(f_in, dtype);
+    const int64_t K = sage ? 2 * f_in : f_in;
+    const int64_t Kp = sage ? 2 * half : f_in;
+    const int64_t out_rows = want_halo_grad ? nT : nL;
+    if (!operand_ok(G, nL, ld_g, f_out, dtype) || !operand_ok(Z, nL, ld_z, Kp, dtype)) return GNN_EINVAL;
+    if (relu && !operand_ok(H_out, nL, ld_out, f_out, dtype)) return GNN_EINVAL;
+    if (dH && (!operand_ok(dH, out_rows, ld_dh, f_in, dtype) || !operand_ok(dZ, nL, ld_dz, Kp, dtype)))
+        return GNN_EINVAL;
+    if (f_in * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const size_t wp_bytes = align_up((size_t)Kp * ldw * sizeof(float));
+    const size_t dwp_bytes = sage ? align_up((size_t)Kp * f_out * sizeof(float)) : 0;
+    const size_t wg_bytes = align_up(update_bwd_ws_bytes(nL, Kp, f_out, dtype));
+    const size_t part_bytes = dH ? align_up(aggregate_partial_bytes(g->bwd, f_in)) : 0;
+    gnn_status st = ensure_workspace(g, wp_bytes + dwp_bytes + wg_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    char *base = static_cast<char *>(g->ws);
+    float *Wp = reinterpret_cast<float *>(base);
+    float *dWp = sage ? reinterpret_cast<float *>(base + wp_bytes) : dW;
+    float *wg = reinterpret_cast<float *>(base + wp_bytes + dwp_bytes);
+    float *partial = reinterpret_cast<float *>(base + wp_bytes + dwp_bytes + wg_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(Kp * ldw, 256), 256, 0, s>>>(W, K, f_out, f_in, half, sage, Kp, Wp, ldw,
+                                                                      dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    {
+        ProfScope prof(g, GNN_PROF_UPD_BWD, s);
+        st = launch_update_bwd(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp, dH ? dZ : nullptr,
+                               ld_dz, dtype, wg, wg_bytes, s);
+    }
+    if (st != GNN_OK) return st;
+    if (sage) {
+        { unpack_dw_kernel<<<(unsigned)ceil_div(K * f_out, 256), 256, 0, s>>>(dWp, f_out, f_in, half, dW); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+    }
+    if (!dH) return GNN_OK;
+    AggParams p{};
+    p.rowptr = g->rowptrT;
+    p.colidx = g->colidxT;
+    p.n_rows = out_rows;
+    p.f = f_in;
+    p.colw = g->colw;
+    p.out = dH;
+    p.ldo = ld_dh;
+    p.out_off = 0;
+    if (sage) {
+        p.mode = AGG_SAGE_BWD;
+        p.X = static_cast<const char *>(dZ) + half * elem_size(dtype);
+        p.ldx = ld_dz;
+        p.self = dZ;
+        p.ld_self = ld_dz;
+        p.n_self = nL;
+    } else {
+        p.mode = AGG_GCN;
+        p.X = dZ;
+        p.ldx = ld_dz;
+    }
+    ProfScope prof(g, GNN_PROF_AGG_BWD, s);
+    return launch_aggregate(p, g->bwd, dtype, partial, s);
+}
+
+gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
+                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || C <= 0 || !loss) return GNN_EINVAL;
+    if (n > 0 && (!logits || !labels || !G || !row_loss || ld < C || ld_g < C)) return GNN_EINVAL;
+    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, dtype, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// halo.cu - pull and push between the partition and its table of stale
+// representations (DIGEST page, system design, Fig. 1(c): pull H_out <- H~_out,
+// push H_in -> H~_in).  The pages note that rows are independent, so the I/O
+// parallelises at the granularity of a vertex; here a group of lanes moves one
+// row with 16-byte vector copies.  Both are bit-exact copies.
+#include <type_traits>
+
+#include "gnn_internal.cuh"
+
+namespace gnn {
+
+namespace {
+
+constexpr uint32_t kCountMask = 3u;  // low bits of a claim word: 0, 1 or 2 (= repeated)
+
+// copy bytes [0, nbytes) of one row; full 16-byte vectors then an element tail
+template <int LPR>
+__device__ __forceinline__ void copy_row(const char *__restrict__ src, char *__restrict__ dst, int64_t nbytes, int es,
+                                         int sub) {
+    const int64_t nvec = nbytes / 16;
+    for (int64_t q = sub; q < nvec; q += LPR)
+        reinterpret_cast<uint4 *>(dst)[q] = __ldg(reinterpret_cast<const uint4 *>(src) + q);
+    const int64_t tail0 = nvec * 16;
+    if (sub == 0) {
+        if (es == 4) {
+            for (int64_t b = tail0; b < nbytes; b += 4)
+                *reinterpret_cast<uint32_t *>(dst + b) = *reinterpret_cast<const uint32_t *>(src + b);
+        } else {
+            for (int64_t b = tail0; b < nbytes; b += 2)
+                *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
+        }
+    }
+}
+
+template <int LPR>
+__global__ void __launch_bounds__(256) pull_kernel(const char *__restrict__ table, int64_t row_bytes_t, int64_t n_table,
+                                                   const int64_t *__restrict__ ids, int64_t n_ids,
+                                                   char *__restrict__ H, int64_t row_bytes_h, int64_t row0,
+                                                   int64_t nbytes, int es, int *err) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = t / LPR;
+    const int sub = (int)(t % LPR);
+    if (i >= n_ids) return;
+    const int64_t id = __ldg(ids + i);
+    if (id < 0 || id >= n_table) {
+        if (sub == 0) atomicOr(err, 1);
+        return;
+    }
+    copy_row<LPR>(table + id * row_bytes_t, H + (row0 + i) * row_bytes_h, nbytes, es, sub);
+}
+
+// claim word = (generation << 2) | min(count, 2)
+__global__ void push_claim_kernel(const int64_t *__restrict__ ids, int64_t n, int64_t n_table, uint32_t *claim,
+                                  uint32_t gen, int *err) {
+    const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= n) return;
+    const int64_t id = ids[v];
+    if (id < 0 || id >= n_table) {
+        atomicOr(err, 1);
+        return;
+    }
+    uint32_t old = claim[id];
+    for (;;) {
+        uint32_t cnt = (old >> 2) == gen ? (old & kCountMask) : 0u;
+        uint32_t want = (gen << 2) | (cnt >= 2u ? 2u : cnt + 1u);
+        if (want == old) break;
+        uint32_t seen = atomicCAS(claim + id, old, want);
+        if (seen == old) break;
+        old = seen;
+    }
+}
+
+template <int LPR>
+__global__ void __launch_bounds__(256) push_copy_kernel(const char *__restrict__ H, int64_t row_bytes_h,
+                                                        const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
+                                                        const uint32_t *__restrict__ claim, uint32_t gen,
+                                                        char *__restrict__ table, int64_t row_bytes_t, int64_t nbytes,
+                                                        int es, int *err) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t v = t / LPR;
+    const int sub = (int)(t % LPR);
+    if (v >= n) return;
+    const int64_t id = __ldg(ids + v);
+    if (id < 0 || id >= n_table) return;  // reported by the claim pass
+    const uint32_t w = claim[id];
+    if (w != ((gen << 2) | 1u)) {
+        if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
+        return;
+    }
+    copy_row<LPR>(H + v * row_bytes_h, table + id * row_bytes_t, nbytes, es, sub);
+}
+
+int lanes_per_row(int64_t nbytes) {
+    int64_t nvec = ceil_div(nbytes, 16);
+    int l = 1;
+    while (l < 32 && l < nvec) l <<= 1;
+    return l;
+}
+
+template <typename F>
+gnn_status dispatch_lpr(int lpr, F &&f) {
+    switch (lpr) {
+        case 1: return f(std::integral_constant<int, 1>());
+        case 2: return f(std::integral_constant<int, 2>());
+        case 4: return f(std::integral_constant<int, 4>());
+        case 8: return f(std::integral_constant<int, 8>());
+        case 16: return f(std::integral_constant<int, 16>());
+        default: return f(std::integral_constant<int, 32>());
+    }
+}
+
+}  // namespace
+
+gnn_status launch_pull(const void *table, int64_t ld_t, int64_t n_table, const int64_t *ids, int64_t n_ids, void *H,
+                       int64_t ld_h, int64_t row0, int64_t f, int es, int *err, cudaStream_t s) {
+    if (n_ids == 0) return GNN_OK;
+    const int64_t nbytes = f * es;
+    const int lpr = lanes_per_row(nbytes);
+    return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
+        constexpr int LPR = decltype(L)::value;
+        const int64_t blocks = ceil_div(n_ids * LPR, 256);
+        { pull_kernel<LPR><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const char *>(table), ld_t * es, n_table, ids,
+                                                          n_ids, static_cast<char *>(H), ld_h * es, row0, nbytes, es,
+                                                          err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+gnn_status ensure_claim(gnn_graph *g, int64_t n_table) {
+    if (g->claim_n >= n_table) return GNN_OK;
+    // grow the claim array; ordered after earlier work on the device
+    GNN_CUDA_TRY(cudaDeviceSynchronize());
+    if (g->claim) GNN_CUDA_TRY(cudaFree(g->claim));
+    g->claim = nullptr;
+    g->claim_n = 0;
+    GNN_CUDA_TRY(cudaMalloc((void **)&g->claim, (size_t)n_table * sizeof(uint32_t)));
+    GNN_CUDA_TRY(cudaMemset(g->claim, 0, (size_t)n_table * sizeof(uint32_t)));
+    g->claim_n = n_table;
+    g->claim_gen = 0;
+    return GNN_OK;
+}
+
+gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
+                       void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    gnn_status st = ensure_claim(g, n_table);
+    if (st != GNN_OK) return st;
+    g->claim_gen += 1;
+    if (g->claim_gen >= (1u << 30)) {
+        GNN_CUDA_TRY(cudaMemsetAsync(g->claim, 0, (size_t)g->claim_n * sizeof(uint32_t), s));
+        g->claim_gen = 1;
+    }
+    const uint32_t gen = g->claim_gen;
+    { push_claim_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, s>>>(ids, n_rows, n_table, g->claim, gen, g->err); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    const int64_t nbytes = f * es;
+    const int lpr = lanes_per_row(nbytes);
+    return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
+        constexpr int LPR = decltype(L)::value;
+        const int64_t blocks = ceil_div(n_rows * LPR, 256);
+        { push_copy_kernel<LPR><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const char *>(H), ld_h * es, ids, n_rows,
+                                                               n_table, g->claim, gen, static_cast<char *>(table),
+                                                               ld_t * es, nbytes, es, g->err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+}  // namespace gnn

@@ -1,0 +1,240 @@
+"""Thin Python binding of libgnn (include/gnn.h): argument marshalling only.
+
+Every function here has the name of a C entry point without the ``gnn_`` prefix
+and forwards torch tensors as raw device pointers plus the current CUDA stream.
+All computation happens in the library's CUDA kernels; if ``libgnn.so`` cannot be
+loaded the import fails loudly (there is no fallback).
+
+Matrix arguments are 2-D CUDA tensors whose last dimension is contiguous; the
+leading dimension is ``tensor.stride(0)`` and the logical width is
+``tensor.shape[1]``, so a padded buffer is passed as a column slice
+(``buf[:, :f]``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgnn.so")
+
+GNN_OK, GNN_EINVAL, GNN_ENOMEM, GNN_ECUDA, GNN_EUNSUPPORTED, GNN_EINDEX = range(6)
+GNN_F32, GNN_BF16 = 0, 1
+GNN_AGG_GCN_SYM, GNN_AGG_SAGE_MEAN = 0, 1
+
+EXPORTS = (
+    "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
+    "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
+    "gnn_graph_copy_transpose", "gnn_status_string", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+)
+
+PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
+
+
+class GnnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().gnn_status_string(status).decode()} (status {status})")
+
+
+_L = None
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libgnn.so not built at {LIB_PATH}; run sparse_aggregation_dense_gb300/build.py")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.gnn_graph_create.argtypes = [vp, vp, i64, i64, i64, vp, i32, vp, ctypes.POINTER(vp)]
+        L.gnn_graph_destroy.argtypes = [vp]
+        L.gnn_halo_pull.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
+        L.gnn_halo_push.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
+        L.gnn_sage_half_offset.argtypes = [i64, i32]
+        L.gnn_sage_half_offset.restype = i64
+        L.gnn_layer_forward.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
+        L.gnn_layer_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp, i64, i32,
+                                         i32, vp]
+        L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, vp]
+        L.gnn_get_error.argtypes = [vp]
+        L.gnn_graph_sizes.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.gnn_graph_copy_transpose.argtypes = [vp, vp, vp, vp, vp]
+        L.gnn_profile_enable.argtypes = [vp, i32]
+        L.gnn_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
+        L.gnn_launch_count.argtypes = []
+        L.gnn_launch_count.restype = i64
+        L.gnn_status_string.argtypes = [i32]
+        L.gnn_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name not in ("gnn_sage_half_offset", "gnn_status_string", "gnn_launch_count"):
+                getattr(L, name).restype = i32
+        _L = L
+    return _L
+
+
+def _check(status: int, what: str):
+    if status != GNN_OK:
+        raise GnnError(status, what)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GNN_F32
+    if t.dtype == torch.bfloat16:
+        return GNN_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _mat(t: torch.Tensor) -> Tuple[int, int]:
+    """(ld, f) of a 2-D tensor with a contiguous last dimension."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("expected a 2-D tensor with contiguous rows")
+    return max(t.stride(0), t.shape[1]), t.shape[1]
+
+
+def agg_code(agg: str) -> int:
+    return {"gcn": GNN_AGG_GCN_SYM, "sage": GNN_AGG_SAGE_MEAN}[agg]
+
+
+class Graph:
+    """Owner of a ``gnn_graph*``; freed by :func:`graph_destroy` or on collection."""
+
+    def __init__(self, handle: int, n_local: int, n_halo: int, nnz: int, agg: str):
+        self.handle = handle
+        self.n_local, self.n_halo, self.nnz, self.agg = n_local, n_halo, nnz, agg
+
+    @property
+    def n_total(self) -> int:
+        return self.n_local + self.n_halo
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            try:
+                _lib().gnn_graph_destroy(ctypes.c_void_p(self.handle))
+            except Exception:
+                pass
+            self.handle = None
+
+
+def graph_create(rowptr: torch.Tensor, colidx: torch.Tensor, n_local: int, n_halo: int,
+                 deg: Optional[torch.Tensor] = None, agg: str = "gcn") -> Graph:
+    assert rowptr.dtype == torch.int32 and colidx.dtype == torch.int32
+    assert rowptr.numel() == n_local + 1
+    if deg is not None:
+        assert deg.dtype == torch.float32 and deg.numel() == n_local + n_halo
+    out = ctypes.c_void_p()
+    nnz = colidx.numel()
+    _check(_lib().gnn_graph_create(_ptr(rowptr), _ptr(colidx) if nnz else None, n_local, n_halo, nnz, _ptr(deg),
+                                   agg_code(agg), ctypes.c_void_p(_stream()), ctypes.byref(out)), "gnn_graph_create")
+    return Graph(out.value, n_local, n_halo, nnz, agg)
+
+
+def graph_destroy(g: Graph):
+    if g.handle:
+        h, g.handle = g.handle, None
+        _check(_lib().gnn_graph_destroy(ctypes.c_void_p(h)), "gnn_graph_destroy")
+
+
+def get_error(g: Graph) -> int:
+    """Synchronise; return (and clear) the graph's device error status."""
+    return int(_lib().gnn_get_error(ctypes.c_void_p(g.handle)))
+
+
+def graph_copy_transpose(g: Graph):
+    """Copies of the transpose (rowptrT, colidxT, permT) as int32 CUDA tensors."""
+    rT = torch.empty(g.n_total + 1, dtype=torch.int32, device="cuda")
+    cT = torch.empty(max(g.nnz, 1), dtype=torch.int32, device="cuda")
+    pT = torch.empty(max(g.nnz, 1), dtype=torch.int32, device="cuda")
+    _check(_lib().gnn_graph_copy_transpose(ctypes.c_void_p(g.handle), _ptr(rT), _ptr(cT), _ptr(pT),
+                                           ctypes.c_void_p(_stream())), "gnn_graph_copy_transpose")
+    return rT, cT[:g.nnz], pT[:g.nnz]
+
+
+def profile_enable(g: Graph, on: bool = True):
+    _check(_lib().gnn_profile_enable(ctypes.c_void_p(g.handle), int(on)), "gnn_profile_enable")
+
+
+def profile_read(g: Graph) -> dict:
+    """{kind: (total_ms, groups)} for the groups recorded since the last read."""
+    ms = (ctypes.c_double * len(PROF_KINDS))()
+    n = (ctypes.c_int64 * len(PROF_KINDS))()
+    _check(_lib().gnn_profile_read(ctypes.c_void_p(g.handle), ms, n), "gnn_profile_read")
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(PROF_KINDS)}
+
+
+def launch_count() -> int:
+    """Kernels launched by libgnn in this process so far."""
+    return int(_lib().gnn_launch_count())
+
+
+def sage_half_offset(f: int, dtype: torch.dtype) -> int:
+    return int(_lib().gnn_sage_half_offset(f, GNN_BF16 if dtype == torch.bfloat16 else GNN_F32))
+
+
+def halo_pull(g: Graph, table: torch.Tensor, halo_ids: torch.Tensor, H: torch.Tensor):
+    """H[n_local + i] = table[halo_ids[i]] over the columns of H's view."""
+    ld_t, _ = _mat(table)
+    ld_h, f = _mat(H)
+    assert halo_ids.dtype == torch.int64 and table.dtype == H.dtype
+    _check(_lib().gnn_halo_pull(ctypes.c_void_p(g.handle), _ptr(table), ld_t, table.shape[0], _ptr(halo_ids),
+                                _ptr(H), ld_h, f, _dtype(H), ctypes.c_void_p(_stream())), "gnn_halo_pull")
+
+
+def halo_push(g: Graph, H: torch.Tensor, local_ids: torch.Tensor, table: torch.Tensor):
+    """table[local_ids[v]] = H[v] over the columns of H's view (v < n_local)."""
+    ld_t, _ = _mat(table)
+    ld_h, f = _mat(H)
+    assert local_ids.dtype == torch.int64 and table.dtype == H.dtype
+    _check(_lib().gnn_halo_push(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(local_ids), _ptr(table), ld_t,
+                                table.shape[0], _dtype(H), ctypes.c_void_p(_stream())), "gnn_halo_push")
+
+
+def layer_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, Z: torch.Tensor, H_out: torch.Tensor):
+    """Z = A_block H (or the SAGE concat), H_out = act(Z W).  Widths from the views of H and H_out."""
+    ld_h, f_in = _mat(H)
+    ld_z, _ = _mat(Z)
+    ld_o, f_out = _mat(H_out)
+    assert W.dtype == torch.float32 and W.is_contiguous() and W.shape[1] == f_out
+    _check(_lib().gnn_layer_forward(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f_in, _ptr(W), f_out, int(relu),
+                                    _ptr(Z), ld_z, _ptr(H_out), ld_o, _dtype(H), ctypes.c_void_p(_stream())),
+           "gnn_layer_forward")
+
+
+def layer_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tensor, W: torch.Tensor, relu: bool,
+                   dW: torch.Tensor, f_in: int, dZ: Optional[torch.Tensor] = None, dH: Optional[torch.Tensor] = None,
+                   want_halo_grad: bool = False):
+    """dW = Z^T dY; with dH: dZ = dY W^T and dH = A_block^T dZ (halo rows too if want_halo_grad)."""
+    ld_g, f_out = _mat(G)
+    ld_o, _ = _mat(H_out)
+    ld_z, _ = _mat(Z)
+    ld_dz = _mat(dZ)[0] if dZ is not None else 0
+    ld_dh = _mat(dH)[0] if dH is not None else 0
+    assert dW.dtype == torch.float32 and dW.is_contiguous()
+    _check(_lib().gnn_layer_backward(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(Z), ld_z,
+                                     _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(dZ), ld_dz, _ptr(dH), ld_dh,
+                                     int(want_halo_grad), _dtype(G), ctypes.c_void_p(_stream())),
+           "gnn_layer_backward")
+
+
+def softmax_ce(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_loss: torch.Tensor,
+               loss: torch.Tensor):
+    ld, C = _mat(logits)
+    ld_g, _ = _mat(G)
+    _check(_lib().gnn_softmax_ce(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g, _ptr(row_loss),
+                                 _ptr(loss), _dtype(logits), ctypes.c_void_p(_stream())), "gnn_softmax_ce")

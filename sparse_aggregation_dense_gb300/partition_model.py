@@ -1,0 +1,124 @@
+"""One partition's L-layer GCN / GraphSAGE model driven through the C ABI.
+
+This module only allocates device buffers (torch) and issues the library's calls
+in the order of one full-graph training epoch on one partition:
+
+  for each layer l:   pull halo rows of layer l from the stale table (DIGEST pull)
+                      forward: aggregate + update (+ ReLU except the last layer)
+                      push the new local rows into the table of layer l + 1
+  loss gradient       softmax cross-entropy over the local rows
+  for l = L-1 .. 0:   backward: dW_l, and dH_l (local + halo rows) for l > 0
+
+No arithmetic happens here; every step runs in libgnn's CUDA kernels.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import gnn
+
+
+def ld_for(f: int, dtype: torch.dtype) -> int:
+    m = 8 if dtype == torch.bfloat16 else 4
+    return (f + m - 1) // m * m
+
+
+def padded(rows: int, f: int, dtype: torch.dtype, device, fill: Optional[float] = 0.0) -> torch.Tensor:
+    """A (rows x ld) buffer returned as its (rows x f) view."""
+    buf = torch.empty((rows, ld_for(f, dtype)), dtype=dtype, device=device)
+    if fill is not None:
+        buf.zero_()
+    return buf[:, :f]
+
+
+class PartitionModel:
+    """Device state of one partition and its L-layer model.
+
+    part: an object with rowptr, colidx (int32 numpy), n_local, n_halo, deg (float32 numpy or
+    None), local_ids, halo_ids (int64 numpy), n_table.
+    widths: [f_0, ..., f_L]; agg "gcn" | "sage"; dtype torch.float32 | torch.bfloat16.
+    """
+
+    def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda"):
+        self.widths = list(widths)
+        self.L = len(widths) - 1
+        self.agg = agg
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.n_local, self.n_halo, self.n_table = part.n_local, part.n_halo, part.n_table
+        dev = self.device
+        self.rowptr = torch.from_numpy(np.ascontiguousarray(part.rowptr)).to(dev)
+        self.colidx = torch.from_numpy(np.ascontiguousarray(part.colidx)).to(dev)
+        self.deg = None if part.deg is None else torch.from_numpy(np.ascontiguousarray(part.deg)).to(dev)
+        self.local_ids = torch.from_numpy(np.ascontiguousarray(part.local_ids)).to(dev)
+        self.halo_ids = torch.from_numpy(np.ascontiguousarray(part.halo_ids)).to(dev)
+        self.graph = gnn.graph_create(self.rowptr, self.colidx, self.n_local, self.n_halo, self.deg, agg)
+        nL, nT = self.n_local, self.n_local + self.n_halo
+        self.nnz = int(part.colidx.shape[0])
+        sage = agg == "sage"
+        self.Kp = [2 * gnn.sage_half_offset(f, dtype) if sage else f for f in widths[:-1]]
+        # layer inputs H[l] (local + halo rows); the local rows of H[l+1] are layer l's output
+        self.H = [padded(nT, widths[l], dtype, dev) for l in range(self.L)]
+        self.out_last = padded(nL, widths[-1], dtype, dev)
+        self.Z = [padded(nL, self.Kp[l], dtype, dev) for l in range(self.L)]
+        self.dZ = padded(nL, max(self.Kp[1:] + [1]), dtype, dev)
+        self.dH = [None] + [padded(nT, widths[l], dtype, dev) for l in range(1, self.L)]
+        self.G_last = padded(nL, widths[-1], dtype, dev)
+        self.W: List[torch.Tensor] = []
+        self.dW: List[torch.Tensor] = []
+        for l in range(self.L):
+            K = (2 if sage else 1) * widths[l]
+            self.W.append(torch.zeros((K, widths[l + 1]), dtype=torch.float32, device=dev))
+            self.dW.append(torch.zeros((K, widths[l + 1]), dtype=torch.float32, device=dev))
+        self.tables: List[Optional[torch.Tensor]] = [None] * self.L
+        self.labels = torch.zeros(nL, dtype=torch.int32, device=dev)
+        self.row_loss = torch.zeros(max(nL, 1), dtype=torch.float32, device=dev)
+        self.loss = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    # ---- views ------------------------------------------------------------
+    def layer_out(self, l: int) -> torch.Tensor:
+        """Output of layer l (n_local x f_{l+1})."""
+        return self.out_last if l == self.L - 1 else self.H[l + 1][:self.n_local]
+
+    def grad_out(self, l: int) -> torch.Tensor:
+        """Gradient with respect to the output of layer l."""
+        return self.G_last if l == self.L - 1 else self.dH[l + 1][:self.n_local]
+
+    def dZ_view(self, l: int) -> torch.Tensor:
+        return self.dZ[:, :self.Kp[l]]
+
+    # ---- one epoch --------------------------------------------------------
+    def forward(self):
+        for l in range(self.L):
+            if self.n_halo:
+                gnn.halo_pull(self.graph, self.tables[l], self.halo_ids, self.H[l])
+            gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
+            if l + 1 < self.L:
+                gnn.halo_push(self.graph, self.layer_out(l), self.local_ids, self.tables[l + 1])
+
+    def loss_grad(self):
+        gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)
+
+    def backward(self, want_halo_grad: bool = True):
+        for l in reversed(range(self.L)):
+            if l > 0:
+                gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
+                                   l < self.L - 1, self.dW[l], self.widths[l], dZ=self.dZ_view(l),
+                                   dH=self.dH[l] if want_halo_grad else self.dH[l][:self.n_local],
+                                   want_halo_grad=want_halo_grad)
+            else:
+                gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
+                                   l < self.L - 1, self.dW[l], self.widths[l])
+
+    def step(self):
+        self.forward()
+        self.loss_grad()
+        self.backward()
+
+    def check_errors(self):
+        st = gnn.get_error(self.graph)
+        if st != gnn.GNN_OK:
+            raise gnn.GnnError(st, "device error word")

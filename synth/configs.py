@@ -83,4 +83,13 @@ TINY = {
                         lambda seed: synth.rmat_block_partition(14, 1 << 13, 1 << 12, 1.2e5, seed, RMAT)),
 }
 
+# a quarter-scale instance of the R-MAT partition for detailed profiling (inputs
+# still far larger than L2, a few GB on the device)
+PROFILE = {
+    "rmat4m": Workload(
+        "rmat4m", "3-layer GCN, R-MAT scale-22 partition: 2,097,152 local + 1,048,576 halo, ~100M entries",
+        "gcn", "bf16", [128, 256, 256, 172], "normal",
+        lambda seed: synth.rmat_block_partition(22, 1 << 21, 1 << 20, RMAT_BLOCK_SAMPLES / 4, seed, RMAT)),
+}
+
 BENCH_WORKLOAD = "rmat16m"

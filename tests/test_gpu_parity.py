@@ -1,0 +1,484 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Index work (transpose, pull, push) must match bit for bit; floating point must
+satisfy |x - r| <= tol * (|r| + rms(r)) with tol 1e-4 (fp32) or 2e-2 (bf16
+storage, fp32 accumulation).  Small workloads are compared on every row; the
+full-size ones on sampled rows (random rows plus the heaviest rows and rows just
+past the heavy-row split), which the oracle computes one by one, and the
+transpose at full size through properties that fix it uniquely.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.configs import TINY, WORKLOADS
+from sparse_aggregation_dense_gb300 import PartitionModel, gnn, ld_for, padded
+from tests._gpu import (TOL, close, close_mostly, column_subset, gen_matrix, maybe_round, sample_with_heavy, to_device, to_host,
+                        torch_dtype, widen)
+
+pytestmark = pytest.mark.gpu
+
+SMALL_FULL = ["er5k", "rmat131k"]
+BIG_FULL = ["powerlaw233k", "sage2m", "rmat16m"]
+ALL = list(WORKLOADS)
+SEED = 0
+
+_cache = {}
+
+
+def problem(name: str, size: str):
+    """(workload, partition, graph) with the graph built once per session."""
+    key = (name, size)
+    if key not in _cache:
+        w = (TINY if size == "tiny" else WORKLOADS)[name]
+        part = w.make(SEED)
+        rp = torch.from_numpy(part.rowptr).cuda()
+        ci = torch.from_numpy(part.colidx).cuda()
+        deg = None if part.deg is None else torch.from_numpy(part.deg).cuda()
+        g = gnn.graph_create(rp, ci, part.n_local, part.n_halo, deg, w.agg)
+        _cache[key] = (w, part, g)
+    return _cache[key]
+
+
+def is_sampled(size: str, name: str) -> bool:
+    return size == "full" and name in BIG_FULL
+
+
+CASES = [(n, "tiny") for n in ALL] + [(n, "full") for n in ALL]
+
+
+def case_id(c):
+    return f"{c[0]}-{c[1]}"
+
+
+# ---------------------------------------------------------------------------
+# transpose (bit-exact)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", CASES, ids=case_id)
+def test_transpose_bit_exact(case):
+    name, size = case
+    w, part, g = problem(name, size)
+    rT, cT, pT = (t.cpu().numpy() for t in gnn.graph_copy_transpose(g))
+    if not is_sampled(size, name):
+        orT, ocT, opT = oracle.transpose(part)
+        np.testing.assert_array_equal(rT, orT)
+        np.testing.assert_array_equal(cT, ocT)
+        np.testing.assert_array_equal(pT, opT)
+        return
+    # full size: properties that determine the stable transpose uniquely
+    nT = part.n_total
+    cnt = np.bincount(part.colidx, minlength=nT)
+    np.testing.assert_array_equal(rT, np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32))
+    assert np.all(np.bincount(pT, minlength=part.nnz) == 1)  # a permutation of the entries
+    row_of = np.repeat(np.arange(part.n_local, dtype=np.int32), np.diff(part.rowptr))
+    np.testing.assert_array_equal(cT, row_of[pT])  # entry k came from row colidxT[k]
+    trow = np.repeat(np.arange(nT, dtype=np.int32), cnt)
+    np.testing.assert_array_equal(part.colidx[pT], trow)  # ... and carries column (transpose row) of k
+    same_row = trow[1:] == trow[:-1]
+    assert np.all(cT[1:][same_row] > cT[:-1][same_row])  # ascending source rows within a transpose row
+
+
+# ---------------------------------------------------------------------------
+# pull / push (bit-exact)
+# ---------------------------------------------------------------------------
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy()
+    return t.contiguous().view(torch.int32).cpu().numpy()
+
+
+@pytest.mark.parametrize("case", CASES, ids=case_id)
+def test_pull_push_bit_exact(case):
+    name, size = case
+    w, part, g = problem(name, size)
+    dt = w.dtype
+    f = w.widths[0]
+    tdt = torch_dtype(dt)
+    table_h = gen_matrix(part.n_table, f, dt, SEED, synth.STREAM_FEATURES, w.feat_dist)
+    table = to_device(table_h, dt, f)
+    H = padded(part.n_total, f, tdt, "cuda")
+    gnn.halo_pull(g, table, torch.from_numpy(part.halo_ids).cuda(), H)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    H_ref = np.zeros((part.n_total, table_h.shape[1]), dtype=table_h.dtype)
+    assert oracle.halo_pull(table_h, part.halo_ids, H_ref, part.n_local, f) == oracle.OK
+    np.testing.assert_array_equal(_bits(H[part.n_local:]), H_ref[part.n_local:, :f].view(
+        np.int16 if dt == "bf16" else np.int32))
+    # push fresh local rows into the table
+    out_h = gen_matrix(part.n_local, f, dt, SEED, 77, "normal")
+    out = to_device(out_h, dt, f)
+    gnn.halo_push(g, out, torch.from_numpy(part.local_ids).cuda(), table)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    ref = table_h.copy()
+    assert oracle.halo_push(out_h, part.n_local, f, part.local_ids, ref) == oracle.OK
+    np.testing.assert_array_equal(_bits(table), ref[:, :f].view(np.int16 if dt == "bf16" else np.int32))
+
+
+# ---------------------------------------------------------------------------
+# forward layer
+# ---------------------------------------------------------------------------
+
+FWD_CASES = [(n, s, l) for (n, s) in CASES for l in range(WORKLOADS[n].layers)
+             if not (s == "full" and n in BIG_FULL and l != 1)]
+
+
+@pytest.mark.parametrize("case", FWD_CASES, ids=lambda c: f"{c[0]}-{c[1]}-L{c[2]}")
+def test_forward_layer(case):
+    name, size, l = case
+    w, part, g = problem(name, size)
+    dt, agg = w.dtype, w.agg
+    tdt = torch_dtype(dt)
+    f_in, f_out = w.widths[l], w.widths[l + 1]
+    relu = l < w.layers - 1
+    sage = agg == "sage"
+    K = 2 * f_in if sage else f_in
+    half = gnn.sage_half_offset(f_in, tdt)
+    Kp = 2 * half if sage else f_in
+    H_h = gen_matrix(part.n_total, f_in, dt, SEED, 100 + l)
+    W = synth.glorot(K, f_out, SEED, synth.STREAM_WEIGHT + l)
+    H = to_device(H_h, dt, f_in)
+    Z = padded(part.n_local, Kp, tdt, "cuda", fill=None)
+    Z.as_strided((part.n_local, Z.stride(0)), (Z.stride(0), 1)).fill_(7.0)  # padding must come back zero
+    Hout = padded(part.n_local, f_out, tdt, "cuda")
+    gnn.layer_forward(g, H, torch.from_numpy(W).cuda(), relu, Z, Hout)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    if is_sampled(size, name):
+        rows = sample_with_heavy(part.rowptr, 1500, SEED)
+        cols, cmap = column_subset(part.rowptr, part.colidx, rows, part.n_total)
+        cols = np.union1d(cols, rows)
+        cmap = -np.ones(part.n_total, np.int64)
+        cmap[cols] = np.arange(cols.shape[0])
+        Hsub = oracle.widen(gen_matrix(0, f_in, dt, SEED, 100 + l, ids=cols)[:, :f_in], dt == "bf16")
+        hmap = cmap
+    else:
+        rows = np.arange(part.n_local, dtype=np.int64)
+        Hsub = widen(H_h, dt, f_in)
+        hmap = None
+    wts = oracle.gcn_dinv(part) if not sage else oracle.sage_invcnt(part)
+    Zr = oracle.aggregate(part, Hsub, f_in, agg, rows=rows, hmap=hmap, weights=wts)
+    Zr = maybe_round(Zr, dt)
+    Hr = oracle.update(Zr, maybe_round(W.astype(np.float64), dt), relu)
+    rows_t = torch.from_numpy(rows).cuda()
+    Zg = to_host(Z.index_select(0, rows_t))
+    Hg = to_host(Hout.index_select(0, rows_t))
+    tol = TOL[dt]
+    if sage:
+        close(Zg[:, :f_in], Zr[:, :f_in], 0.0, "Z self half (a copy)")
+        close(Zg[:, half:half + f_in], Zr[:, f_in:], tol, "Z mean half")
+        assert np.all(Zg[:, f_in:half] == 0) and np.all(Zg[:, half + f_in:] == 0)
+    else:
+        close(Zg, Zr, tol, "Z")
+    close(Hg, Hr, tol, "H_out")
+    # padding columns of the written rows (up to the 16-byte boundary) are zero
+    ldz = Z.stride(0)
+    buf = Z.as_strided((part.n_local, ldz), (ldz, 1)).index_select(0, rows_t).float().cpu().numpy()
+    assert np.all(buf[:, (2 * half if sage else f_in):] == 0)
+
+
+# ---------------------------------------------------------------------------
+# backward layer
+# ---------------------------------------------------------------------------
+
+BWD_CASES = [(n, s, l) for (n, s) in CASES for l in range(WORKLOADS[n].layers)
+             if not (s == "full" and n in BIG_FULL and l != 1)]
+
+
+def _z_input(part, f_in, dt, sage, half, Kp, l):
+    """Saved-aggregation input in the library's layout and in the oracle's compact layout."""
+    tdt = torch_dtype(dt)
+    ld = ld_for(Kp, tdt)
+    a = gen_matrix(part.n_local, f_in, dt, SEED, 400 + l)
+    if not sage:
+        return a, widen(a, dt, f_in)
+    b = gen_matrix(part.n_local, f_in, dt, SEED, 500 + l)
+    z = np.zeros((part.n_local, ld), dtype=a.dtype)
+    z[:, :f_in] = a[:, :f_in]
+    z[:, half:half + f_in] = b[:, :f_in]
+    compact = np.concatenate([widen(a, dt, f_in), widen(b, dt, f_in)], axis=1)
+    return z, compact
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"{c[0]}-{c[1]}-L{c[2]}")
+def test_backward_layer(case):
+    name, size, l = case
+    w, part, g = problem(name, size)
+    dt, agg = w.dtype, w.agg
+    tdt = torch_dtype(dt)
+    f_in, f_out = w.widths[l], w.widths[l + 1]
+    relu = l < w.layers - 1
+    sage = agg == "sage"
+    K = 2 * f_in if sage else f_in
+    half = gnn.sage_half_offset(f_in, tdt)
+    Kp = 2 * half if sage else f_in
+    nL, nT = part.n_local, part.n_total
+    G_h = gen_matrix(nL, f_out, dt, SEED, 200 + l)
+    Ho_h = gen_matrix(nL, f_out, dt, SEED, 300 + l)
+    Z_h, Z_c = _z_input(part, f_in, dt, sage, half, Kp, l)
+    W = synth.glorot(K, f_out, SEED, synth.STREAM_WEIGHT + l)
+    G = to_device(G_h, dt, f_out)
+    Ho = to_device(Ho_h, dt, f_out)
+    Z = to_device(Z_h, dt, Kp)
+    dW = torch.zeros((K, f_out), dtype=torch.float32, device="cuda")
+    dZ = padded(nL, Kp, tdt, "cuda")
+    dH = padded(nT, f_in, tdt, "cuda")
+    gnn.layer_backward(g, G, Ho, Z, torch.from_numpy(W).cuda(), relu, dW, f_in, dZ=dZ, dH=dH, want_halo_grad=True)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    tol = TOL[dt]
+    Wr = maybe_round(W.astype(np.float64), dt)
+    Gw, How = widen(G_h, dt, f_out), widen(Ho_h, dt, f_out)
+    dWg = dW.cpu().numpy()
+    sampled = is_sampled(size, name)
+    if sampled:
+        rng = np.random.default_rng(l)
+        ent = [(int(rng.integers(K)), int(rng.integers(f_out))) for _ in range(16)] + [(0, 0), (K - 1, f_out - 1)]
+        ref = oracle.update_backward_dw_entries(Gw, How, Z_c, relu, ent)
+        close(np.array([dWg[k, j] for k, j in ent]), ref, tol, "dW entries")
+    else:
+        dWr, _ = oracle.update_backward(Gw, How, Z_c, W.astype(np.float64), relu, want_dz=False)
+        close(dWg, dWr, tol, "dW")
+    # dH on output rows U (random local + halo rows and the heaviest transpose rows)
+    if sampled:
+        rowptrT = np.concatenate([[0], np.cumsum(np.bincount(part.colidx, minlength=nT))])
+        U = sample_with_heavy(rowptrT, 600, SEED + 1)
+        sel = np.zeros(nT, bool)
+        sel[U] = True
+        keep = sel[part.colidx]
+        cnt = np.zeros(nL, np.int64)
+        row_of = np.repeat(np.arange(nL), np.diff(part.rowptr))
+        np.add.at(cnt, row_of[keep], 1)
+        sub_rowptr = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        sub = synth.Partition(sub_rowptr, part.colidx[keep], nL, part.n_halo, part.deg, part.local_ids,
+                              part.halo_ids, part.n_table)
+        T = oracle.transpose(sub)
+        V = np.unique(T[1]).astype(np.int64)
+    else:
+        U = np.arange(nT, dtype=np.int64)
+        T = oracle.transpose(part)
+        V = np.arange(nL, dtype=np.int64)
+    vmap = -np.ones(nL, np.int64)
+    vmap[V] = np.arange(V.shape[0])
+    _, dZr = oracle.update_backward(Gw[V], How[V], Z_c[V], Wr, relu, want_dz=True)
+    dZr = maybe_round(dZr, dt)
+    wts = oracle.gcn_dinv(part) if not sage else oracle.sage_invcnt(part)
+    dHr = oracle.aggregate_backward(part, T, dZr, f_in, agg, rows=U, dmap=vmap, weights=wts)
+    dHg = to_host(dH.index_select(0, torch.from_numpy(U).cuda()))
+    close(dHg, dHr, tol, "dH")
+    # the intermediate dZ rows as well (compact layout)
+    dZg = to_host(dZ.index_select(0, torch.from_numpy(V[:2000]).cuda()))
+    dZr_rows = dZr[:min(2000, V.shape[0])]
+    if sage:
+        close(dZg[:, :f_in], dZr_rows[:, :f_in], tol, "dZ self")
+        close(dZg[:, half:half + f_in], dZr_rows[:, f_in:], tol, "dZ mean")
+    else:
+        close(dZg, dZr_rows, tol, "dZ")
+
+
+# ---------------------------------------------------------------------------
+# whole epoch: pulls, forwards, pushes, loss, backwards with halo gradients
+# ---------------------------------------------------------------------------
+
+EPOCH_CASES = [(n, "tiny") for n in ALL] + [(n, "full") for n in SMALL_FULL]
+
+
+def _load_model(w, part):
+    dt = w.dtype
+    tdt = torch_dtype(dt)
+    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda")
+    tables_h = []
+    for l in range(w.layers):
+        stream = synth.STREAM_FEATURES if l == 0 else synth.STREAM_TABLE + l
+        t = gen_matrix(part.n_table, w.widths[l], dt, SEED, stream, w.feat_dist if l == 0 else "normal")
+        tables_h.append(t)
+        m.tables[l] = to_device(t, dt, w.widths[l])
+    m.H[0][:part.n_local] = m.tables[0][torch.from_numpy(part.local_ids).cuda()]
+    Ws = []
+    for l in range(w.layers):
+        K = (2 if w.agg == "sage" else 1) * w.widths[l]
+        Ws.append(synth.glorot(K, w.widths[l + 1], SEED, synth.STREAM_WEIGHT + l))
+        m.W[l].copy_(torch.from_numpy(Ws[l]))
+    y = synth.labels(part.n_local, w.widths[-1], SEED, ids=part.local_ids)
+    m.labels.copy_(torch.from_numpy(y))
+    return m, tables_h, Ws, y
+
+
+@pytest.mark.parametrize("case", EPOCH_CASES, ids=case_id)
+def test_epoch(case):
+    name, size = case
+    w, part, _ = problem(name, size)
+    dt = w.dtype
+    m, tables_h, Ws, y = _load_model(w, part)
+    m.step()
+    m.check_errors()
+    bf = dt == "bf16"
+    ref = oracle.epoch(part, [widen(t, dt, f) for t, f in zip(tables_h, w.widths)],
+                       [maybe_round(x.astype(np.float64), dt) for x in Ws], y, w.agg, bf16=bf)
+    tol = TOL[dt]
+    # fp32: every element within tolerance.  bf16: the chained layers may flip a
+    # few ReLU mask decisions (see close_mostly); the per-layer tests are exact.
+    chk = close if not bf else close_mostly
+    chk(to_host(m.out_last), ref["Hout"][-1], tol, "logits")
+    assert abs(float(m.loss.item()) - ref["loss"]) <= tol * abs(ref["loss"])
+    for l in range(w.layers):
+        chk(m.dW[l].cpu().numpy(), ref["dW"][l], tol, f"dW[{l}]")
+    for l in range(1, w.layers):
+        chk(to_host(m.dH[l]), ref["dH"][l], tol, f"dH[{l}] (local + halo)")
+        pushed = to_host(m.tables[l].index_select(0, torch.from_numpy(part.local_ids).cuda()))
+        chk(pushed, ref["Hout"][l - 1], tol, f"pushed table {l}")
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def _custom_graph(rows, n_halo, agg="gcn", deg=None):
+    """Graph from a list of column lists (rows of the block)."""
+    rowptr = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    colidx = np.array([c for r in rows for c in r], dtype=np.int32)
+    n_local = len(rows)
+    part = synth.Partition(rowptr, colidx, n_local, n_halo, deg, np.arange(n_local, dtype=np.int64),
+                           np.arange(n_local, n_local + n_halo, dtype=np.int64), n_local + n_halo)
+    g = gnn.graph_create(torch.from_numpy(rowptr).cuda(), torch.from_numpy(colidx).cuda(), n_local, n_halo,
+                         None if deg is None else torch.from_numpy(deg).cuda(), agg)
+    return part, g
+
+
+def _run_layer_pair(part, g, agg, dt, f_in, f_out, relu, seed=3):
+    """Forward + backward on generator inputs; compare every row with the oracle."""
+    tdt = torch_dtype(dt)
+    sage = agg == "sage"
+    K = 2 * f_in if sage else f_in
+    half = gnn.sage_half_offset(f_in, tdt)
+    Kp = 2 * half if sage else f_in
+    nL, nT = part.n_local, part.n_total
+    H_h = gen_matrix(nT, f_in, dt, seed, 1)
+    W = synth.glorot(K, f_out, seed, 2)
+    Z = padded(nL, Kp, tdt, "cuda")
+    Ho = padded(nL, f_out, tdt, "cuda")
+    Wd = torch.from_numpy(W).cuda()
+    gnn.layer_forward(g, to_device(H_h, dt, f_in), Wd, relu, Z, Ho)
+    tol = TOL[dt]
+    Zr = maybe_round(oracle.aggregate(part, widen(H_h, dt, f_in), f_in, agg), dt)
+    Hr = oracle.update(Zr, maybe_round(W.astype(np.float64), dt), relu)
+    Zg = to_host(Z)
+    if sage:
+        close(Zg[:, :f_in], Zr[:, :f_in], tol, "Z self")
+        close(Zg[:, half:half + f_in], Zr[:, f_in:], tol, "Z mean")
+    else:
+        close(Zg, Zr, tol, "Z")
+    close(to_host(Ho), Hr, tol, "H_out")
+    G_h = gen_matrix(nL, f_out, dt, seed, 4)
+    dW = torch.zeros((K, f_out), dtype=torch.float32, device="cuda")
+    dZ = padded(nL, Kp, tdt, "cuda")
+    dH = padded(nT, f_in, tdt, "cuda")
+    gnn.layer_backward(g, to_device(G_h, dt, f_out), Ho, Z, Wd, relu, dW, f_in, dZ=dZ, dH=dH, want_halo_grad=True)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    Zc = np.concatenate([Zg[:, :f_in], Zg[:, half:half + f_in]], axis=1) if sage else Zg
+    dWr, dZr = oracle.update_backward(widen(G_h, dt, f_out), to_host(Ho), Zc, maybe_round(W.astype(np.float64), dt),
+                                      relu)
+    close(dW.cpu().numpy(), dWr, tol, "dW")
+    dHr = oracle.aggregate_backward(part, oracle.transpose(part), maybe_round(dZr, dt), f_in, agg)
+    close(to_host(dH), dHr, tol, "dH")
+    return Z, Ho, dW, dH
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("agg", ["gcn", "sage"])
+@pytest.mark.parametrize("f_in,f_out", [(1, 3), (5, 41), (47, 172), (100, 47), (602, 41), (256, 256)])
+def test_ragged_widths(dt, agg, f_in, f_out):
+    part = synth.chunglu_partition(1500, 12000, 16.0, 3, seed=5)
+    g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(), part.n_local,
+                         part.n_halo, torch.from_numpy(part.deg).cuda(), agg)
+    _run_layer_pair(part, g, agg, dt, f_in, f_out, relu=True)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("agg", ["gcn", "sage"])
+def test_heavy_rows_and_columns(dt, agg):
+    # one hub row with 3000 entries (several chunks and a partial one) and one hub
+    # column referenced by 2500 rows; rows of exactly 512 and 513 entries
+    rng = np.random.default_rng(11)
+    nL, nH = 3000, 700
+    nT = nL + nH
+    hub = nL + 5
+    sizes = {7: 2999, 11: 511, 13: 512}  # entries besides the self loop
+    rows = []
+    for v in range(nL):
+        pool = np.setdiff1d(np.arange(nT), [v, hub])
+        if v in sizes:
+            cols = set(rng.choice(pool, sizes[v], replace=False).tolist())
+        else:
+            cols = set(rng.choice(pool, int(rng.integers(0, 12)), replace=False).tolist())
+            if v < 2500:
+                cols.add(hub)  # hub halo column: a heavy transpose row
+        rows.append(sorted(cols | {v}))
+    part, g = _custom_graph(rows, nH, agg)
+    deg = np.diff(part.rowptr)
+    assert deg[7] == 3000 and deg[11] == 512 and deg[13] == 513
+    assert np.sum(part.colidx == hub) > 2000
+    a = _run_layer_pair(part, g, agg, dt, 96, 40, relu=True)
+    b = _run_layer_pair(part, g, agg, dt, 96, 40, relu=True)
+    for x, y in zip(a, b):  # bitwise reproducible
+        assert torch.equal(x, y)
+
+
+def test_no_halo_empty_rows_and_single_row():
+    # no halo, a row with no entries at all (no self loop), a row with only itself
+    rows = [[0, 1], [], [2], [0, 1, 3], [3, 4]]
+    deg = np.array([3, 2, 1, 2, 2], dtype=np.float32)
+    part, g = _custom_graph(rows, 0, "gcn", deg)
+    Z, Ho, dW, dH = _run_layer_pair(part, g, "gcn", "f32", 8, 4, relu=False)
+    assert float(Z[1].abs().max()) == 0.0
+    part1, g1 = _custom_graph([[0, 1]], 1, "gcn")
+    _run_layer_pair(part1, g1, "gcn", "f32", 16, 8, relu=True)
+    part2, g2 = _custom_graph([[0, 1]], 1, "sage")
+    _run_layer_pair(part2, g2, "sage", "bf16", 16, 8, relu=True)
+
+
+def test_bad_ids_are_reported_and_rows_left_alone():
+    part = synth.er_partition(300, 200, 0.05, seed=1)
+    g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(), part.n_local,
+                         part.n_halo, torch.from_numpy(part.deg).cuda(), "gcn")
+    f = 12
+    table_h = gen_matrix(part.n_table, f, "f32", 0, 1)
+    table = to_device(table_h, "f32", f)
+    ids = part.halo_ids.copy()
+    ids[5] = part.n_table  # out of range
+    ids[6] = -1
+    H = padded(part.n_total, f, torch.float32, "cuda")
+    H.fill_(-3.0)
+    gnn.halo_pull(g, table, torch.from_numpy(ids).cuda(), H)
+    assert gnn.get_error(g) == gnn.GNN_EINDEX
+    assert gnn.get_error(g) == gnn.GNN_OK  # cleared
+    Hh = H.cpu().numpy()
+    assert np.all(Hh[part.n_local + 5] == -3.0) and np.all(Hh[part.n_local + 6] == -3.0)
+    good = [i for i in range(part.n_halo) if i not in (5, 6)]
+    np.testing.assert_array_equal(Hh[part.n_local + np.array(good)], table_h[ids[good], :f])
+    # push with a repeated id: neither copy is written, the others are
+    lids = part.local_ids.copy()
+    lids[9] = lids[3]
+    before = table.cpu().numpy().copy()
+    out_h = gen_matrix(part.n_local, f, "f32", 0, 9)
+    gnn.halo_push(g, to_device(out_h, "f32", f), torch.from_numpy(lids).cuda(), table)
+    assert gnn.get_error(g) == gnn.GNN_EINDEX
+    after = table.cpu().numpy()
+    np.testing.assert_array_equal(after[lids[3]], before[lids[3]])
+    ok = [v for v in range(part.n_local) if v not in (3, 9)]
+    np.testing.assert_array_equal(after[lids[ok]], out_h[ok, :f])
+    # a second, clean push after the failed one works (claim generations advance)
+    gnn.halo_push(g, to_device(out_h, "f32", f), torch.from_numpy(part.local_ids).cuda(), table)
+    assert gnn.get_error(g) == gnn.GNN_OK
+    np.testing.assert_array_equal(table.cpu().numpy()[part.local_ids], out_h[:, :f])
+
+
+def test_bad_csr_is_rejected():
+    rowptr = torch.tensor([0, 2, 3], dtype=torch.int32, device="cuda")
+    colidx = torch.tensor([0, 5, 1], dtype=torch.int32, device="cuda")  # 5 >= n_local + n_halo = 4
+    with pytest.raises(gnn.GnnError) as e:
+        gnn.graph_create(rowptr, colidx, 2, 2, None, "gcn")
+    assert e.value.status == gnn.GNN_EINDEX
+    rowptr2 = torch.tensor([0, 3, 2], dtype=torch.int32, device="cuda")  # not monotone
+    with pytest.raises(gnn.GnnError):
+        gnn.graph_create(rowptr2, colidx[:2], 2, 2, None, "gcn")
