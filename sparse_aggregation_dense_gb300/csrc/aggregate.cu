@@ -8,16 +8,22 @@
 // Backward over the transpose CSR (A^T kept explicitly, CAGNET GNN section):
 //   GCN:  dH[u] = dinv[u] * sum_{v in rowT u} dinv[v] * dZ[v]
 //   SAGE: dH[u] = [u local] dZ_self[u] + sum_{v in rowT u, v != u} inv_cnt[v] * dZ_mean[v]
+// The column factors live in per-entry weights built with the graph, so the
+// kernel streams (column id, weight) pairs and gathers feature rows.
 //
-// Design (HBM-bound gather): one warp per work item.  An item is a whole light
-// row (<= kHeavyNnz entries) or one kChunkNnz-entry chunk of a heavy row;
-// chunks are scheduled first so hub rows spread over all SMs.  Lanes of a warp
-// split the feature row into 16-byte vectors; a warp handles 32 / LPG entries
-// at once (LPG lanes per entry) and keeps U entries' loads in flight.  Column
-// ids and weights are loaded 32 at a time, coalesced, and broadcast by
-// shuffles.  Accumulation is fp32.  A chunk writes an fp32 partial; a fix-up
-// pass adds a heavy row's partials in chunk order, so the result does not
-// depend on scheduling (no atomics).
+// Design (a gather bound by memory latency and DRAM traffic):
+//  - one warp per work item: a whole light row (<= kHeavyNnz entries) or one
+//    kChunkNnz-entry chunk of a heavy row; chunks are scheduled first so hub
+//    rows spread over all SMs; a chunk writes an fp32 partial and a fix-up adds
+//    a heavy row's partials in chunk order (deterministic, no atomics);
+//  - lanes split a feature row into 16-byte vectors; LPG lanes serve one entry
+//    and the warp serves 32 / LPG entries at once;
+//  - the gathers are software-pipelined: U loads per lane group are always in
+//    flight - each slot is consumed and immediately refilled with the entry U
+//    slots ahead - and the next 32 column ids are loaded one batch ahead;
+//  - L2 residency: column ids carry a hotness tier (access-count rank); rows
+//    of the hottest tiers that fit a share of L2 are loaded with an evict_last
+//    policy, the rest and the streamed ids / weights / outputs with evict_first.
 #include "gnn_internal.cuh"
 
 namespace gnn {
@@ -46,16 +52,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// store EPV consecutive values (16 bytes) with columns >= f_left zeroed
-__device__ __forceinline__ void store16(float *dst, const float *v, int f_left) {
-    float4 o;
-    o.x = 0 < f_left ? v[0] : 0.f;
-    o.y = 1 < f_left ? v[1] : 0.f;
-    o.z = 2 < f_left ? v[2] : 0.f;
-    o.w = 3 < f_left ? v[3] : 0.f;
-    *reinterpret_cast<float4 *>(dst) = o;
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
-__device__ __forceinline__ void store16(__nv_bfloat16 *dst, const float *v, int f_left) {
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// read-only 16-byte load with an L2 eviction policy
+__device__ __forceinline__ uint4 ld_policy(const void *ptr, uint64_t pol) {
+    uint4 v;
+    asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "l"(pol));
+    return v;
+}
+// streamed 4-byte loads (no L1 allocation, evict_first in L2)
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *ptr, uint64_t pol) {
+    uint32_t v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_policy(void *ptr, const uint4 &v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// store EPV consecutive values (16 bytes) with columns >= f_left zeroed
+__device__ __forceinline__ void store16(float *dst, const float *v, int f_left, uint64_t pol) {
+    uint4 o;
+    o.x = __float_as_uint(0 < f_left ? v[0] : 0.f);
+    o.y = __float_as_uint(1 < f_left ? v[1] : 0.f);
+    o.z = __float_as_uint(2 < f_left ? v[2] : 0.f);
+    o.w = __float_as_uint(3 < f_left ? v[3] : 0.f);
+    st_policy(dst, o, pol);
+}
+__device__ __forceinline__ void store16(__nv_bfloat16 *dst, const float *v, int f_left, uint64_t pol) {
     float w[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) w[k] = k < f_left ? v[k] : 0.f;
@@ -64,9 +101,9 @@ __device__ __forceinline__ void store16(__nv_bfloat16 *dst, const float *v, int 
     o.y = pack_bf16x2(w[2], w[3]);
     o.z = pack_bf16x2(w[4], w[5]);
     o.w = pack_bf16x2(w[6], w[7]);
-    *reinterpret_cast<uint4 *>(dst) = o;
+    st_policy(dst, o, pol);
 }
-// store 4 consecutive values (fix-up granularity)
+// 4 consecutive values (fix-up granularity)
 __device__ __forceinline__ void store4(float *dst, float4 v) { *reinterpret_cast<float4 *>(dst) = v; }
 __device__ __forceinline__ void store4(__nv_bfloat16 *dst, float4 v) {
     uint2 o;
@@ -81,135 +118,275 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *src) {
                        __uint_as_float(v.y & 0xffff0000u));
 }
 
-template <typename T, int LPG, int VPT, int U>
-__global__ void __launch_bounds__(256) aggregate_kernel(const AggParams p, const int32_t *__restrict__ chunk_row,
-                                                        const int32_t *__restrict__ chunk_begin,
-                                                        const int32_t *__restrict__ chunk_end, int64_t n_chunks,
-                                                        float *__restrict__ partial, int64_t pld) {
-    constexpr int EPV = 16 / (int)sizeof(T);
-    constexpr int GROUPS = 32 / LPG;
-    static_assert(GROUPS * U <= 32 && (32 % (GROUPS * U)) == 0, "step must divide the warp");
-    const int lane = threadIdx.x & 31;
-    const int g = lane / LPG, gl = lane % LPG;
-    const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+constexpr uint32_t kHotBit = 0x80000000u;
 
+// one batch of 32 entries: lane i holds (column | hot bit, weight) of entry base + i
+__device__ __forceinline__ void load_batch(const uint32_t *__restrict__ colidx, const float *__restrict__ wts,
+                                           uint32_t colmask, int hot_tier, int32_t b, int32_t n, int32_t base,
+                                           int lane, uint64_t pol_stream, uint32_t &c, float &w) {
+    c = 0;
+    w = 0.f;
+    if (base + lane < n) {
+        const uint32_t raw = ld_stream_u32(colidx + b + base + lane, pol_stream);
+        w = __uint_as_float(ld_stream_u32(wts + b + base + lane, pol_stream));
+        const uint32_t col = raw & colmask;
+        const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;
+        c = col | (tier <= hot_tier ? kHotBit : 0u);
+    }
+}
+
+// cp.async of 16 bytes into shared memory with an L2 eviction policy
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gsrc), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared memory of one warp: a ring of D steps; a step holds, for every lane,
+// VPT 16-byte vectors of the row its lane group gathers and the entry weight.
+template <int VPT, int D>
+struct WarpRing {
+    static constexpr int kVecs = D * VPT * 32;  // uint4 per warp
+    static constexpr int kBytes = kVecs * 16 + D * 32 * 4;
+};
+
+// One work item: a whole light row or one chunk of a heavy row.
+struct Item {
     int64_t r;
     int32_t b, e;
-    bool is_chunk;
-    if (item < n_chunks) {
-        r = chunk_row[item];
-        if (r >= p.n_rows) return;
-        b = chunk_begin[item];
-        e = chunk_end[item];
-        is_chunk = true;
+    bool chunk;
+    bool skip;  // no work for this warp (heavy row in the row range, or past n_rows)
+};
+
+__device__ __forceinline__ Item load_item(int64_t it, int64_t n_chunks, const int32_t *__restrict__ chunk_row,
+                                          const int32_t *__restrict__ chunk_begin,
+                                          const int32_t *__restrict__ chunk_end, const int32_t *__restrict__ rowptr,
+                                          int64_t n_rows) {
+    Item x;
+    if (it < n_chunks) {
+        x.r = chunk_row[it];
+        x.b = chunk_begin[it];
+        x.e = chunk_end[it];
+        x.chunk = true;
+        x.skip = x.r >= n_rows;
     } else {
-        r = item - n_chunks;
-        if (r >= p.n_rows) return;
-        b = p.rowptr[r];
-        e = p.rowptr[r + 1];
-        if (e - b > kHeavyNnz) return;  // handled by its chunks and the fix-up
-        is_chunk = false;
+        x.r = it - n_chunks;
+        x.chunk = false;
+        if (x.r < n_rows) {
+            x.b = rowptr[x.r];
+            x.e = rowptr[x.r + 1];
+            x.skip = x.e - x.b > kHeavyNnz;  // handled by its chunks and the fix-up
+        } else {
+            x.b = x.e = 0;
+            x.skip = true;
+        }
     }
+    return x;
+}
 
+// Persistent warps: warp w of W handles items w, w + W, w + 2W, ... as one
+// continuous stream of entries.  The issue side runs D steps ahead of the
+// consume side (a step: every lane group gathers one entry into the warp's
+// shared-memory ring with cp.async); the consume side accumulates a step and
+// finishes an item (writes its row or partial) when its steps are done, so
+// the gather pipeline never drains between rows.
+template <typename T, int LPG, int VPT, int D, int MINB>
+__global__ void __launch_bounds__(256, MINB)
+    aggregate_kernel(const AggParams p, const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_begin,
+                     const int32_t *__restrict__ chunk_end, int64_t n_chunks, float *__restrict__ partial,
+                     int64_t pld) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+    constexpr int GROUPS = 32 / LPG;
+    static_assert(D >= 1 && D <= 32, "ring depth");
+    extern __shared__ uint4 smem_ring[];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int g = lane / LPG, gl = lane % LPG;
+    uint4 *ring = smem_ring + wib * WarpRing<VPT, D>::kVecs;
+    float *wring = reinterpret_cast<float *>(smem_ring + 8 * WarpRing<VPT, D>::kVecs) + wib * D * 32;
+
+    const int64_t W = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + wib;
+    const int64_t n_items = n_chunks + p.n_rows;
+    const uint64_t pol_keep = policy_evict_last();
+    const uint64_t pol_stream = policy_evict_first();
     const T *__restrict__ X = static_cast<const T *>(p.X);
-    const bool skip_self = p.mode != AGG_GCN;
-    const bool col_weight = p.mode != AGG_SAGE_FWD;
-    const int64_t f = p.f;
+    const int64_t f = p.f, ldx = p.ldx;
+    const uint32_t *__restrict__ colidx = p.colidx;
+    const float *__restrict__ wts = p.wts;
+    const uint32_t colmask = p.colmask;
+    const int hot_tier = p.hot_tier;
+    const int32_t *__restrict__ rowptr = p.rowptr;
+    const int64_t n_rows = p.n_rows;
 
+    // ---- issue side: item it_i, next entry pos_i, column-id batches ----
+    int64_t it_i = w0;
+    Item cur_i = it_i < n_items ? load_item(it_i, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows) : Item{0, 0, 0, false, true};
+    int32_t pos_i = 0, bbase = 0;
+    uint32_t c_cur = 0, c_next = 0;
+    float w_cur = 0.f, w_next = 0.f;
+    bool issue_live = it_i < n_items;
+    // advance the issue side to an item with entries (or the end); load its batches
+    auto settle_issue = [&]() {
+        while (issue_live && (cur_i.skip || pos_i >= cur_i.e - cur_i.b)) {
+            it_i += W;
+            if (it_i >= n_items) {
+                issue_live = false;
+                break;
+            }
+            cur_i = load_item(it_i, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+            pos_i = 0;
+            if (!cur_i.skip && cur_i.e > cur_i.b) {
+                bbase = 0;
+                load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 0, lane, pol_stream, c_cur,
+                           w_cur);
+                load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 32, lane, pol_stream,
+                           c_next, w_next);
+            }
+        }
+    };
+    if (issue_live && !cur_i.skip && cur_i.e > cur_i.b) {
+        load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 0, lane, pol_stream, c_cur, w_cur);
+        load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 32, lane, pol_stream, c_next,
+                   w_next);
+    }
+    settle_issue();
+    int64_t s_issue = 0;  // steps issued (ring slot = s % D)
+    auto issue_step = [&]() {
+        if (!issue_live) return;
+        const int32_t n = cur_i.e - cur_i.b;
+        if (pos_i >= bbase + 32) {
+            bbase += 32;
+            c_cur = c_next;
+            w_cur = w_next;
+            load_batch(colidx, wts, colmask, hot_tier, cur_i.b, n, bbase + 32, lane, pol_stream, c_next, w_next);
+        }
+        const int src = pos_i - bbase + g;
+        const uint32_t cc = __shfl_sync(0xffffffffu, c_cur, src);
+        const float ww = __shfl_sync(0xffffffffu, w_cur, src);
+        const bool live = pos_i + g < n;
+        const int slot = (int)(s_issue % D);
+        uint4 *dst = ring + slot * VPT * 32 + lane;
+        wring[slot * 32 + lane] = live ? ww : 0.f;
+        const T *row = X + (int64_t)(cc & ~kHotBit) * ldx;
+        const uint64_t pol = (cc & kHotBit) ? pol_keep : pol_stream;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int64_t col = (int64_t)(v * LPG + gl) * EPV;
+            if (col < f) {
+                if (live)
+                    cp_async16(dst + v * 32, row + col, pol);
+                else
+                    dst[v * 32] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        ++s_issue;
+        pos_i += GROUPS;
+        settle_issue();
+    };
+
+    // ---- consume side ----
+    const uint64_t pol_out = pol_stream;
     float acc[VPT][EPV];
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
 
-    for (int32_t base = b; base < e; base += 32) {
-        const int n_here = min(32, e - base);
-        int32_t c = 0;
-        float w = 0.f;
-        if (lane < n_here) {
-            c = __ldg(p.colidx + base + lane);
-            w = col_weight ? __ldg(p.colw + c) : 1.f;
-            if (skip_self && (int64_t)c == r) w = 0.f;
-        }
-        for (int j = 0; j < n_here; j += GROUPS * U) {
-            uint4 raw[U][VPT];
-            float wu[U];
+    // finish item x (id it): reduce the lane groups and write the row or the partial
+    auto finish = [&](const Item &x, int64_t it) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int jj = j + u * GROUPS + g;
-                const int32_t cc = __shfl_sync(0xffffffffu, c, jj);
-                const float ww = __shfl_sync(0xffffffffu, w, jj);
-                const bool live = jj < n_here;
-                wu[u] = live ? ww : 0.f;
-                const T *row = X + (int64_t)cc * p.ldx;
+        for (int off = LPG; off < 32; off <<= 1)
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) acc[v][k] += __shfl_xor_sync(0xffffffffu, acc[v][k], off);
+        if (g == 0) {
+            if (x.chunk) {
+                float *dst = partial + it * pld;
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
                     const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-                    if (live && col < f)
-                        raw[u][v] = __ldg(reinterpret_cast<const uint4 *>(row + col));
-                    else
-                        raw[u][v] = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
+                    if (col < f) {
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+                        for (int k = 0; k < EPV; k += 4)
+                            *reinterpret_cast<float4 *>(dst + col + k) =
+                                make_float4(acc[v][k], acc[v][k + 1], acc[v][k + 2], acc[v][k + 3]);
+                    }
+                }
+            } else {
+                const float scale = p.rowscale ? __ldg(p.rowscale + x.r) : 1.f;
+                T *out = static_cast<T *>(p.out) + x.r * p.ldo;
+                const T *selfrow = nullptr;
+                if (p.self_mode == SELF_COPY) selfrow = X + x.r * ldx;
+                if (p.self_mode == SELF_ADD && x.r < p.n_self) selfrow = static_cast<const T *>(p.self) + x.r * p.ld_self;
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
-                    float x[EPV];
-                    unpack16(X, raw[u][v], x);
+                    const int64_t col = (int64_t)(v * LPG + gl) * EPV;
+                    if (col >= f) continue;
+                    float o[EPV];
 #pragma unroll
-                    for (int k = 0; k < EPV; ++k) acc[v][k] = fmaf(wu[u], x[k], acc[v][k]);
+                    for (int k = 0; k < EPV; ++k) o[k] = acc[v][k] * scale;
+                    if (selfrow) {
+                        float sv[EPV];
+                        unpack16(X, __ldg(reinterpret_cast<const uint4 *>(selfrow + col)), sv);
+                        if (p.self_mode == SELF_ADD) {
+#pragma unroll
+                            for (int k = 0; k < EPV; ++k) o[k] += sv[k];
+                        } else {
+                            store16(out + col, sv, (int)(f - col), pol_out);
+                        }
+                    }
+                    store16(out + p.out_off + col, o, (int)(f - col), pol_out);
                 }
+            }
         }
-    }
-    // reduce the GROUPS partial sums of the warp (fixed butterfly order)
-#pragma unroll
-    for (int off = LPG; off < 32; off <<= 1)
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) acc[v][k] += __shfl_xor_sync(0xffffffffu, acc[v][k], off);
-    if (g != 0) return;
+            for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
+    };
 
-    if (is_chunk) {
-        float *dst = partial + item * pld;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-            if (col < f) {
-#pragma unroll
-                for (int k = 0; k < EPV; k += 4)
-                    *reinterpret_cast<float4 *>(dst + col + k) =
-                        make_float4(acc[v][k], acc[v][k + 1], acc[v][k + 2], acc[v][k + 3]);
-            }
-        }
-        return;
+    // prologue: D steps in flight
+#pragma unroll 1
+    for (int d = 0; d < D; ++d) {
+        issue_step();
+        cp_async_commit();
     }
-
-    const float scale = p.mode == AGG_SAGE_BWD ? 1.f : __ldg(p.colw + r);
-    T *out = static_cast<T *>(p.out) + r * p.ldo;
-    const T *selfrow = nullptr;
-    if (p.mode == AGG_SAGE_FWD) selfrow = X + r * p.ldx;
-    if (p.mode == AGG_SAGE_BWD && r < p.n_self) selfrow = static_cast<const T *>(p.self) + r * p.ld_self;
+    int64_t it_c = w0;
+    int64_t s_cons = 0;
+#pragma unroll 1
+    while (it_c < n_items) {
+        const Item x = load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+        if (!x.skip) {
+            const int32_t steps = (x.e - x.b + GROUPS - 1) / GROUPS;
+#pragma unroll 1
+            for (int32_t t = 0; t < steps; ++t) {
+                cp_async_wait<D - 1>();
+                const int slot = (int)(s_cons % D);
+                const float w = wring[slot * 32 + lane];
+                const uint4 *src = ring + slot * VPT * 32 + lane;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-        if (col >= f) continue;
-        float o[EPV];
+                for (int v = 0; v < VPT; ++v) {
+                    float xv[EPV];
+                    unpack16(X, src[v * 32], xv);
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) o[k] = acc[v][k] * scale;
-        if (selfrow) {
-            float s[EPV];
-            unpack16(X, __ldg(reinterpret_cast<const uint4 *>(selfrow + col)), s);
-            if (p.mode == AGG_SAGE_BWD) {
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) o[k] += s[k];
-            } else {
-                store16(out + col, s, (int)(f - col));
+                    for (int k = 0; k < EPV; ++k) acc[v][k] = fmaf(w, xv[k], acc[v][k]);
+                }
+                ++s_cons;
+                issue_step();
+                cp_async_commit();
             }
+            finish(x, it_c);
         }
-        store16(out + p.out_off + col, o, (int)(f - col));
+        it_c += W;
     }
+    cp_async_wait<0>();
 }
 
 template <typename T>
@@ -225,12 +402,12 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
     const int32_t c0 = heavy_choff[h], c1 = heavy_choff[h + 1];
     const int64_t f = p.f;
     const int64_t fpad = (f + EPV - 1) / EPV * EPV;
-    const float scale = p.mode == AGG_SAGE_BWD ? 1.f : __ldg(p.colw + r);
+    const float scale = p.rowscale ? __ldg(p.rowscale + r) : 1.f;
     const T *X = static_cast<const T *>(p.X);
     T *out = static_cast<T *>(p.out) + r * p.ldo;
     const T *selfrow = nullptr;
-    if (p.mode == AGG_SAGE_FWD) selfrow = X + r * p.ldx;
-    if (p.mode == AGG_SAGE_BWD && r < p.n_self) selfrow = static_cast<const T *>(p.self) + r * p.ld_self;
+    if (p.self_mode == SELF_COPY) selfrow = X + r * p.ldx;
+    if (p.self_mode == SELF_ADD && r < p.n_self) selfrow = static_cast<const T *>(p.self) + r * p.ld_self;
     for (int64_t col = (int64_t)lane * 4; col < fpad; col += 128) {
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (col < f) {
@@ -245,7 +422,7 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
         float4 o = make_float4(s.x * scale, s.y * scale, s.z * scale, s.w * scale);
         if (selfrow) {
             float4 sv = col < f ? load4(selfrow + col) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (p.mode == AGG_SAGE_BWD) {
+            if (p.self_mode == SELF_ADD) {
                 o.x += sv.x;
                 o.y += sv.y;
                 o.z += sv.z;
@@ -266,13 +443,21 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
     }
 }
 
-template <typename T, int LPG, int VPT, int U>
+template <typename T, int LPG, int VPT, int D, int MINB>
 gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
     const int64_t items = sc.n_chunks + p.n_rows;
     if (items > 0) {
-        const int64_t blocks = ceil_div(items * 32, 256);
-        { aggregate_kernel<T, LPG, VPT, U><<<(unsigned)blocks, 256, 0, s>>>(p, sc.chunk_row, sc.chunk_begin,
-                                                                           sc.chunk_end, sc.n_chunks, partial, pld); GNN_LAUNCHED(1); }
+        const int smem = 8 * WarpRing<VPT, D>::kBytes;
+        auto kern = aggregate_kernel<T, LPG, VPT, D, MINB>;
+        GNN_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        // persistent warps: as many blocks as fit on the GPU at once
+        int per_sm = 0;
+        GNN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+        if (per_sm < 1) per_sm = 1;
+        int64_t blocks = (int64_t)num_sms() * per_sm;
+        if (blocks > ceil_div(items, 8)) blocks = ceil_div(items, 8);
+        { kern<<<(unsigned)blocks, 256, smem, s>>>(p, sc.chunk_row, sc.chunk_begin, sc.chunk_end, sc.n_chunks,
+                                                    partial, pld); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
     if (sc.n_heavy > 0) {
@@ -286,16 +471,18 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
 
 template <typename T>
 gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
+    // steps in flight per warp D: D * 512 * VPT bytes of gathered rows per warp;
+    // shared memory (8 warps per block) then sets the blocks per SM (MINB)
     const int64_t bytes = p.f * (int64_t)sizeof(T);
-    if (bytes <= 128) return launch_cfg<T, 8, 1, 8>(p, sc, partial, pld, s);
-    if (bytes <= 256) return launch_cfg<T, 16, 1, 8>(p, sc, partial, pld, s);
-    if (bytes <= 512) return launch_cfg<T, 32, 1, 8>(p, sc, partial, pld, s);
-    if (bytes <= 1024) return launch_cfg<T, 32, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 32, 3, 2>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 32, 4, 2>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 32, 5, 2>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 32, 6, 1>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 32, 8, 1>(p, sc, partial, pld, s);
+    if (bytes <= 128) return launch_cfg<T, 8, 1, 8, 5>(p, sc, partial, pld, s);
+    if (bytes <= 256) return launch_cfg<T, 16, 1, 8, 5>(p, sc, partial, pld, s);
+    if (bytes <= 512) return launch_cfg<T, 32, 1, 8, 5>(p, sc, partial, pld, s);
+    if (bytes <= 1024) return launch_cfg<T, 32, 2, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1536) return launch_cfg<T, 32, 3, 3, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 32, 4, 2, 3>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 32, 5, 2, 3>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 32, 6, 2, 2>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 32, 8, 1, 2>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 

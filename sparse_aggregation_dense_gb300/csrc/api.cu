@@ -165,6 +165,8 @@ static void destroy_graph(gnn_graph *g) {
     cudaFree(g->colidxT);
     cudaFree(g->permT);
     cudaFree(g->colw);
+    cudaFree(g->wfwd);
+    cudaFree(g->wbwd);
     cudaFree(g->err);
     cudaFree(g->ws);
     cudaFree(g->claim);
@@ -234,6 +236,17 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     // schedules
     TRY(build_schedule(g->rowptr, n_local, &g->fwd, s));
     TRY(build_schedule(g->rowptrT, nT, &g->bwd, s));
+    // per-entry weights: the column factor of each entry (forward over the
+    // block, backward over the transpose), 0 on the diagonal for the mean
+    const bool sage = agg == GNN_AGG_SAGE_MEAN;
+    TRY_CUDA(cudaMalloc((void **)&g->wfwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
+    TRY_CUDA(cudaMalloc((void **)&g->wbwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
+    TRY(launch_entry_weights(g->rowptr, g->colidx, n_local, sage ? nullptr : g->colw, sage, g->wfwd, s));
+    TRY(launch_entry_weights(g->rowptrT, g->colidxT, nT, g->colw, sage, g->wbwd, s));
+    // hotness tiers: forward columns by how often they are gathered (their
+    // transpose row length), backward columns (local rows) by their row length
+    TRY(tag_tiers(g->colidx, nnz, g->rowptrT, nT, &g->fwd, s));
+    TRY(tag_tiers(g->colidxT, nnz, g->rowptr, n_local, &g->bwd, s));
     TRY_CUDA(cudaStreamSynchronize(s));
     TRY_CUDA(cudaGetLastError());
 #undef TRY
@@ -264,7 +277,10 @@ gnn_status gnn_graph_copy_transpose(const gnn_graph *g, int32_t *rowptrT, int32_
     const size_t nT1 = (size_t)(g->n_local + g->n_halo + 1) * sizeof(int32_t);
     const size_t nz = (size_t)g->nnz * sizeof(int32_t);
     if (rowptrT) GNN_CUDA_TRY(cudaMemcpyAsync(rowptrT, g->rowptrT, nT1, cudaMemcpyDeviceToDevice, s));
-    if (colidxT && nz) GNN_CUDA_TRY(cudaMemcpyAsync(colidxT, g->colidxT, nz, cudaMemcpyDeviceToDevice, s));
+    if (colidxT && nz) {
+        gnn_status st = copy_untagged(g->colidxT, colidxT, g->nnz, g->bwd.tagged ? kColMask : 0xffffffffu, s);
+        if (st != GNN_OK) return st;
+    }
     if (permT && nz) GNN_CUDA_TRY(cudaMemcpyAsync(permT, g->permT, nz, cudaMemcpyDeviceToDevice, s));
     return GNN_OK;
 }
@@ -334,13 +350,16 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
     GNN_CUDA_TRY(cudaGetLastError());
     AggParams p{};
     p.rowptr = g->rowptr;
-    p.colidx = g->colidx;
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
+    p.wts = g->wfwd;
+    p.rowscale = g->colw;
     p.n_rows = nL;
+    p.colmask = g->fwd.tagged ? kColMask : 0xffffffffu;
+    p.hot_tier = hot_tier_for(g->fwd, round_up(f_in * elem_size(dtype), 32));
     p.X = H;
     p.ldx = ld_h;
     p.f = f_in;
-    p.colw = g->colw;
-    p.mode = sage ? AGG_SAGE_FWD : AGG_GCN;
+    p.self_mode = sage ? SELF_COPY : SELF_NONE;
     p.out = Z;
     p.ldo = ld_z;
     p.out_off = sage ? half : 0;
@@ -372,9 +391,11 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     if (f_in * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
     cudaStream_t s = as_stream(stream);
     const int64_t ldw = round_up(f_out, 4);
+    const bool use_tc = dtype == GNN_BF16 && update_bwd_tc_supported(Kp, f_out) && !force_simt_update();
     const size_t wp_bytes = align_up((size_t)Kp * ldw * sizeof(float));
     const size_t dwp_bytes = sage ? align_up((size_t)Kp * f_out * sizeof(float)) : 0;
-    const size_t wg_bytes = align_up(update_bwd_ws_bytes(nL, Kp, f_out, dtype));
+    const size_t wg_bytes = align_up(use_tc ? update_bwd_tc_ws_bytes(nL, Kp, f_out)
+                                            : update_bwd_ws_bytes(nL, Kp, f_out, dtype));
     const size_t part_bytes = dH ? align_up(aggregate_partial_bytes(g->bwd, f_in)) : 0;
     gnn_status st = ensure_workspace(g, wp_bytes + dwp_bytes + wg_bytes + part_bytes, s);
     if (st != GNN_OK) return st;
@@ -388,8 +409,12 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     GNN_CUDA_TRY(cudaGetLastError());
     {
         ProfScope prof(g, GNN_PROF_UPD_BWD, s);
-        st = launch_update_bwd(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp, dH ? dZ : nullptr,
-                               ld_dz, dtype, wg, wg_bytes, s);
+        if (use_tc)
+            st = launch_update_bwd_tc(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp,
+                                      dH ? dZ : nullptr, ld_dz, wg, g->err, s);
+        else
+            st = launch_update_bwd(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp,
+                                   dH ? dZ : nullptr, ld_dz, dtype, wg, wg_bytes, s);
     }
     if (st != GNN_OK) return st;
     if (sage) {
@@ -399,24 +424,26 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     if (!dH) return GNN_OK;
     AggParams p{};
     p.rowptr = g->rowptrT;
-    p.colidx = g->colidxT;
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidxT);
+    p.wts = g->wbwd;
+    p.rowscale = sage ? nullptr : g->colw;
     p.n_rows = out_rows;
+    p.colmask = g->bwd.tagged ? kColMask : 0xffffffffu;
+    p.hot_tier = hot_tier_for(g->bwd, round_up(f_in * elem_size(dtype), 32));
     p.f = f_in;
-    p.colw = g->colw;
     p.out = dH;
     p.ldo = ld_dh;
     p.out_off = 0;
+    p.ldx = ld_dz;
     if (sage) {
-        p.mode = AGG_SAGE_BWD;
+        p.self_mode = SELF_ADD;
         p.X = static_cast<const char *>(dZ) + half * elem_size(dtype);
-        p.ldx = ld_dz;
         p.self = dZ;
         p.ld_self = ld_dz;
         p.n_self = nL;
     } else {
-        p.mode = AGG_GCN;
+        p.self_mode = SELF_NONE;
         p.X = dZ;
-        p.ldx = ld_dz;
     }
     ProfScope prof(g, GNN_PROF_AGG_BWD, s);
     return launch_aggregate(p, g->bwd, dtype, partial, s);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,8 +20,19 @@ constexpr int kWarp = 32;
 constexpr int kHeavyNnz = 512;
 constexpr int kChunkNnz = 512;
 
+// Column ids of the graph's CSR copies carry a 5-bit "hotness tier" in bits
+// 27..31 (when the column count is below 2^27): tier t holds the columns of
+// access-count rank below about 1024 * 2^(t/2).  An aggregation keeps the rows of
+// the hottest tiers that fit a share of L2 resident (evict_last) and streams the
+// rest (evict_first).
+constexpr int kTierShift = 27;
+constexpr uint32_t kColMask = (1u << kTierShift) - 1u;
+constexpr int kTiers = 32;
+
 // Heavy-row schedule of one CSR (block rows or transpose rows).
 struct Schedule {
+    bool tagged = false;           // column ids carry tiers
+    int64_t tier_rows[kTiers] = {};  // columns per tier
     int64_t n_rows = 0;        // rows of the CSR
     int64_t n_heavy = 0;       // rows split into chunks
     int64_t n_chunks = 0;      // total chunks
@@ -43,6 +55,8 @@ struct gnn_graph {
     int32_t *rowptrT = nullptr, *colidxT = nullptr, *permT = nullptr;
     // GCN: dinv over n_local + n_halo columns; GraphSAGE: inverse neighbour counts of local rows
     float *colw = nullptr;
+    // per-entry weights of the block (forward) and of its transpose (backward)
+    float *wfwd = nullptr, *wbwd = nullptr;
     gnn::Schedule fwd, bwd;
     int *err = nullptr;  // device error word
     // workspace (heavy-row partials, dW split partials, packed W)
@@ -89,6 +103,13 @@ gnn_status exclusive_scan_i32(const int32_t *in, int32_t *out, int64_t n, bool w
 gnn_status csr_transpose(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, int64_t n_cols, int64_t nnz,
                          int32_t *rowptrT, int32_t *colidxT, int32_t *permT, cudaStream_t s);
 gnn_status build_schedule(const int32_t *rowptr, int64_t n_rows, Schedule *sc, cudaStream_t s);
+// Tag colidx entries with the tier of their column's access count, where the
+// count of column c is ptr[c + 1] - ptr[c] (ptr: n_cols + 1 entries).
+gnn_status tag_tiers(int32_t *colidx, int64_t nnz, const int32_t *ptr, int64_t n_cols, Schedule *sc, cudaStream_t s);
+// Largest tier whose rows (row_bytes each, tiers 0..t together) fit the L2 share.
+int hot_tier_for(const Schedule &sc, int64_t row_bytes);
+// Copy column ids without their tier bits.
+gnn_status copy_untagged(const int32_t *src, int32_t *dst, int64_t n, uint32_t mask, cudaStream_t s);
 void free_schedule(Schedule *sc);
 
 // ---- kernels launched by the API ------------------------------------------
@@ -98,6 +119,10 @@ gnn_status launch_gcn_dinv(const int32_t *rowptr, const int32_t *colidx, int64_t
                            int64_t nnz, const float *deg, float *dinv, cudaStream_t s);
 gnn_status launch_sage_invcnt(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, float *out,
                               cudaStream_t s);
+// per-entry weights: w[e] = colw[col_e] (or 1 when colw is null), 0 when
+// skip_self and col_e equals the entry's row
+gnn_status launch_entry_weights(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, const float *colw,
+                                bool skip_self, float *w, cudaStream_t s);
 
 gnn_status launch_pull(const void *table, int64_t ld_t, int64_t n_table, const int64_t *ids, int64_t n_ids,
                        void *H, int64_t ld_h, int64_t row0, int64_t f, int es, int *err, cudaStream_t s);
@@ -105,29 +130,33 @@ gnn_status ensure_claim(gnn_graph *g, int64_t n_table);
 gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                        void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s);
 
-// Aggregation over a CSR with its heavy-row schedule.
-//   out[r, off : off + f] = rowscale(r) * sum_{e in row r, keep(e)} colw(col_e) * X[col_e, 0:f]
-// mode selects the weights and the self term:
-enum AggMode {
-    AGG_GCN = 0,        // rowscale = colw[r], weight = colw[c]                 (forward and backward)
-    AGG_SAGE_FWD = 1,   // rowscale = colw[r], weight 1, skip c == r, out[r, 0:f] = X[r] copied
-    AGG_SAGE_BWD = 2,   // rowscale 1, weight = colw[c], skip c == r, + self[r, 0:f] for r < n_self
+// Aggregation over a CSR with its heavy-row schedule:
+//   out[r, off : off + f] = rowscale[r] * sum_{e in row r} wts[e] * X[col_e, 0:f]   (+ the self term)
+// The per-entry weights hold the column factor (GCN: dinv[c]; GraphSAGE: 1 or
+// inv_cnt[c], and 0 on the diagonal entry the mean leaves out).
+enum SelfMode {
+    SELF_NONE = 0,
+    SELF_COPY = 1,  // out[r, 0:f] = X[r, 0:f]                      (GraphSAGE forward)
+    SELF_ADD = 2,   // result += self[r, 0:f] for r < n_self          (GraphSAGE backward)
 };
 struct AggParams {
     const int32_t *rowptr;
-    const int32_t *colidx;
-    int64_t n_rows;      // output rows computed: [0, n_rows)
+    const uint32_t *colidx;  // column ids, tier bits above colmask
+    const float *wts;        // per-entry weights
+    const float *rowscale;   // per-row scale, nullptr for 1
+    int64_t n_rows;          // output rows computed: [0, n_rows)
+    uint32_t colmask;
+    int hot_tier;            // entries with tier <= hot_tier are gathered with evict_last
     const void *X;
     int64_t ldx;
     int64_t f;
-    const float *colw;
-    int mode;
+    int self_mode;
     void *out;
     int64_t ldo;
-    int64_t out_off;     // column of out where the aggregate is written
-    const void *self;    // AGG_SAGE_BWD: dZ (self half at column 0); AGG_SAGE_FWD: unused (X)
+    int64_t out_off;         // column of out where the aggregate is written
+    const void *self;        // SELF_ADD source (row stride ld_self)
     int64_t ld_self;
-    int64_t n_self;      // AGG_SAGE_BWD: rows r < n_self get the self term
+    int64_t n_self;
 };
 gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s);
 size_t aggregate_partial_bytes(const Schedule &sc, int64_t f);
@@ -141,6 +170,17 @@ bool update_fwd_tc_supported(int64_t Kp, int64_t N);
 size_t update_tc_wt_bytes(int64_t Kp, int64_t N);
 gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w,
                                 int64_t N, int relu, void *out, int64_t ld_o, void *wt_ws, int *err, cudaStream_t s);
+// 2-D bf16 tensor map with 128-byte swizzle (box_inner x box_outer elements)
+bool make_map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_outer);
+int num_sms();
+// Dense update, backward, on the tensor cores (bf16): dZ = dY W^T and the dW
+// partials of each CTA (ws: update_bwd_tc_ws_bytes), then dWp = their sum.
+bool update_bwd_tc_supported(int64_t Kp, int64_t N);
+size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp, int64_t N);
+gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
+                                int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
+                                float *dWp, void *dZ, int64_t ld_dz, void *ws, int *err, cudaStream_t s);
 // GNN_UPDATE_SIMT=1 in the environment selects the CUDA-core update for bf16 too
 bool force_simt_update();
 // Dense update, backward: dZ = dY Wp^T (n x Kp) when dZ != NULL; dWp partials then dW.

@@ -212,6 +212,29 @@ gnn_status launch_sage_invcnt(const int32_t *rowptr, const int32_t *colidx, int6
     return GNN_OK;
 }
 
+__global__ void entry_weights_kernel(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ colidx,
+                                     int64_t n_rows, const float *__restrict__ colw, int skip_self,
+                                     float *__restrict__ w) {
+    const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= n_rows) return;
+    for (int64_t e = rowptr[r] + lane; e < rowptr[r + 1]; e += 32) {
+        const int32_t c = colidx[e];
+        float v = colw ? colw[c] : 1.0f;
+        if (skip_self && (int64_t)c == r) v = 0.0f;
+        w[e] = v;
+    }
+}
+
+gnn_status launch_entry_weights(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, const float *colw,
+                                bool skip_self, float *w, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    { entry_weights_kernel<<<(unsigned)ceil_div(n_rows * 32, 256), 256, 0, s>>>(rowptr, colidx, n_rows, colw,
+                                                                               skip_self ? 1 : 0, w); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
 // ---------------------------------------------------------------------------
 // stable transpose: row ids of every entry, LSD radix sort of the column ids
 // (8-bit digits, 4096-entry tiles, warp ranks by match_any), then counts
@@ -431,6 +454,106 @@ gnn_status build_schedule(const int32_t *rowptr, int64_t n_rows, Schedule *sc, c
     GNN_CUDA_TRY(cudaFreeAsync(nch, s));
     GNN_CUDA_TRY(cudaFreeAsync(flag, s));
     return GNN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// hotness tiers (L2 residency hints of the aggregation)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int count_bin(int32_t c) {
+    // 8 bins per octave: 1 + 8 * floor(log2 c) + the 3 bits below the leading one
+    if (c <= 0) return 0;
+    const int lz = 31 - __clz(c);
+    const int sub = lz >= 3 ? (c >> (lz - 3)) & 7 : (c << (3 - lz)) & 7;
+    return 1 + 8 * lz + sub;
+}
+
+__global__ void count_bins_kernel(const int32_t *__restrict__ ptr, int64_t n, int32_t *hist) {
+    __shared__ int32_t h[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride)
+        atomicAdd(&h[count_bin(ptr[x + 1] - ptr[x])], 1);
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+__global__ void tag_tiers_kernel(int32_t *__restrict__ colidx, int64_t nnz, const int32_t *__restrict__ ptr,
+                                 const uint8_t *__restrict__ tier_of_bin) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += stride) {
+        const int32_t c = colidx[e];
+        const uint32_t t = tier_of_bin[count_bin(ptr[c + 1] - ptr[c])];
+        colidx[e] = (int32_t)((uint32_t)c | (t << kTierShift));
+    }
+}
+
+__global__ void untag_kernel(const int32_t *__restrict__ src, int32_t *__restrict__ dst, int64_t n, uint32_t mask) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        dst[i] = (int32_t)((uint32_t)src[i] & mask);
+}
+
+gnn_status copy_untagged(const int32_t *src, int32_t *dst, int64_t n, uint32_t mask, cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    { untag_kernel<<<152 * 8, 256, 0, s>>>(src, dst, n, mask); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
+gnn_status tag_tiers(int32_t *colidx, int64_t nnz, const int32_t *ptr, int64_t n_cols, Schedule *sc, cudaStream_t s) {
+    sc->tagged = false;
+    for (int t = 0; t < kTiers; ++t) sc->tier_rows[t] = 0;
+    if (n_cols >= ((int64_t)1 << kTierShift) || n_cols == 0 || nnz == 0) return GNN_OK;
+    int32_t *hist = nullptr;
+    uint8_t *tob = nullptr;
+    GNN_CUDA_TRY(cudaMallocAsync((void **)&hist, 256 * sizeof(int32_t), s));
+    GNN_CUDA_TRY(cudaMallocAsync((void **)&tob, 256, s));
+    GNN_CUDA_TRY(cudaMemsetAsync(hist, 0, 256 * sizeof(int32_t), s));
+    { count_bins_kernel<<<152 * 4, 256, 0, s>>>(ptr, n_cols, hist); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    int32_t h[256];
+    GNN_CUDA_TRY(cudaMemcpyAsync(h, hist, sizeof(h), cudaMemcpyDeviceToHost, s));
+    GNN_CUDA_TRY(cudaStreamSynchronize(s));
+    // walk bins from the most accessed down; a bin's tier is the first whose rank
+    // bound covers every column up to and including the bin
+    uint8_t t_of[256];
+    int64_t cum = 0;
+    int t = 0;
+    for (int b = 255; b >= 0; --b) {
+        cum += h[b];
+        while (t < kTiers - 1 && (double)cum > 1024.0 * exp2(0.5 * t)) ++t;
+        t_of[b] = (uint8_t)t;
+        sc->tier_rows[t] += h[b];
+    }
+    GNN_CUDA_TRY(cudaMemcpyAsync(tob, t_of, sizeof(t_of), cudaMemcpyHostToDevice, s));
+    { tag_tiers_kernel<<<152 * 16, 256, 0, s>>>(colidx, nnz, ptr, tob); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    GNN_CUDA_TRY(cudaFreeAsync(hist, s));
+    GNN_CUDA_TRY(cudaFreeAsync(tob, s));
+    GNN_CUDA_TRY(cudaStreamSynchronize(s));
+    sc->tagged = true;
+    return GNN_OK;
+}
+
+int hot_tier_for(const Schedule &sc, int64_t row_bytes) {
+    if (!sc.tagged) return kTiers;  // no tiers: every entry takes the keep policy
+    static int64_t budget = 0;
+    if (!budget) {
+        int dev = 0, l2 = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        budget = (int64_t)((l2 > 0 ? l2 : 64 << 20) * 0.55);
+    }
+    int64_t rows = 0;
+    int hot = -1;
+    for (int t = 0; t < kTiers; ++t) {
+        rows += sc.tier_rows[t];
+        if (rows * row_bytes > budget) break;
+        hot = t;
+    }
+    return hot;
 }
 
 }  // namespace gnn

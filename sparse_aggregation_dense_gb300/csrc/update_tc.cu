@@ -222,6 +222,8 @@ __global__ void pack_wt_bf16_kernel(const float *__restrict__ Wp, int64_t ldw, i
     Wt[x] = __float2bfloat16_rn(v);
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -235,7 +237,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+bool make_map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
               uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -259,8 +261,6 @@ int num_sms() {
     return n;
 }
 
-}  // namespace
-
 size_t update_tc_wt_bytes(int64_t Kp, int64_t N) {
     return (size_t)round_up(N, 16) * (size_t)round_up(Kp, kBK) * 2;
 }
@@ -282,8 +282,8 @@ gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t 
     { pack_wt_bf16_kernel<<<(unsigned)ceil_div(N_pad * K_pad, 256), 256, 0, s>>>(Wp, ld_w, Kp, N, K_pad, N_pad, Wt); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     CUtensorMap mapA, mapB;
-    if (!make_map(&mapA, Z, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_z * 2, kBK, kBM)) return GNN_ECUDA;
-    if (!make_map(&mapB, Wt, (uint64_t)K_pad, (uint64_t)N_pad, (uint64_t)K_pad * 2, kBK, (uint32_t)N_pad))
+    if (!make_map_bf16_2d(&mapA, Z, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_z * 2, kBK, kBM)) return GNN_ECUDA;
+    if (!make_map_bf16_2d(&mapB, Wt, (uint64_t)K_pad, (uint64_t)N_pad, (uint64_t)K_pad * 2, kBK, (uint32_t)N_pad))
         return GNN_ECUDA;
     const size_t w_bytes = (size_t)KC * N_pad * 128;
     int stages = (int)((kSmemLimit - w_bytes - sizeof(Bars) - 1024) / kTileBytes);

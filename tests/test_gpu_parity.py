@@ -316,9 +316,17 @@ def test_epoch(case):
     ref = oracle.epoch(part, [widen(t, dt, f) for t, f in zip(tables_h, w.widths)],
                        [maybe_round(x.astype(np.float64), dt) for x in Ws], y, w.agg, bf16=bf)
     tol = TOL[dt]
-    # fp32: every element within tolerance.  bf16: the chained layers may flip a
-    # few ReLU mask decisions (see close_mostly); the per-layer tests are exact.
-    chk = close if not bf else close_mostly
+    # Chained layers: a pre-activation within rounding of zero may take the other
+    # ReLU branch on the two sides (the GPU decides in fp32, the oracle in
+    # double), which moves a whole column of the next dW.  So the chained
+    # comparison allows a small fraction of elements outside the elementwise
+    # bound (none in most runs) under a tight norm bound; the per-layer tests,
+    # which feed both sides the same H_out, stay strictly elementwise.
+    if bf:
+        chk = close_mostly
+    else:
+        def chk(gpu, ref, tol, what):
+            close_mostly(gpu, ref, tol, what, max_frac=2e-3, norm_tol=1e-5)
     chk(to_host(m.out_last), ref["Hout"][-1], tol, "logits")
     assert abs(float(m.loss.item()) - ref["loss"]) <= tol * abs(ref["loss"])
     for l in range(w.layers):
