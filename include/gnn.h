@@ -205,6 +205,30 @@ typedef enum {
 gnn_status gnn_profile_enable(gnn_graph *g, int on);
 gnn_status gnn_profile_read(gnn_graph *g, double *ms, int64_t *count);
 
+/* Forward aggregation that allocates no device memory.  No counterpart in the
+ * method's sources: this entry point exists for callers that cannot call
+ * cudaMalloc at the point where they aggregate - e.g. a serving or training
+ * loop whose device memory is all reserved up front by another allocator (a
+ * framework's caching pool), or code that must not pay for the device-wide
+ * synchronisation that cudaMalloc / cudaFree can cause.
+ *   Computes exactly the Z of gnn_layer_forward (GCN: A_hat_block H; GraphSAGE:
+ *   the self / mean halves), with the same arguments, layout and errors:
+ *   H  device (n_local + n_halo) x ld_h, dtype;  Z  device n_local x ld_z.
+ * It runs the same kernels, but keeps the fp32 partial sums of the heavy-row
+ * chunks in a fixed 16 MiB array that is part of the library (held on every
+ * GPU that loads libgnn until the process exits) instead of the graph's
+ * workspace.  A graph and width whose partials would not fit (chunks of rows
+ * longer than 512 entries x f rounded up to 8 x 4 bytes > 16 MiB) are rejected
+ * with GNN_EUNSUPPORTED before anything is launched; so are widths above 4096
+ * bytes.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) once for that device.  All calls share the array:
+ * calls that overlap on the GPU (other streams, other threads) race, so
+ * serialise them.  Nothing in the array needs to start at zero: every call
+ * overwrites the partials it reads.  The graph must have been created before
+ * (gnn_graph_create allocates). */
+gnn_status gnn_aggregate_forward_noalloc(const gnn_graph *g, const void *H, int64_t ld_h, int64_t f, void *Z,
+                                         int64_t ld_z, gnn_dtype dtype, void *stream);
+
 /* Number of kernels libgnn has launched in this process so far (all graphs). */
 int64_t gnn_launch_count(void);
 

@@ -24,6 +24,8 @@
 //  - L2 residency: column ids carry a hotness tier (access-count rank); rows
 //    of the hottest tiers that fit a share of L2 are loaded with an evict_last
 //    policy, the rest and the streamed ids / weights / outputs with evict_first.
+#include <mutex>
+
 #include "gnn_internal.cuh"
 
 namespace gnn {
@@ -499,4 +501,85 @@ gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt
     return launch_typed<float>(p, sc, partial, pld, s);
 }
 
+// ---------------------------------------------------------------------------
+// Forward aggregation that allocates nothing (gnn_aggregate_forward_noalloc).
+//
+// The only scratch the aggregation needs is the fp32 partial of each chunk of a
+// heavy row.  This entry point keeps those partials in the fixed array below
+// instead of the graph's growing workspace, so a call never allocates device
+// memory.  The array is part of the library image: every GPU that loads
+// libgnn holds it until the process exits.  Every chunk overwrites its own
+// partial before the fix-up reads it, so nothing in the array has to start at
+// zero; calls that overlap on the GPU (two streams, or two threads) share the
+// array and race.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchFloats = kNoAllocScratchBytes / sizeof(float);
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_noalloc_mutex;
+float *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per
+// device (the host-side name of the array is not a device address).
+gnn_status noalloc_scratch(float **out) {
+    int dev = 0;
+    GNN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return GNN_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        GNN_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+        g_noalloc_addr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return GNN_OK;
+}
+
+bool rows_ok(const void *p, int64_t rows, int64_t ld, int64_t f, gnn_dtype t) {
+    if (rows == 0) return true;
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return false;
+    return ld >= f && ld % elems_per_16b(t) == 0;
+}
+
+}  // namespace
+
 }  // namespace gnn
+
+extern "C" gnn_status gnn_aggregate_forward_noalloc(const gnn_graph *g, const void *H, int64_t ld_h, int64_t f,
+                                                    void *Z, int64_t ld_z, gnn_dtype dtype, void *stream) {
+    using namespace gnn;
+    if (!g || (dtype != GNN_F32 && dtype != GNN_BF16) || f <= 0) return GNN_EINVAL;
+    const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    const int64_t half = gnn_sage_half_offset(f, dtype);
+    const int64_t Kp = sage ? 2 * half : f;
+    if (!rows_ok(H, nT, ld_h, f, dtype) || !rows_ok(Z, nL, ld_z, Kp, dtype)) return GNN_EINVAL;
+    if (f * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    if (aggregate_partial_bytes(g->fwd, f) > kNoAllocScratchBytes) return GNN_EUNSUPPORTED;
+    if (nL == 0) return GNN_OK;
+    float *scratch = nullptr;
+    gnn_status st = noalloc_scratch(&scratch);
+    if (st != GNN_OK) return st;
+    AggParams p{};
+    p.rowptr = g->rowptr;
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
+    p.wts = g->wfwd;
+    p.rowscale = g->colw;
+    p.n_rows = nL;
+    p.colmask = g->fwd.tagged ? kColMask : 0xffffffffu;
+    p.hot_tier = hot_tier_for(g->fwd, round_up(f * elem_size(dtype), 32));
+    p.X = H;
+    p.ldx = ld_h;
+    p.f = f;
+    p.self_mode = sage ? SELF_COPY : SELF_NONE;
+    p.out = Z;
+    p.ldo = ld_z;
+    p.out_off = sage ? half : 0;
+    return launch_aggregate(p, g->fwd, dtype, scratch, static_cast<cudaStream_t>(stream));
+}
+

@@ -29,6 +29,7 @@ EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
     "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
     "gnn_graph_copy_transpose", "gnn_status_string", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+    "gnn_aggregate_forward_noalloc",
 )
 
 PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
@@ -65,6 +66,7 @@ def _lib():
         L.gnn_graph_copy_transpose.argtypes = [vp, vp, vp, vp, vp]
         L.gnn_profile_enable.argtypes = [vp, i32]
         L.gnn_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
+        L.gnn_aggregate_forward_noalloc.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp]
         L.gnn_launch_count.argtypes = []
         L.gnn_launch_count.restype = i64
         L.gnn_status_string.argtypes = [i32]
@@ -176,6 +178,15 @@ def profile_read(g: Graph) -> dict:
     n = (ctypes.c_int64 * len(PROF_KINDS))()
     _check(_lib().gnn_profile_read(ctypes.c_void_p(g.handle), ms, n), "gnn_profile_read")
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(PROF_KINDS)}
+
+
+def aggregate_forward_noalloc(g: Graph, H: torch.Tensor, Z: torch.Tensor):
+    """Z of layer_forward for H, computed without any device allocation."""
+    ld_h, f = _mat(H)
+    ld_z, _ = _mat(Z)
+    _check(_lib().gnn_aggregate_forward_noalloc(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(Z), ld_z,
+                                                _dtype(H), ctypes.c_void_p(_stream())),
+           "gnn_aggregate_forward_noalloc")
 
 
 def launch_count() -> int:
