@@ -137,27 +137,6 @@ __device__ __forceinline__ void load_batch(const uint32_t *__restrict__ colidx, 
     }
 }
 
-// cp.async of 16 bytes into shared memory with an L2 eviction policy
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint64_t pol) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-                 "l"(gsrc), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Shared memory of one warp: a ring of D steps; a step holds, for every lane,
-// VPT 16-byte vectors of the row its lane group gathers and the entry weight.
-template <int VPT, int D>
-struct WarpRing {
-    static constexpr int kVecs = D * VPT * 32;  // uint4 per warp
-    static constexpr int kBytes = kVecs * 16 + D * 32 * 4;
-};
-
 // One work item: a whole light row or one chunk of a heavy row.
 struct Item {
     int64_t r;
@@ -192,33 +171,138 @@ __device__ __forceinline__ Item load_item(int64_t it, int64_t n_chunks, const in
     return x;
 }
 
-// Persistent warps: warp w of W handles items w, w + W, w + 2W, ... as one
-// continuous stream of entries.  The issue side runs D steps ahead of the
-// consume side (a step: every lane group gathers one entry into the warp's
-// shared-memory ring with cp.async); the consume side accumulates a step and
-// finishes an item (writes its row or partial) when its steps are done, so
-// the gather pipeline never drains between rows.
-template <typename T, int LPG, int VPT, int D, int MINB>
-__global__ void __launch_bounds__(256, MINB)
+
+__device__ __forceinline__ void bulk_copy_row(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+        "l"(gsrc), "r"(bytes), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                 : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait: false after ~2 s
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
+    if (bar_try(bar, parity)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        if (bar_try(bar, parity)) return true;
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > 2000000000ull) return false;
+    }
+}
+
+// Shared memory of one warp: NS slots of BE gathered rows (R bytes each), the
+// entries' weights and one mbarrier per slot.
+template <int R, int BE, int NS>
+struct BulkRing {
+    static constexpr int kRowBytes = NS * BE * R;
+    static constexpr int kBytes = kRowBytes + NS * BE * 4 + NS * 8;
+};
+
+// acc += w * row (this lane's VPT 16-byte vectors of a gathered row in shared
+// memory), two fp32 lanes per packed FMA
+__device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, float w) {
+    unsigned long long acc, xv, wv, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x0), "f"(x1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(wv) : "f"(w));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(wv), "l"(xv), "l"(acc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
+}
+
+template <typename T, int LPG, int VPT>
+__device__ __forceinline__ void accumulate_row(float (&acc)[VPT][16 / sizeof(T)], const uint8_t *row, float w, int gl) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(row + (v * LPG + gl) * 16);
+        float xv[EPV];
+        unpack16(static_cast<const T *>(nullptr), q, xv);
+#pragma unroll
+        for (int k = 0; k < EPV; k += 2) fma2(acc[v][k], acc[v][k + 1], xv[k], xv[k + 1], w);
+    }
+}
+
+// Advance `it` by W to the next item that has entries to gather (or the end).
+__device__ __forceinline__ bool next_work_item(int64_t &it, Item &x, int64_t W, int64_t n_items, int64_t n_chunks,
+                                               const int32_t *__restrict__ chunk_row,
+                                               const int32_t *__restrict__ chunk_begin,
+                                               const int32_t *__restrict__ chunk_end,
+                                               const int32_t *__restrict__ rowptr, int64_t n_rows) {
+    for (;;) {
+        it += W;
+        if (it >= n_items) return false;
+        x = load_item(it, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+        if (!x.skip && x.e > x.b) return true;
+    }
+}
+
+// lane j: column id (tier bits kept) and weight of entry base + j of item x
+__device__ __forceinline__ void fetch_window(const Item &x, bool valid, int32_t base,
+                                             const uint32_t *__restrict__ colidx, const float *__restrict__ wts,
+                                             int lane, uint64_t pol, uint32_t &c, float &w) {
+    c = 0;
+    w = 0.f;
+    if (valid && base + lane < x.e - x.b) {
+        c = ld_stream_u32(colidx + x.b + base + lane, pol);
+        w = __uint_as_float(ld_stream_u32(wts + x.b + base + lane, pol));
+    }
+}
+
+// Persistent warps: warp w of W handles items w, w + W, ... as one stream of
+// batches (a batch: up to BE consecutive entries of one item).  Lane j of a
+// batch loads entry j's column id and weight and issues one bulk copy of that
+// row into the warp's slot; the consume side, NS - 1 batches behind, reads the
+// rows from shared memory and accumulates; an item is written out when its
+// last batch is consumed.
+template <typename T, int LPG, int VPT, int BE, int NS, int WPC>
+__global__ void __launch_bounds__(WPC * 32)
     aggregate_kernel(const AggParams p, const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_begin,
                      const int32_t *__restrict__ chunk_end, int64_t n_chunks, float *__restrict__ partial,
                      int64_t pld) {
     constexpr int EPV = 16 / (int)sizeof(T);
     constexpr int GROUPS = 32 / LPG;
-    static_assert(D >= 1 && D <= 32, "ring depth");
-    extern __shared__ uint4 smem_ring[];
+    constexpr int R = LPG * VPT * 16;
+    static_assert(BE <= 32, "one lane per entry of a batch");
+    using Ring = BulkRing<R, BE, NS>;
+    extern __shared__ __align__(16) uint8_t smem_bulk[];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int g = lane / LPG, gl = lane % LPG;
-    uint4 *ring = smem_ring + wib * WarpRing<VPT, D>::kVecs;
-    float *wring = reinterpret_cast<float *>(smem_ring + 8 * WarpRing<VPT, D>::kVecs) + wib * D * 32;
+    uint8_t *rows = smem_bulk + wib * Ring::kRowBytes;
+    float *wring = reinterpret_cast<float *>(smem_bulk + WPC * Ring::kRowBytes) + wib * NS * BE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_bulk + WPC * Ring::kRowBytes + WPC * NS * BE * 4) + wib * NS;
 
-    const int64_t W = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + wib;
+    const int64_t W = (int64_t)gridDim.x * WPC;
+    const int64_t w0 = (int64_t)blockIdx.x * WPC + wib;
     const int64_t n_items = n_chunks + p.n_rows;
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const T *__restrict__ X = static_cast<const T *>(p.X);
     const int64_t f = p.f, ldx = p.ldx;
+    const uint32_t nbytes = (uint32_t)(((f * (int64_t)sizeof(T)) + 15) / 16 * 16);
     const uint32_t *__restrict__ colidx = p.colidx;
     const float *__restrict__ wts = p.wts;
     const uint32_t colmask = p.colmask;
@@ -226,91 +310,123 @@ __global__ void __launch_bounds__(256, MINB)
     const int32_t *__restrict__ rowptr = p.rowptr;
     const int64_t n_rows = p.n_rows;
 
-    // ---- issue side: item it_i, next entry pos_i, column-id batches ----
-    int64_t it_i = w0;
-    Item cur_i = it_i < n_items ? load_item(it_i, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows) : Item{0, 0, 0, false, true};
-    int32_t pos_i = 0, bbase = 0;
-    uint32_t c_cur = 0, c_next = 0;
-    float w_cur = 0.f, w_next = 0.f;
-    bool issue_live = it_i < n_items;
-    // advance the issue side to an item with entries (or the end); load its batches
-    auto settle_issue = [&]() {
-        while (issue_live && (cur_i.skip || pos_i >= cur_i.e - cur_i.b)) {
-            it_i += W;
-            if (it_i >= n_items) {
-                issue_live = false;
-                break;
-            }
-            cur_i = load_item(it_i, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
-            pos_i = 0;
-            if (!cur_i.skip && cur_i.e > cur_i.b) {
-                bbase = 0;
-                load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 0, lane, pol_stream, c_cur,
-                           w_cur);
-                load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 32, lane, pol_stream,
-                           c_next, w_next);
-            }
-        }
-    };
-    if (issue_live && !cur_i.skip && cur_i.e > cur_i.b) {
-        load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 0, lane, pol_stream, c_cur, w_cur);
-        load_batch(colidx, wts, colmask, hot_tier, cur_i.b, cur_i.e - cur_i.b, 32, lane, pol_stream, c_next,
-                   w_next);
-    }
-    settle_issue();
-    int64_t s_issue = 0;  // steps issued (ring slot = s % D)
-    auto issue_step = [&]() {
-        if (!issue_live) return;
-        const int32_t n = cur_i.e - cur_i.b;
-        if (pos_i >= bbase + 32) {
-            bbase += 32;
-            c_cur = c_next;
-            w_cur = w_next;
-            load_batch(colidx, wts, colmask, hot_tier, cur_i.b, n, bbase + 32, lane, pol_stream, c_next, w_next);
-        }
-        const int src = pos_i - bbase + g;
-        const uint32_t cc = __shfl_sync(0xffffffffu, c_cur, src);
-        const float ww = __shfl_sync(0xffffffffu, w_cur, src);
-        const bool live = pos_i + g < n;
-        const int slot = (int)(s_issue % D);
-        uint4 *dst = ring + slot * VPT * 32 + lane;
-        wring[slot * 32 + lane] = live ? ww : 0.f;
-        const T *row = X + (int64_t)(cc & ~kHotBit) * ldx;
-        const uint64_t pol = (cc & kHotBit) ? pol_keep : pol_stream;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-            if (col < f) {
-                if (live)
-                    cp_async16(dst + v * 32, row + col, pol);
-                else
-                    dst[v * 32] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        ++s_issue;
-        pos_i += GROUPS;
-        settle_issue();
-    };
+    if (lane == 0)
+        for (int s = 0; s < NS; ++s) bar_init(&bars[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    // ---- issue side ----
+    // The column ids and weights of the next 64 entries of the current item
+    // sit in registers (lane j holds entry wb + j in (ic0, iw0) and wb + 32 + j
+    // in (ic1, iw1)); the next item with its first 32 ids is fetched one item
+    // ahead.  Issuing a batch therefore never waits on an index load.
+    Item ci = Item{0, 0, 0, false, true}, ni = Item{0, 0, 0, false, true};
+    int64_t it_i = w0 - W;
+    bool more = next_work_item(it_i, ci, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+    int64_t it_n = it_i;
+    bool nmore = more && next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr,
+                                        n_rows);
+    int32_t off_i = 0, wb = 0;
+    uint32_t ic0, ic1, nc0;
+    float iw0, iw1, nw0;
+    fetch_window(ci, more, 0, colidx, wts, lane, pol_stream, ic0, iw0);
+    fetch_window(ci, more, 32, colidx, wts, lane, pol_stream, ic1, iw1);
+    fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);
+    int64_t s_i = 0;
+    bool ok = true;
+
+#define GNN_ISSUE_BATCH()                                                                                   \
+    do {                                                                                                    \
+        if (!more) break;                                                                                   \
+        const int slot = (int)(s_i % NS);                                                                   \
+        const int32_t n_ci = ci.e - ci.b;                                                                   \
+        const int32_t left = n_ci - off_i;                                                                  \
+        const int cnt = left < BE ? left : BE;                                                              \
+        const int src = (off_i - wb + lane) & 31;                                                           \
+        const uint32_t raw = __shfl_sync(0xffffffffu, ic0, src);                                            \
+        const float wv = __shfl_sync(0xffffffffu, iw0, src);                                                \
+        const bool live = lane < cnt;                                                                       \
+        if (lane < BE) wring[slot * BE + lane] = live ? wv : 0.f;                                           \
+        if (lane == 0) bar_expect(&bars[slot], (uint32_t)cnt * nbytes);                                     \
+        __syncwarp();                                                                                       \
+        if (live) {                                                                                         \
+            const uint32_t col = raw & colmask;                                                             \
+            const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;                            \
+            bulk_copy_row(rows + (slot * BE + lane) * R, X + (int64_t)col * ldx, nbytes, &bars[slot],        \
+                          tier <= hot_tier ? pol_keep : pol_stream);                                        \
+        }                                                                                                   \
+        ++s_i;                                                                                              \
+        off_i += BE;                                                                                        \
+        if (off_i >= n_ci) {                                                                                \
+            more = nmore;                                                                                   \
+            if (more) {                                                                                     \
+                ci = ni;                                                                                    \
+                off_i = 0;                                                                                  \
+                wb = 0;                                                                                     \
+                ic0 = nc0;                                                                                  \
+                iw0 = nw0;                                                                                  \
+                fetch_window(ci, true, 32, colidx, wts, lane, pol_stream, ic1, iw1);                        \
+                nmore = next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end,   \
+                                       rowptr, n_rows);                                                     \
+                fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);                        \
+            }                                                                                               \
+        } else if (off_i >= wb + 32) {                                                                      \
+            wb += 32;                                                                                       \
+            ic0 = ic1;                                                                                      \
+            iw0 = iw1;                                                                                      \
+            fetch_window(ci, true, wb + 32, colidx, wts, lane, pol_stream, ic1, iw1);                      \
+        }                                                                                                   \
+    } while (0)
+
+#pragma unroll 1
+    for (int s = 0; s < NS; ++s) GNN_ISSUE_BATCH();
 
     // ---- consume side ----
-    const uint64_t pol_out = pol_stream;
     float acc[VPT][EPV];
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
-
-    // finish item x (id it): reduce the lane groups and write the row or the partial
-    auto finish = [&](const Item &x, int64_t it) {
+    int64_t s_c = 0;
+#pragma unroll 1
+    for (int64_t it_c = w0; it_c < n_items && ok; it_c += W) {
+        const Item x = load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+        if (x.skip) continue;
+#pragma unroll 1
+        for (int32_t off = 0; off < x.e - x.b; off += BE) {
+            const int slot = (int)(s_c % NS);
+            if (!bar_wait(&bars[slot], (uint32_t)((s_c / NS) & 1))) {
+                ok = false;
+                break;
+            }
+            const int32_t left = x.e - x.b - off;
+            const int cnt = left < BE ? left : BE;
+            const uint8_t *sr = rows + slot * BE * R;
+            if (cnt == BE) {  // full batch: no per-row predicate
 #pragma unroll
-        for (int off = LPG; off < 32; off <<= 1)
+                for (int j = 0; j < BE; j += GROUPS)
+                    accumulate_row<T, LPG, VPT>(acc, sr + (j + g) * R, wring[slot * BE + j + g], gl);
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < cnt; j += GROUPS)
+                    if (j + g < cnt) accumulate_row<T, LPG, VPT>(acc, sr + (j + g) * R, wring[slot * BE + j + g], gl);
+            }
+            ++s_c;
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            GNN_ISSUE_BATCH();
+        }
+        if (!ok) break;
+        // finish the item: reduce the lane groups, write the row or the partial
+#pragma unroll
+        for (int o = LPG; o < 32; o <<= 1)
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                for (int k = 0; k < EPV; ++k) acc[v][k] += __shfl_xor_sync(0xffffffffu, acc[v][k], off);
+                for (int k = 0; k < EPV; ++k) acc[v][k] += __shfl_xor_sync(0xffffffffu, acc[v][k], o);
         if (g == 0) {
             if (x.chunk) {
-                float *dst = partial + it * pld;
+                float *dst = partial + it_c * pld;
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
                     const int64_t col = (int64_t)(v * LPG + gl) * EPV;
@@ -326,7 +442,8 @@ __global__ void __launch_bounds__(256, MINB)
                 T *out = static_cast<T *>(p.out) + x.r * p.ldo;
                 const T *selfrow = nullptr;
                 if (p.self_mode == SELF_COPY) selfrow = X + x.r * ldx;
-                if (p.self_mode == SELF_ADD && x.r < p.n_self) selfrow = static_cast<const T *>(p.self) + x.r * p.ld_self;
+                if (p.self_mode == SELF_ADD && x.r < p.n_self)
+                    selfrow = static_cast<const T *>(p.self) + x.r * p.ld_self;
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
                     const int64_t col = (int64_t)(v * LPG + gl) * EPV;
@@ -341,10 +458,10 @@ __global__ void __launch_bounds__(256, MINB)
 #pragma unroll
                             for (int k = 0; k < EPV; ++k) o[k] += sv[k];
                         } else {
-                            store16(out + col, sv, (int)(f - col), pol_out);
+                            store16(out + col, sv, (int)(f - col), pol_stream);
                         }
                     }
-                    store16(out + p.out_off + col, o, (int)(f - col), pol_out);
+                    store16(out + p.out_off + col, o, (int)(f - col), pol_stream);
                 }
             }
         }
@@ -352,43 +469,14 @@ __global__ void __launch_bounds__(256, MINB)
         for (int v = 0; v < VPT; ++v)
 #pragma unroll
             for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
-    };
-
-    // prologue: D steps in flight
-#pragma unroll 1
-    for (int d = 0; d < D; ++d) {
-        issue_step();
-        cp_async_commit();
     }
-    int64_t it_c = w0;
-    int64_t s_cons = 0;
-#pragma unroll 1
-    while (it_c < n_items) {
-        const Item x = load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
-        if (!x.skip) {
-            const int32_t steps = (x.e - x.b + GROUPS - 1) / GROUPS;
-#pragma unroll 1
-            for (int32_t t = 0; t < steps; ++t) {
-                cp_async_wait<D - 1>();
-                const int slot = (int)(s_cons % D);
-                const float w = wring[slot * 32 + lane];
-                const uint4 *src = ring + slot * VPT * 32 + lane;
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    float xv[EPV];
-                    unpack16(X, src[v * 32], xv);
-#pragma unroll
-                    for (int k = 0; k < EPV; ++k) acc[v][k] = fmaf(w, xv[k], acc[v][k]);
-                }
-                ++s_cons;
-                issue_step();
-                cp_async_commit();
-            }
-            finish(x, it_c);
-        }
-        it_c += W;
+#undef GNN_ISSUE_BATCH
+    if (!ok) {
+        // a copy never completed: report, then let every copy still in flight
+        // land (bounded) before the warp's shared memory is released
+        if (lane == 0 && p.err) atomicOr(p.err, 4);
+        for (int64_t s = s_c; s < s_i; ++s) bar_wait(&bars[s % NS], (uint32_t)((s / NS) & 1));
     }
-    cp_async_wait<0>();
 }
 
 template <typename T>
@@ -445,21 +533,22 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
     }
 }
 
-template <typename T, int LPG, int VPT, int D, int MINB>
+template <typename T, int LPG, int VPT, int BE, int NS, int WPC>
 gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
     const int64_t items = sc.n_chunks + p.n_rows;
     if (items > 0) {
-        const int smem = 8 * WarpRing<VPT, D>::kBytes;
-        auto kern = aggregate_kernel<T, LPG, VPT, D, MINB>;
+        constexpr int R = LPG * VPT * 16;
+        const int smem = WPC * BulkRing<R, BE, NS>::kBytes;
+        auto kern = aggregate_kernel<T, LPG, VPT, BE, NS, WPC>;
         GNN_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         // persistent warps: as many blocks as fit on the GPU at once
         int per_sm = 0;
-        GNN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+        GNN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WPC * 32, smem));
         if (per_sm < 1) per_sm = 1;
         int64_t blocks = (int64_t)num_sms() * per_sm;
-        if (blocks > ceil_div(items, 8)) blocks = ceil_div(items, 8);
-        { kern<<<(unsigned)blocks, 256, smem, s>>>(p, sc.chunk_row, sc.chunk_begin, sc.chunk_end, sc.n_chunks,
-                                                    partial, pld); GNN_LAUNCHED(1); }
+        if (blocks > ceil_div(items, WPC)) blocks = ceil_div(items, WPC);
+        { kern<<<(unsigned)blocks, WPC * 32, smem, s>>>(p, sc.chunk_row, sc.chunk_begin, sc.chunk_end, sc.n_chunks,
+                                                        partial, pld); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
     if (sc.n_heavy > 0) {
@@ -476,15 +565,16 @@ gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, 
     // steps in flight per warp D: D * 512 * VPT bytes of gathered rows per warp;
     // shared memory (8 warps per block) then sets the blocks per SM (MINB)
     const int64_t bytes = p.f * (int64_t)sizeof(T);
-    if (bytes <= 128) return launch_cfg<T, 8, 1, 8, 5>(p, sc, partial, pld, s);
-    if (bytes <= 256) return launch_cfg<T, 16, 1, 8, 5>(p, sc, partial, pld, s);
-    if (bytes <= 512) return launch_cfg<T, 32, 1, 8, 5>(p, sc, partial, pld, s);
-    if (bytes <= 1024) return launch_cfg<T, 32, 2, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 32, 3, 3, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 32, 4, 2, 3>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 32, 5, 2, 3>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 32, 6, 2, 2>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 32, 8, 1, 2>(p, sc, partial, pld, s);
+    // a warp keeps NS batches of BE rows in flight (8-16 KB of shared memory)
+    if (bytes <= 128) return launch_cfg<T, 8, 1, 32, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 256) return launch_cfg<T, 16, 1, 16, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 512) return launch_cfg<T, 32, 1, 8, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1024) return launch_cfg<T, 32, 2, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1536) return launch_cfg<T, 32, 3, 2, 5, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 32, 4, 2, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 32, 5, 2, 3, 4>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 32, 6, 1, 5, 4>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 32, 8, 1, 4, 4>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 
@@ -566,6 +656,7 @@ extern "C" gnn_status gnn_aggregate_forward_noalloc(const gnn_graph *g, const vo
     gnn_status st = noalloc_scratch(&scratch);
     if (st != GNN_OK) return st;
     AggParams p{};
+    p.err = g->err;
     p.rowptr = g->rowptr;
     p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
     p.wts = g->wfwd;

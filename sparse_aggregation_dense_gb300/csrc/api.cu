@@ -349,6 +349,7 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
                                                                       dtype == GNN_BF16); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     AggParams p{};
+    p.err = g->err;
     p.rowptr = g->rowptr;
     p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
     p.wts = g->wfwd;
@@ -423,6 +424,7 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     }
     if (!dH) return GNN_OK;
     AggParams p{};
+    p.err = g->err;
     p.rowptr = g->rowptrT;
     p.colidx = reinterpret_cast<const uint32_t *>(g->colidxT);
     p.wts = g->wbwd;

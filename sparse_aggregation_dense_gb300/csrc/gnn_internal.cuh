@@ -157,6 +157,7 @@ struct AggParams {
     const void *self;        // SELF_ADD source (row stride ld_self)
     int64_t ld_self;
     int64_t n_self;
+    int *err;                // device error word (a gather that never completed sets bit 4)
 };
 gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s);
 size_t aggregate_partial_bytes(const Schedule &sc, int64_t f);
