@@ -235,6 +235,12 @@ int64_t gnn_launch_count(void);
 /* Static text for a status code. */
 const char *gnn_status_string(gnn_status s);
 
+/* Static text of the last CUDA runtime error behind a GNN_ECUDA (or
+ * GNN_ENOMEM) status returned by any call in this process, e.g. "an illegal
+ * memory access was encountered"; "no error" if there was none.  Process-wide,
+ * not per thread or per graph: read it right after the failing call. */
+const char *gnn_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

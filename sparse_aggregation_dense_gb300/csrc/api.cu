@@ -149,6 +149,8 @@ const char *gnn_status_string(gnn_status s) {
     return "unknown status";
 }
 
+const char *gnn_last_cuda_error(void) { return last_cuda_error_text(); }
+
 int64_t gnn_sage_half_offset(int64_t f, gnn_dtype dtype) {
     return round_up(f, dtype == GNN_BF16 ? 8 : 4);
 }
@@ -287,10 +289,10 @@ gnn_status gnn_graph_copy_transpose(const gnn_graph *g, int32_t *rowptrT, int32_
 
 gnn_status gnn_get_error(gnn_graph *g) {
     if (!g) return GNN_EINVAL;
-    if (cudaDeviceSynchronize() != cudaSuccess) return GNN_ECUDA;
+    GNN_CUDA_TRY(cudaDeviceSynchronize());
     int v = 0;
-    if (cudaMemcpy(&v, g->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GNN_ECUDA;
-    if (cudaMemset(g->err, 0, sizeof(int)) != cudaSuccess) return GNN_ECUDA;
+    GNN_CUDA_TRY(cudaMemcpy(&v, g->err, sizeof(int), cudaMemcpyDeviceToHost));
+    GNN_CUDA_TRY(cudaMemset(g->err, 0, sizeof(int)));
     return v ? GNN_EINDEX : GNN_OK;
 }
 

@@ -85,6 +85,8 @@ namespace gnn {
     } while (0)
 
 gnn_status cuda_status(cudaError_t e);
+// text of the last CUDA runtime error cuda_status saw (gnn_last_cuda_error)
+const char *last_cuda_error_text();
 // process-wide count of kernel launches (gnn_launch_count)
 void count_launches(int64_t n);
 #define GNN_LAUNCHED(n) gnn::count_launches(n)

@@ -13,21 +13,35 @@ namespace {
 
 constexpr uint32_t kCountMask = 3u;  // low bits of a claim word: 0, 1 or 2 (= repeated)
 
-// copy bytes [0, nbytes) of one row; full 16-byte vectors then an element tail
+constexpr int kRowsPerGroup = 8;  // rows a lane group moves at once (their loads are all in flight)
+
+// Copy rows src_row(k) -> dst_row(k) for the kRowsPerGroup rows of a lane
+// group; a row with a null source or destination is skipped.  Full 16-byte
+// vectors first (all rows' loads issued before the stores), then the tail.
 template <int LPR>
-__device__ __forceinline__ void copy_row(const char *__restrict__ src, char *__restrict__ dst, int64_t nbytes, int es,
-                                         int sub) {
+__device__ __forceinline__ void copy_rows(const char *const (&src)[kRowsPerGroup], char *const (&dst)[kRowsPerGroup],
+                                          int64_t nbytes, int es, int sub) {
     const int64_t nvec = nbytes / 16;
-    for (int64_t q = sub; q < nvec; q += LPR)
-        reinterpret_cast<uint4 *>(dst)[q] = __ldg(reinterpret_cast<const uint4 *>(src) + q);
-    const int64_t tail0 = nvec * 16;
+    for (int64_t q = sub; q < nvec; q += LPR) {
+        uint4 v[kRowsPerGroup];
+#pragma unroll
+        for (int k = 0; k < kRowsPerGroup; ++k)
+            if (src[k] && dst[k]) v[k] = __ldg(reinterpret_cast<const uint4 *>(src[k]) + q);
+#pragma unroll
+        for (int k = 0; k < kRowsPerGroup; ++k)
+            if (src[k] && dst[k]) reinterpret_cast<uint4 *>(dst[k])[q] = v[k];
+    }
     if (sub == 0) {
-        if (es == 4) {
-            for (int64_t b = tail0; b < nbytes; b += 4)
-                *reinterpret_cast<uint32_t *>(dst + b) = *reinterpret_cast<const uint32_t *>(src + b);
-        } else {
-            for (int64_t b = tail0; b < nbytes; b += 2)
-                *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
+        const int64_t tail0 = nvec * 16;
+        for (int k = 0; k < kRowsPerGroup; ++k) {
+            if (!src[k] || !dst[k]) continue;
+            if (es == 4) {
+                for (int64_t b = tail0; b < nbytes; b += 4)
+                    *reinterpret_cast<uint32_t *>(dst[k] + b) = *reinterpret_cast<const uint32_t *>(src[k] + b);
+            } else {
+                for (int64_t b = tail0; b < nbytes; b += 2)
+                    *reinterpret_cast<uint16_t *>(dst[k] + b) = *reinterpret_cast<const uint16_t *>(src[k] + b);
+            }
         }
     }
 }
@@ -38,15 +52,27 @@ __global__ void __launch_bounds__(256) pull_kernel(const char *__restrict__ tabl
                                                    char *__restrict__ H, int64_t row_bytes_h, int64_t row0,
                                                    int64_t nbytes, int es, int *err) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t i = t / LPR;
+    const int64_t i0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
-    if (i >= n_ids) return;
-    const int64_t id = __ldg(ids + i);
-    if (id < 0 || id >= n_table) {
-        if (sub == 0) atomicOr(err, 1);
-        return;
+    if (i0 >= n_ids) return;
+    const char *src[kRowsPerGroup];
+    char *dst[kRowsPerGroup];
+#pragma unroll
+    for (int k = 0; k < kRowsPerGroup; ++k) {
+        src[k] = nullptr;
+        dst[k] = nullptr;
+        const int64_t i = i0 + k;
+        if (i < n_ids) {
+            const int64_t id = __ldg(ids + i);
+            if (id < 0 || id >= n_table) {
+                if (sub == 0) atomicOr(err, 1);
+            } else {
+                src[k] = table + id * row_bytes_t;
+                dst[k] = H + (row0 + i) * row_bytes_h;
+            }
+        }
     }
-    copy_row<LPR>(table + id * row_bytes_t, H + (row0 + i) * row_bytes_h, nbytes, es, sub);
+    copy_rows<LPR>(src, dst, nbytes, es, sub);
 }
 
 // claim word = (generation << 2) | min(count, 2)
@@ -77,17 +103,27 @@ __global__ void __launch_bounds__(256) push_copy_kernel(const char *__restrict__
                                                         char *__restrict__ table, int64_t row_bytes_t, int64_t nbytes,
                                                         int es, int *err) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t v = t / LPR;
+    const int64_t v0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
-    if (v >= n) return;
-    const int64_t id = __ldg(ids + v);
-    if (id < 0 || id >= n_table) return;  // reported by the claim pass
-    const uint32_t w = claim[id];
-    if (w != ((gen << 2) | 1u)) {
-        if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
-        return;
+    if (v0 >= n) return;
+    const char *src[kRowsPerGroup];
+    char *dst[kRowsPerGroup];
+#pragma unroll
+    for (int k = 0; k < kRowsPerGroup; ++k) {
+        src[k] = nullptr;
+        dst[k] = nullptr;
+        const int64_t v = v0 + k;
+        if (v >= n) continue;
+        const int64_t id = __ldg(ids + v);
+        if (id < 0 || id >= n_table) continue;  // reported by the claim pass
+        if (claim[id] != ((gen << 2) | 1u)) {
+            if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
+            continue;
+        }
+        src[k] = H + v * row_bytes_h;
+        dst[k] = table + id * row_bytes_t;
     }
-    copy_row<LPR>(H + v * row_bytes_h, table + id * row_bytes_t, nbytes, es, sub);
+    copy_rows<LPR>(src, dst, nbytes, es, sub);
 }
 
 int lanes_per_row(int64_t nbytes) {
@@ -118,7 +154,7 @@ gnn_status launch_pull(const void *table, int64_t ld_t, int64_t n_table, const i
     const int lpr = lanes_per_row(nbytes);
     return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
         constexpr int LPR = decltype(L)::value;
-        const int64_t blocks = ceil_div(n_ids * LPR, 256);
+        const int64_t blocks = ceil_div(ceil_div(n_ids, kRowsPerGroup) * LPR, 256);
         { pull_kernel<LPR><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const char *>(table), ld_t * es, n_table, ids,
                                                           n_ids, static_cast<char *>(H), ld_h * es, row0, nbytes, es,
                                                           err); GNN_LAUNCHED(1); }
@@ -158,7 +194,7 @@ gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows
     const int lpr = lanes_per_row(nbytes);
     return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
         constexpr int LPR = decltype(L)::value;
-        const int64_t blocks = ceil_div(n_rows * LPR, 256);
+        const int64_t blocks = ceil_div(ceil_div(n_rows, kRowsPerGroup) * LPR, 256);
         { push_copy_kernel<LPR><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const char *>(H), ld_h * es, ids, n_rows,
                                                                n_table, g->claim, gen, static_cast<char *>(table),
                                                                ld_t * es, nbytes, es, g->err); GNN_LAUNCHED(1); }

@@ -6,14 +6,26 @@
 // Communication in Graph Neural Network Training", GNN section) prescribes for a
 // training algorithm that works on directed graphs; entries of a transpose row
 // are ordered by ascending source row, so every later pass is deterministic.
+#include <atomic>
+
 #include "gnn_internal.cuh"
 
 namespace gnn {
 
+namespace {
+std::atomic<int> g_last_cuda_error{0};  // cudaError_t of the last failed runtime call
+}
+
 gnn_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return GNN_OK;
+    g_last_cuda_error.store((int)e, std::memory_order_relaxed);
     if (e == cudaErrorMemoryAllocation) return GNN_ENOMEM;
     return GNN_ECUDA;
+}
+
+const char *last_cuda_error_text() {
+    const int e = g_last_cuda_error.load(std::memory_order_relaxed);
+    return e ? cudaGetErrorString((cudaError_t)e) : "no error";
 }
 
 // ---------------------------------------------------------------------------

@@ -9,7 +9,8 @@
 //               128 x N_pad x 16 into one of two TMEM accumulators
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the 32
 //               TMEM lanes of its quarter, each thread one row), ReLU, round to
-//               bf16, store; then the accumulator is handed back to the MMA warp
+//               bf16 into a swizzled 32 x 64 staging tile, TMA store of the tile;
+//               then the accumulator is handed back to the MMA warp
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs
 // of tile i + 1.  Every wait is bounded (see tc_common.cuh).
 #include <cudaTypedefs.h>
@@ -27,6 +28,8 @@ constexpr int kTileBytes = kBM * kBK * 2;
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;
 constexpr size_t kSmemLimit = 227 * 1024;
+constexpr int kStageOut = 32 * 128;           // one 32-row x 64-column bf16 output tile
+constexpr int kOutBytes = 4 * 2 * kStageOut;  // 4 epilogue warps x 2 buffers
 
 struct Bars {
     uint64_t full[kMaxStages];
@@ -46,14 +49,15 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     update_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                         __nv_bfloat16 *__restrict__ out, int64_t ld_out, int64_t M, int N, int N_pad, int KC,
-                         int stages, int relu, int64_t n_tiles, int *err) {
+                         const __grid_constant__ CUtensorMap mapO, int64_t M, int N, int N_pad, int KC, int stages,
+                         int relu, int64_t n_tiles, int *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
     const int w_chunk = N_pad * 128;
     uint8_t *sA = sW + KC * w_chunk;
-    Bars *bars = reinterpret_cast<Bars *>(sA + stages * kTileBytes);
+    uint8_t *sO = sA + stages * kTileBytes;  // 1024-aligned: W chunks and A tiles are multiples of 1 KB
+    Bars *bars = reinterpret_cast<Bars *>(sO + kOutBytes);
     volatile int *abort_flag = &bars->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,34 +170,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        int acc = 0;
+        uint8_t *stage_out = sO + (warp - 2) * 2 * kStageOut;
+        int acc = 0, ob = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
             if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, abort_flag)) break;
             tc::tc_fence_after();
-            const int64_t row = t * kBM + q * 32 + lane;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride;
-            __nv_bfloat16 *orow = out + row * ld_out;
-            for (int c = 0; c < N_pad; c += 16) {
-                uint32_t r[16];
-                tc::tmem_ld16(taddr + (uint32_t)c, r);
-                if (row < M && c < N) {
+            for (int cc = 0; cc < N_pad; cc += 64) {
+                // the TMA store that last read this buffer must be done with it
+                if (lane == 0) tc::bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t *buf = stage_out + ob * kStageOut;
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    const int c = cc + sub * 16;
+                    uint32_t r[16];
+                    if (c < N_pad) {
+                        tc::tmem_ld16(taddr + (uint32_t)c, r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = 0u;
+                    }
                     float v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        float x = __uint_as_float(r[i]);
+                        const float x = __uint_as_float(r[i]);
                         v[i] = (relu && !(x > 0.f)) ? 0.f : x;
                     }
-                    if (c + 16 <= N) {
-                        uint4 lo = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
-                        uint4 hi = make_uint4(pack2(v[8], v[9]), pack2(v[10], v[11]), pack2(v[12], v[13]),
-                                              pack2(v[14], v[15]));
-                        reinterpret_cast<uint4 *>(orow + c)[0] = lo;
-                        reinterpret_cast<uint4 *>(orow + c)[1] = hi;
-                    } else {
-                        for (int i = 0; i < 16 && c + i < N; ++i) orow[c + i] = __float2bfloat16_rn(v[i]);
-                    }
+                    // 16-byte chunks 2*sub and 2*sub+1 of this thread's 128-byte row, 128-byte swizzle
+                    uint4 lo = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+                    uint4 hi = make_uint4(pack2(v[8], v[9]), pack2(v[10], v[11]), pack2(v[12], v[13]),
+                                          pack2(v[14], v[15]));
+                    uint8_t *rowp = buf + lane * 128;
+                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub) ^ (lane & 7)) * 16)) = lo;
+                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub + 1) ^ (lane & 7)) * 16)) = hi;
                 }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(&mapO, cc, (int32_t)(t * kBM + q * 32), buf);
+                    tc::bulk_commit();
+                }
+                ob ^= 1;
             }
             tc::tc_fence_before();
             __syncwarp();
@@ -203,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) tc::bulk_wait<0>();
+        __syncwarp();
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -270,7 +291,7 @@ bool update_fwd_tc_supported(int64_t Kp, int64_t N) {
     const int64_t KC = ceil_div(Kp, kBK);
     if (N_pad > 256 || KC < 1) return false;
     const size_t w = (size_t)KC * N_pad * 128;
-    return w + 2 * kTileBytes + sizeof(Bars) + 1024 <= kSmemLimit;
+    return w + 2 * kTileBytes + kOutBytes + sizeof(Bars) + 1024 <= kSmemLimit;
 }
 
 gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w,
@@ -281,21 +302,21 @@ gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t 
     __nv_bfloat16 *Wt = static_cast<__nv_bfloat16 *>(wt_ws);
     { pack_wt_bf16_kernel<<<(unsigned)ceil_div(N_pad * K_pad, 256), 256, 0, s>>>(Wp, ld_w, Kp, N, K_pad, N_pad, Wt); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
-    CUtensorMap mapA, mapB;
+    CUtensorMap mapA, mapB, mapO;
     if (!make_map_bf16_2d(&mapA, Z, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_z * 2, kBK, kBM)) return GNN_ECUDA;
     if (!make_map_bf16_2d(&mapB, Wt, (uint64_t)K_pad, (uint64_t)N_pad, (uint64_t)K_pad * 2, kBK, (uint32_t)N_pad))
         return GNN_ECUDA;
+    if (!make_map_bf16_2d(&mapO, out, (uint64_t)N, (uint64_t)n, (uint64_t)ld_o * 2, 64, 32)) return GNN_ECUDA;
     const size_t w_bytes = (size_t)KC * N_pad * 128;
-    int stages = (int)((kSmemLimit - w_bytes - sizeof(Bars) - 1024) / kTileBytes);
+    int stages = (int)((kSmemLimit - w_bytes - kOutBytes - sizeof(Bars) - 1024) / kTileBytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return GNN_EUNSUPPORTED;
-    const size_t smem = w_bytes + (size_t)stages * kTileBytes + sizeof(Bars) + 1024;
+    const size_t smem = w_bytes + (size_t)stages * kTileBytes + kOutBytes + sizeof(Bars) + 1024;
     GNN_CUDA_TRY(cudaFuncSetAttribute(update_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const int64_t n_tiles = ceil_div(n, kBM);
     const int64_t grid = n_tiles < num_sms() ? n_tiles : num_sms();
-    { update_fwd_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(mapA, mapB, static_cast<__nv_bfloat16 *>(out), ld_o, n,
-                                                                (int)N, (int)N_pad, (int)KC, stages, relu, n_tiles,
-                                                                err); GNN_LAUNCHED(1); }
+    { update_fwd_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(mapA, mapB, mapO, n, (int)N, (int)N_pad, (int)KC,
+                                                                stages, relu, n_tiles, err); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

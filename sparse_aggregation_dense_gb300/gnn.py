@@ -28,7 +28,7 @@ GNN_AGG_GCN_SYM, GNN_AGG_SAGE_MEAN = 0, 1
 EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
     "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
-    "gnn_graph_copy_transpose", "gnn_status_string", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+    "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc",
 )
 
@@ -38,7 +38,10 @@ PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
 class GnnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {_lib().gnn_status_string(status).decode()} (status {status})")
+        msg = f"{what}: {_lib().gnn_status_string(status).decode()} (status {status})"
+        if status in (GNN_ECUDA, GNN_ENOMEM):
+            msg += f": {last_cuda_error()}"
+        super().__init__(msg)
 
 
 _L = None
@@ -70,6 +73,8 @@ def _lib():
         L.gnn_launch_count.argtypes = []
         L.gnn_launch_count.restype = i64
         L.gnn_status_string.argtypes = [i32]
+        L.gnn_last_cuda_error.argtypes = []
+        L.gnn_last_cuda_error.restype = ctypes.c_char_p
         L.gnn_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
             if name not in ("gnn_sage_half_offset", "gnn_status_string", "gnn_launch_count"):
@@ -156,6 +161,11 @@ def graph_destroy(g: Graph):
 def get_error(g: Graph) -> int:
     """Synchronise; return (and clear) the graph's device error status."""
     return int(_lib().gnn_get_error(ctypes.c_void_p(g.handle)))
+
+
+def last_cuda_error() -> str:
+    """Text of the last CUDA runtime error behind a GNN_ECUDA status."""
+    return _lib().gnn_last_cuda_error().decode()
 
 
 def graph_copy_transpose(g: Graph):

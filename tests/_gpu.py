@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from sparse_aggregation_dense_gb300 import ld_for
+from sparse_aggregation_dense_gb300 import gnn, ld_for
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
@@ -102,3 +102,9 @@ def column_subset(rowptr: np.ndarray, colidx: np.ndarray, rows: np.ndarray, n_co
     cmap = -np.ones(n_cols, np.int64)
     cmap[cols] = np.arange(cols.shape[0])
     return cols, cmap
+
+
+def assert_ok(g) -> None:
+    """The graph's device error status is clean; on a CUDA failure, say which."""
+    st = gnn.get_error(g)
+    assert st == gnn.GNN_OK, f"status {st}: {gnn.last_cuda_error() if st == gnn.GNN_ECUDA else 'device error word set'}"

@@ -15,7 +15,7 @@ import oracle
 import synth
 from synth.configs import TINY, WORKLOADS
 from sparse_aggregation_dense_gb300 import PartitionModel, gnn, ld_for, padded
-from tests._gpu import (TOL, close, close_mostly, column_subset, gen_matrix, maybe_round, sample_with_heavy, to_device, to_host,
+from tests._gpu import (TOL, assert_ok, close, close_mostly, column_subset, gen_matrix, maybe_round, sample_with_heavy, to_device, to_host,
                         torch_dtype, widen)
 
 pytestmark = pytest.mark.gpu
@@ -102,7 +102,7 @@ def test_pull_push_bit_exact(case):
     table = to_device(table_h, dt, f)
     H = padded(part.n_total, f, tdt, "cuda")
     gnn.halo_pull(g, table, torch.from_numpy(part.halo_ids).cuda(), H)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     H_ref = np.zeros((part.n_total, table_h.shape[1]), dtype=table_h.dtype)
     assert oracle.halo_pull(table_h, part.halo_ids, H_ref, part.n_local, f) == oracle.OK
     np.testing.assert_array_equal(_bits(H[part.n_local:]), H_ref[part.n_local:, :f].view(
@@ -111,7 +111,7 @@ def test_pull_push_bit_exact(case):
     out_h = gen_matrix(part.n_local, f, dt, SEED, 77, "normal")
     out = to_device(out_h, dt, f)
     gnn.halo_push(g, out, torch.from_numpy(part.local_ids).cuda(), table)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     ref = table_h.copy()
     assert oracle.halo_push(out_h, part.n_local, f, part.local_ids, ref) == oracle.OK
     np.testing.assert_array_equal(_bits(table), ref[:, :f].view(np.int16 if dt == "bf16" else np.int32))
@@ -144,7 +144,7 @@ def test_forward_layer(case):
     Z.as_strided((part.n_local, Z.stride(0)), (Z.stride(0), 1)).fill_(7.0)  # padding must come back zero
     Hout = padded(part.n_local, f_out, tdt, "cuda")
     gnn.layer_forward(g, H, torch.from_numpy(W).cuda(), relu, Z, Hout)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     if is_sampled(size, name):
         rows = sample_with_heavy(part.rowptr, 1500, SEED)
         cols, cmap = column_subset(part.rowptr, part.colidx, rows, part.n_total)
@@ -225,7 +225,7 @@ def test_backward_layer(case):
     dZ = padded(nL, Kp, tdt, "cuda")
     dH = padded(nT, f_in, tdt, "cuda")
     gnn.layer_backward(g, G, Ho, Z, torch.from_numpy(W).cuda(), relu, dW, f_in, dZ=dZ, dH=dH, want_halo_grad=True)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     tol = TOL[dt]
     Wr = maybe_round(W.astype(np.float64), dt)
     Gw, How = widen(G_h, dt, f_out), widen(Ho_h, dt, f_out)
@@ -382,7 +382,7 @@ def _run_layer_pair(part, g, agg, dt, f_in, f_out, relu, seed=3):
     dZ = padded(nL, Kp, tdt, "cuda")
     dH = padded(nT, f_in, tdt, "cuda")
     gnn.layer_backward(g, to_device(G_h, dt, f_out), Ho, Z, Wd, relu, dW, f_in, dZ=dZ, dH=dH, want_halo_grad=True)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     Zc = np.concatenate([Zg[:, :f_in], Zg[:, half:half + f_in]], axis=1) if sage else Zg
     dWr, dZr = oracle.update_backward(widen(G_h, dt, f_out), to_host(Ho), Zc, maybe_round(W.astype(np.float64), dt),
                                       relu)
@@ -459,7 +459,7 @@ def test_bad_ids_are_reported_and_rows_left_alone():
     H.fill_(-3.0)
     gnn.halo_pull(g, table, torch.from_numpy(ids).cuda(), H)
     assert gnn.get_error(g) == gnn.GNN_EINDEX
-    assert gnn.get_error(g) == gnn.GNN_OK  # cleared
+    assert_ok(g)  # cleared
     Hh = H.cpu().numpy()
     assert np.all(Hh[part.n_local + 5] == -3.0) and np.all(Hh[part.n_local + 6] == -3.0)
     good = [i for i in range(part.n_halo) if i not in (5, 6)]
@@ -477,7 +477,7 @@ def test_bad_ids_are_reported_and_rows_left_alone():
     np.testing.assert_array_equal(after[lids[ok]], out_h[ok, :f])
     # a second, clean push after the failed one works (claim generations advance)
     gnn.halo_push(g, to_device(out_h, "f32", f), torch.from_numpy(part.local_ids).cuda(), table)
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
     np.testing.assert_array_equal(table.cpu().numpy()[part.local_ids], out_h[:, :f])
 
 

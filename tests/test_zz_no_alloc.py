@@ -21,7 +21,7 @@ import torch
 import synth
 from synth.configs import WORKLOADS
 from sparse_aggregation_dense_gb300 import gnn, padded
-from tests._gpu import TOL, close, gen_matrix, to_device, to_host, torch_dtype
+from tests._gpu import TOL, assert_ok, close, gen_matrix, to_device, to_host, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def test_noalloc_matches_layer_forward_twice(rmat_graph, dt, f):
         Z = padded(part.n_local, f, tdt, "cuda")
         Z.fill_(float("nan"))
         gnn.aggregate_forward_noalloc(g, H, Z)
-        assert gnn.get_error(g) == gnn.GNN_OK
+        assert_ok(g)
         got = to_host(Z)
         close(got, ref, TOL[dt], f"no-alloc Z, call {call + 1}")
         assert np.array_equal(got, ref)  # same kernels, same order: identical bits
@@ -63,4 +63,4 @@ def test_noalloc_rejects_partials_beyond_its_array(rmat_graph):
     st = lib.gnn_aggregate_forward_noalloc(ctypes.c_void_p(g.handle), ptr, 2048, 2048, ptr, 2048, gnn.GNN_BF16,
                                            None)
     assert st == gnn.GNN_EUNSUPPORTED
-    assert gnn.get_error(g) == gnn.GNN_OK
+    assert_ok(g)
