@@ -666,6 +666,7 @@ extern "C" gnn_status gnn_aggregate_forward_noalloc(const gnn_graph *g, const vo
     p.hot_tier = hot_tier_for(g->fwd, round_up(f * elem_size(dtype), 32));
     p.X = H;
     p.ldx = ld_h;
+    p.n_x = g->n_local + g->n_halo;
     p.f = f;
     p.self_mode = sage ? SELF_COPY : SELF_NONE;
     p.out = Z;

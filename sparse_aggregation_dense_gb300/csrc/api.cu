@@ -361,6 +361,7 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
     p.hot_tier = hot_tier_for(g->fwd, round_up(f_in * elem_size(dtype), 32));
     p.X = H;
     p.ldx = ld_h;
+    p.n_x = nT;
     p.f = f_in;
     p.self_mode = sage ? SELF_COPY : SELF_NONE;
     p.out = Z;
@@ -439,6 +440,7 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     p.ldo = ld_dh;
     p.out_off = 0;
     p.ldx = ld_dz;
+    p.n_x = nL;
     if (sage) {
         p.self_mode = SELF_ADD;
         p.X = static_cast<const char *>(dZ) + half * elem_size(dtype);

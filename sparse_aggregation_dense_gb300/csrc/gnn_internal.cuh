@@ -151,6 +151,7 @@ struct AggParams {
     int hot_tier;            // entries with tier <= hot_tier are gathered with evict_last
     const void *X;
     int64_t ldx;
+    int64_t n_x;             // rows of X: every column id is below it
     int64_t f;
     int self_mode;
     void *out;
@@ -159,7 +160,7 @@ struct AggParams {
     const void *self;        // SELF_ADD source (row stride ld_self)
     int64_t ld_self;
     int64_t n_self;
-    int *err;                // device error word (a gather that never completed sets bit 4)
+    int *err;                // device error word
 };
 gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s);
 size_t aggregate_partial_bytes(const Schedule &sc, int64_t f);

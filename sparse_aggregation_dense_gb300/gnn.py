@@ -77,7 +77,7 @@ def _lib():
         L.gnn_last_cuda_error.restype = ctypes.c_char_p
         L.gnn_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
-            if name not in ("gnn_sage_half_offset", "gnn_status_string", "gnn_launch_count"):
+            if name not in ("gnn_sage_half_offset", "gnn_status_string", "gnn_last_cuda_error", "gnn_launch_count"):
                 getattr(L, name).restype = i32
         _L = L
     return _L

@@ -73,3 +73,11 @@ def test_host_side_argument_checks(lib):
     assert lib.gnn_status_string(5) == b"bad index data on the device"
     lib.gnn_last_cuda_error.restype = ctypes.c_char_p
     assert isinstance(lib.gnn_last_cuda_error(), bytes) and lib.gnn_last_cuda_error()
+
+
+def test_binding_reports_cuda_error_text():
+    # the Python binding returns the library's static text, not a raw pointer
+    from sparse_aggregation_dense_gb300 import gnn
+    assert isinstance(gnn.last_cuda_error(), str) and gnn.last_cuda_error()
+    err = gnn.GnnError(gnn.GNN_ECUDA, "call")
+    assert str(err).startswith("call: CUDA runtime error (status 3): ")
