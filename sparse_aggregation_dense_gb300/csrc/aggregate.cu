@@ -18,9 +18,10 @@
 //    a heavy row's partials in chunk order (deterministic, no atomics);
 //  - lanes split a feature row into 16-byte vectors; LPG lanes serve one entry
 //    and the warp serves 32 / LPG entries at once;
-//  - the gathers are software-pipelined: U loads per lane group are always in
-//    flight - each slot is consumed and immediately refilled with the entry U
-//    slots ahead - and the next 32 column ids are loaded one batch ahead;
+//  - the gathers are TMA gathers of four rows (tile::gather4) into a per-warp
+//    shared-memory ring of NS slots (a slot: BE entries), completed on one
+//    mbarrier per slot; the warp consumes one slot while the next NS - 1 are
+//    in flight, and the next 64 column ids sit in registers, fetched ahead;
 //  - L2 residency: column ids carry a hotness tier (access-count rank); rows
 //    of the hottest tiers that fit a share of L2 are loaded with an evict_last
 //    policy, the rest and the streamed ids / weights / outputs with evict_first.
@@ -172,12 +173,16 @@ __device__ __forceinline__ Item load_item(int64_t it, int64_t n_chunks, const in
 }
 
 
-__device__ __forceinline__ void bulk_copy_row(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
-                                              uint64_t pol) {
+// TMA gather of four rows r0..r3 of the tensor behind `map`, columns [x, x + box):
+// the rows land one after another at smem_dst; completion is counted in bytes
+// on the mbarrier
+__device__ __forceinline__ void tma_gather4(void *smem_dst, const CUtensorMap *map, int32_t x, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint64_t *bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-        "l"(gsrc), "r"(bytes), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "l"(pol)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "l"(pol)
         : "memory");
 }
 __device__ __forceinline__ void bar_init(uint64_t *bar) {
@@ -215,7 +220,9 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Shared memory of one warp: NS slots of BE gathered rows (R bytes each), the
-// entries' weights and one mbarrier per slot.
+// entries' weights and one mbarrier per slot.  A slot is laid out box-major:
+// box v (bytes [v * LPG * 16, (v + 1) * LPG * 16) of every row) holds the BE
+// rows one after another, as the TMA gathers deliver them.
 template <int R, int BE, int NS>
 struct BulkRing {
     static constexpr int kRowBytes = NS * BE * R;
@@ -233,12 +240,12 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, f
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
 }
 
-template <typename T, int LPG, int VPT>
+template <typename T, int LPG, int VPT, int BE>
 __device__ __forceinline__ void accumulate_row(float (&acc)[VPT][16 / sizeof(T)], const uint8_t *row, float w, int gl) {
     constexpr int EPV = 16 / (int)sizeof(T);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(row + (v * LPG + gl) * 16);
+        const uint4 q = *reinterpret_cast<const uint4 *>(row + v * (BE * LPG * 16) + gl * 16);
         float xv[EPV];
         unpack16(static_cast<const T *>(nullptr), q, xv);
 #pragma unroll
@@ -274,21 +281,27 @@ __device__ __forceinline__ void fetch_window(const Item &x, bool valid, int32_t 
 
 // Persistent warps: warp w of W handles items w, w + W, ... as one stream of
 // batches (a batch: up to BE consecutive entries of one item).  Lane j of a
-// batch loads entry j's column id and weight and issues one bulk copy of that
-// row into the warp's slot; the consume side, NS - 1 batches behind, reads the
-// rows from shared memory and accumulates; an item is written out when its
-// last batch is consumed.
+// batch holds entry j's column id and weight; every fourth lane gathers its
+// four entries' rows with one TMA gather per box into the warp's slot (a short
+// last group repeats its last row, weighted 0).  The consume side, NS - 1
+// batches behind, reads the rows from shared memory and accumulates; an item
+// is written out when its last batch is consumed.
 template <typename T, int LPG, int VPT, int BE, int NS, int WPC>
 __global__ void __launch_bounds__(WPC * 32)
-    aggregate_kernel(const AggParams p, const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_begin,
-                     const int32_t *__restrict__ chunk_end, int64_t n_chunks, float *__restrict__ partial,
-                     int64_t pld) {
+    aggregate_kernel(const AggParams p, const __grid_constant__ CUtensorMap xmap, const int32_t *__restrict__ chunk_row,
+                     const int32_t *__restrict__ chunk_begin, const int32_t *__restrict__ chunk_end, int64_t n_chunks,
+                     float *__restrict__ partial, int64_t pld) {
     constexpr int EPV = 16 / (int)sizeof(T);
     constexpr int GROUPS = 32 / LPG;
     constexpr int R = LPG * VPT * 16;
-    static_assert(BE <= 32, "one lane per entry of a batch");
+    constexpr int BOX = LPG * 16;  // bytes of one gathered box of a row
+    static_assert(BE <= 32 && BE % 4 == 0 && 32 % BE == 0, "whole groups of four entries inside one id window");
+    static_assert(BOX % 128 == 0, "TMA destinations stay 128-byte aligned");
     using Ring = BulkRing<R, BE, NS>;
-    extern __shared__ __align__(16) uint8_t smem_bulk[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // TMA destinations must be 128-byte aligned: round the dynamic base up
+    // (the launch adds 128 bytes for this)
+    uint8_t *smem_bulk = smem_raw + ((128u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 127u)) & 127u);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int g = lane / LPG, gl = lane % LPG;
     uint8_t *rows = smem_bulk + wib * Ring::kRowBytes;
@@ -302,7 +315,6 @@ __global__ void __launch_bounds__(WPC * 32)
     const uint64_t pol_stream = policy_evict_first();
     const T *__restrict__ X = static_cast<const T *>(p.X);
     const int64_t f = p.f, ldx = p.ldx;
-    const uint32_t nbytes = (uint32_t)(((f * (int64_t)sizeof(T)) + 15) / 16 * 16);
     const uint32_t *__restrict__ colidx = p.colidx;
     const float *__restrict__ wts = p.wts;
     const uint32_t colmask = p.colmask;
@@ -342,18 +354,27 @@ __global__ void __launch_bounds__(WPC * 32)
         const int32_t n_ci = ci.e - ci.b;                                                                   \
         const int32_t left = n_ci - off_i;                                                                  \
         const int cnt = left < BE ? left : BE;                                                              \
-        const int src = (off_i - wb + lane) & 31;                                                           \
+        /* lanes past the batch repeat its last entry: a valid row, weight 0 */                           \
+        const int src = (off_i - wb + (lane < cnt ? lane : cnt - 1)) & 31;                                  \
         const uint32_t raw = __shfl_sync(0xffffffffu, ic0, src);                                            \
         const float wv = __shfl_sync(0xffffffffu, iw0, src);                                                \
-        const bool live = lane < cnt;                                                                       \
-        if (lane < BE) wring[slot * BE + lane] = live ? wv : 0.f;                                           \
-        if (lane == 0) bar_expect(&bars[slot], (uint32_t)cnt * nbytes);                                     \
+        if (lane < BE) wring[slot * BE + lane] = lane < cnt ? wv : 0.f;                                     \
+        const int32_t col = (int32_t)(raw & colmask);                                                       \
+        const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;                                \
+        const uint32_t hot = __ballot_sync(0xffffffffu, lane < cnt && tier <= hot_tier);                    \
+        const int32_t c1 = __shfl_down_sync(0xffffffffu, col, 1);                                           \
+        const int32_t c2 = __shfl_down_sync(0xffffffffu, col, 2);                                           \
+        const int32_t c3 = __shfl_down_sync(0xffffffffu, col, 3);                                           \
+        const int ngr = (cnt + 3) >> 2;                                                                     \
+        if (lane == 0) bar_expect(&bars[slot], (uint32_t)(ngr * VPT * 4 * BOX));                            \
         __syncwarp();                                                                                       \
-        if (live) {                                                                                         \
-            const uint32_t col = raw & colmask;                                                             \
-            const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;                            \
-            bulk_copy_row(rows + (slot * BE + lane) * R, X + (int64_t)col * ldx, nbytes, &bars[slot],        \
-                          tier <= hot_tier ? pol_keep : pol_stream);                                        \
+        if ((lane & 3) == 0 && lane < 4 * ngr) {                                                            \
+            /* keep the group in L2 when most of its rows are hot */                                        \
+            const uint64_t pol = __popc((hot >> lane) & 0xfu) >= 2 ? pol_keep : pol_stream;                 \
+            uint8_t *dst = rows + slot * BE * R + lane * BOX;                                               \
+            _Pragma("unroll") for (int v = 0; v < VPT; ++v)                                                \
+                tma_gather4(dst + v * BE * BOX, &xmap, v * (BOX / (int)sizeof(T)), col, c1, c2, c3,         \
+                            &bars[slot], pol);                                                              \
         }                                                                                                   \
         ++s_i;                                                                                              \
         off_i += BE;                                                                                        \
@@ -405,11 +426,11 @@ __global__ void __launch_bounds__(WPC * 32)
             if (cnt == BE) {  // full batch: no per-row predicate
 #pragma unroll
                 for (int j = 0; j < BE; j += GROUPS)
-                    accumulate_row<T, LPG, VPT>(acc, sr + (j + g) * R, wring[slot * BE + j + g], gl);
+                    accumulate_row<T, LPG, VPT, BE>(acc, sr + (j + g) * BOX, wring[slot * BE + j + g], gl);
             } else {
 #pragma unroll 1
                 for (int j = 0; j < cnt; j += GROUPS)
-                    if (j + g < cnt) accumulate_row<T, LPG, VPT>(acc, sr + (j + g) * R, wring[slot * BE + j + g], gl);
+                    if (j + g < cnt) accumulate_row<T, LPG, VPT, BE>(acc, sr + (j + g) * BOX, wring[slot * BE + j + g], gl);
             }
             ++s_c;
             __syncwarp();
@@ -538,7 +559,13 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
     const int64_t items = sc.n_chunks + p.n_rows;
     if (items > 0) {
         constexpr int R = LPG * VPT * 16;
-        const int smem = WPC * BulkRing<R, BE, NS>::kBytes;
+        const int smem = WPC * BulkRing<R, BE, NS>::kBytes + 128;
+        // the gathered matrix, one row high boxes of LPG * 16 bytes (zero past column f)
+        CUtensorMap xmap;
+        memset(&xmap, 0, sizeof(xmap));
+        if (p.n_x > 0 && !make_map_rows(&xmap, sizeof(T) == 2, p.X, (uint64_t)p.f, (uint64_t)p.n_x,
+                                        (uint64_t)p.ldx * sizeof(T), (uint32_t)(LPG * 16 / (int)sizeof(T))))
+            return GNN_ECUDA;
         auto kern = aggregate_kernel<T, LPG, VPT, BE, NS, WPC>;
         GNN_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         // persistent warps: as many blocks as fit on the GPU at once
@@ -547,8 +574,8 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
         if (per_sm < 1) per_sm = 1;
         int64_t blocks = (int64_t)num_sms() * per_sm;
         if (blocks > ceil_div(items, WPC)) blocks = ceil_div(items, WPC);
-        { kern<<<(unsigned)blocks, WPC * 32, smem, s>>>(p, sc.chunk_row, sc.chunk_begin, sc.chunk_end, sc.n_chunks,
-                                                        partial, pld); GNN_LAUNCHED(1); }
+        { kern<<<(unsigned)blocks, WPC * 32, smem, s>>>(p, xmap, sc.chunk_row, sc.chunk_begin, sc.chunk_end,
+                                                        sc.n_chunks, partial, pld); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
     if (sc.n_heavy > 0) {
@@ -570,11 +597,11 @@ gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, 
     if (bytes <= 256) return launch_cfg<T, 16, 1, 16, 2, 4>(p, sc, partial, pld, s);
     if (bytes <= 512) return launch_cfg<T, 32, 1, 8, 2, 4>(p, sc, partial, pld, s);
     if (bytes <= 1024) return launch_cfg<T, 32, 2, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 32, 3, 2, 5, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 32, 4, 2, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 32, 5, 2, 3, 4>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 32, 6, 1, 5, 4>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 32, 8, 1, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1536) return launch_cfg<T, 32, 3, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 32, 4, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 32, 5, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 32, 6, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 32, 8, 4, 2, 2>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 

@@ -177,6 +177,11 @@ gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t 
 // 2-D bf16 tensor map with 128-byte swizzle (box_inner x box_outer elements)
 bool make_map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                       uint32_t box_inner, uint32_t box_outer);
+// 2-D tensor map over rows of `inner` elements (bf16 or fp32), a box one row
+// high and box_inner elements wide, no swizzle, zero fill past the edges: the
+// map of the matrix the aggregation gathers rows from (TMA gather of 4 rows)
+bool make_map_rows(CUtensorMap *m, bool bf16, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                   uint32_t box_inner);
 int num_sms();
 // Dense update, backward, on the tensor cores (bf16): dZ = dY W^T and the dW
 // partials of each CTA (ws: update_bwd_tc_ws_bytes), then dWp = their sum.
