@@ -12,12 +12,14 @@
 // kernel streams (column id, weight) pairs and gathers feature rows.
 //
 // Design (a gather bound by memory latency and DRAM traffic):
-//  - one warp per work item: a whole light row (<= kHeavyNnz entries) or one
-//    kChunkNnz-entry chunk of a heavy row; chunks are scheduled first so hub
-//    rows spread over all SMs; a chunk writes an fp32 partial and a fix-up adds
-//    a heavy row's partials in chunk order (deterministic, no atomics);
-//  - lanes split a feature row into 16-byte vectors; LPG lanes serve one entry
-//    and the warp serves 32 / LPG entries at once;
+//  - work items: row groups (runs of consecutive light rows, <= kHeavyNnz
+//    entries each, whose entries form one range) and kChunkNnz-entry chunks of
+//    heavy rows; chunks are scheduled first so hub rows spread over all SMs; a
+//    chunk writes an fp32 partial and a fix-up adds a heavy row's partials in
+//    chunk order (deterministic, no atomics);
+//  - a warp streams an item's entries in batches that may span rows; the 32
+//    lanes split a feature row into VW-byte pieces (VPT boxes of 32 * VW bytes)
+//    and walk the batch entry by entry, writing each row out where it ends;
 //  - the gathers are TMA gathers of four rows (tile::gather4) into a per-warp
 //    shared-memory ring of NS slots (a slot: BE entries), completed on one
 //    mbarrier per slot; the warp consumes one slot while the next NS - 1 are
@@ -121,58 +123,6 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *src) {
                        __uint_as_float(v.y & 0xffff0000u));
 }
 
-constexpr uint32_t kHotBit = 0x80000000u;
-
-// one batch of 32 entries: lane i holds (column | hot bit, weight) of entry base + i
-__device__ __forceinline__ void load_batch(const uint32_t *__restrict__ colidx, const float *__restrict__ wts,
-                                           uint32_t colmask, int hot_tier, int32_t b, int32_t n, int32_t base,
-                                           int lane, uint64_t pol_stream, uint32_t &c, float &w) {
-    c = 0;
-    w = 0.f;
-    if (base + lane < n) {
-        const uint32_t raw = ld_stream_u32(colidx + b + base + lane, pol_stream);
-        w = __uint_as_float(ld_stream_u32(wts + b + base + lane, pol_stream));
-        const uint32_t col = raw & colmask;
-        const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;
-        c = col | (tier <= hot_tier ? kHotBit : 0u);
-    }
-}
-
-// One work item: a whole light row or one chunk of a heavy row.
-struct Item {
-    int64_t r;
-    int32_t b, e;
-    bool chunk;
-    bool skip;  // no work for this warp (heavy row in the row range, or past n_rows)
-};
-
-__device__ __forceinline__ Item load_item(int64_t it, int64_t n_chunks, const int32_t *__restrict__ chunk_row,
-                                          const int32_t *__restrict__ chunk_begin,
-                                          const int32_t *__restrict__ chunk_end, const int32_t *__restrict__ rowptr,
-                                          int64_t n_rows) {
-    Item x;
-    if (it < n_chunks) {
-        x.r = chunk_row[it];
-        x.b = chunk_begin[it];
-        x.e = chunk_end[it];
-        x.chunk = true;
-        x.skip = x.r >= n_rows;
-    } else {
-        x.r = it - n_chunks;
-        x.chunk = false;
-        if (x.r < n_rows) {
-            x.b = rowptr[x.r];
-            x.e = rowptr[x.r + 1];
-            x.skip = x.e - x.b > kHeavyNnz;  // handled by its chunks and the fix-up
-        } else {
-            x.b = x.e = 0;
-            x.skip = true;
-        }
-    }
-    return x;
-}
-
-
 // TMA gather of four rows r0..r3 of the tensor behind `map`, columns [x, x + box):
 // the rows land one after another at smem_dst; completion is counted in bytes
 // on the mbarrier
@@ -240,16 +190,135 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, f
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
 }
 
-template <typename T, int LPG, int VPT, int BE>
-__device__ __forceinline__ void accumulate_row(float (&acc)[VPT][16 / sizeof(T)], const uint8_t *row, float w, int gl) {
-    constexpr int EPV = 16 / (int)sizeof(T);
+// One work item: a row group (consecutive light rows, one entry range) or one
+// chunk of a heavy row.  Rows at or past n_rows (halo rows of a transpose whose
+// gradient is not wanted) are cut off.
+struct Item {
+    int32_t r0, r1;  // rows [r0, r1); a chunk: its row, r0 + 1
+    int32_t b, e;    // entries [b, e)
+    bool chunk;
+    bool skip;       // nothing to compute (all its rows at or past n_rows)
+};
+
+__device__ __forceinline__ Item load_item(int64_t it, int64_t n_chunks, const int32_t *__restrict__ chunk_row,
+                                          const int32_t *__restrict__ chunk_begin,
+                                          const int32_t *__restrict__ chunk_end, const int32_t *__restrict__ group_r0,
+                                          const int32_t *__restrict__ group_r1, const int32_t *__restrict__ rowptr,
+                                          int64_t n_rows) {
+    Item x;
+    if (it < n_chunks) {
+        x.r0 = chunk_row[it];
+        x.r1 = x.r0 + 1;
+        x.b = chunk_begin[it];
+        x.e = chunk_end[it];
+        x.chunk = true;
+        x.skip = x.r0 >= n_rows;
+    } else {
+        const int64_t gi = it - n_chunks;
+        x.r0 = group_r0[gi];
+        x.r1 = group_r1[gi];
+        if (x.r1 > n_rows) x.r1 = (int32_t)n_rows;
+        x.chunk = false;
+        x.skip = x.r0 >= x.r1;
+        x.b = x.skip ? 0 : rowptr[x.r0];
+        x.e = x.skip ? 0 : rowptr[x.r1];
+    }
+    return x;
+}
+
+// this lane's VW bytes of a gathered row in shared memory, as 32-bit words
+template <int VW>
+__device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[VW / 4]) {
+    if constexpr (VW == 16) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(p);
+        w[0] = q.x;
+        w[1] = q.y;
+        w[2] = q.z;
+        w[3] = q.w;
+    } else if constexpr (VW == 8) {
+        const uint2 q = *reinterpret_cast<const uint2 *>(p);
+        w[0] = q.x;
+        w[1] = q.y;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    }
+}
+
+// acc += w * (this lane's VW-byte pieces of one gathered row); `row` points at
+// the lane's piece in box 0, box v sits v * BE * 32 * VW bytes further
+template <typename T, int VW, int VPT, int BE>
+__device__ __forceinline__ void accumulate_entry(float (&acc)[VPT][VW / sizeof(T)], const uint8_t *row, float w) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(row + v * (BE * LPG * 16) + gl * 16);
-        float xv[EPV];
-        unpack16(static_cast<const T *>(nullptr), q, xv);
+        uint32_t q[VW / 4];
+        lds_words<VW>(row + v * (BE * 32 * VW), q);
+        if constexpr (sizeof(T) == 2) {
 #pragma unroll
-        for (int k = 0; k < EPV; k += 2) fma2(acc[v][k], acc[v][k + 1], xv[k], xv[k + 1], w);
+            for (int k = 0; k < VW / 4; ++k)
+                fma2(acc[v][2 * k], acc[v][2 * k + 1], __uint_as_float(q[k] << 16), __uint_as_float(q[k] & 0xffff0000u),
+                     w);
+        } else if constexpr (VW >= 8) {
+#pragma unroll
+            for (int k = 0; k < VW / 4; k += 2)
+                fma2(acc[v][k], acc[v][k + 1], __uint_as_float(q[k]), __uint_as_float(q[k + 1]), w);
+        } else {
+            acc[v][0] = fmaf(w, __uint_as_float(q[0]), acc[v][0]);
+        }
+    }
+}
+
+// global <-> registers for this lane's VW bytes (VW / sizeof(T) values)
+template <int VW>
+__device__ __forceinline__ void ldg_words(const void *p, uint32_t (&w)[VW / 4]) {
+    if constexpr (VW == 16) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(p));
+        w[0] = q.x;
+        w[1] = q.y;
+        w[2] = q.z;
+        w[3] = q.w;
+    } else if constexpr (VW == 8) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(p));
+        w[0] = q.x;
+        w[1] = q.y;
+    } else {
+        w[0] = __ldg(reinterpret_cast<const uint32_t *>(p));
+    }
+}
+template <int VW>
+__device__ __forceinline__ void stg_words(void *p, const uint32_t (&w)[VW / 4], uint64_t pol) {
+    if constexpr (VW == 16) {
+        asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "l"(pol)
+                     : "memory");
+    } else if constexpr (VW == 8) {
+        asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(w[0]), "r"(w[1]), "l"(pol)
+                     : "memory");
+    } else {
+        asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(w[0]), "l"(pol) : "memory");
+    }
+}
+template <typename T, int VW>
+__device__ __forceinline__ void words_to_vals(const uint32_t (&w)[VW / 4], float (&v)[VW / sizeof(T)]) {
+#pragma unroll
+    for (int k = 0; k < VW / 4; ++k) {
+        if constexpr (sizeof(T) == 2) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        } else {
+            v[k] = __uint_as_float(w[k]);
+        }
+    }
+}
+// values at or past f_left are stored as 0
+template <typename T, int VW>
+__device__ __forceinline__ void vals_to_words(const float (&v)[VW / sizeof(T)], int f_left, uint32_t (&w)[VW / 4]) {
+#pragma unroll
+    for (int k = 0; k < VW / 4; ++k) {
+        if constexpr (sizeof(T) == 2) {
+            w[k] = pack_bf16x2(2 * k < f_left ? v[2 * k] : 0.f, 2 * k + 1 < f_left ? v[2 * k + 1] : 0.f);
+        } else {
+            w[k] = __float_as_uint(k < f_left ? v[k] : 0.f);
+        }
     }
 }
 
@@ -258,11 +327,13 @@ __device__ __forceinline__ bool next_work_item(int64_t &it, Item &x, int64_t W, 
                                                const int32_t *__restrict__ chunk_row,
                                                const int32_t *__restrict__ chunk_begin,
                                                const int32_t *__restrict__ chunk_end,
+                                               const int32_t *__restrict__ group_r0,
+                                               const int32_t *__restrict__ group_r1,
                                                const int32_t *__restrict__ rowptr, int64_t n_rows) {
     for (;;) {
         it += W;
         if (it >= n_items) return false;
-        x = load_item(it, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+        x = load_item(it, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1, rowptr, n_rows);
         if (!x.skip && x.e > x.b) return true;
     }
 }
@@ -280,21 +351,24 @@ __device__ __forceinline__ void fetch_window(const Item &x, bool valid, int32_t 
 }
 
 // Persistent warps: warp w of W handles items w, w + W, ... as one stream of
-// batches (a batch: up to BE consecutive entries of one item).  Lane j of a
-// batch holds entry j's column id and weight; every fourth lane gathers its
-// four entries' rows with one TMA gather per box into the warp's slot (a short
-// last group repeats its last row, weighted 0).  The consume side, NS - 1
-// batches behind, reads the rows from shared memory and accumulates; an item
-// is written out when its last batch is consumed.
-template <typename T, int LPG, int VPT, int BE, int NS, int WPC>
+// batches (a batch: up to BE consecutive entries of one item, which may span
+// several rows of a row group).  Lane j of a batch holds entry j's column id
+// and weight; every fourth lane gathers its four entries' rows with one TMA
+// gather per box into the warp's slot (a short last group repeats its last
+// row, weighted 0).  The consume side, NS - 1 batches behind, walks the
+// batch's entries in order: it accumulates runs of entries of one row and
+// writes a row out (or, for a chunk of a heavy row, its fp32 partial) where
+// the row ends.  Each lane owns VW bytes of each of the VPT boxes of a row.
+template <typename T, int VW, int VPT, int BE, int NS, int WPC>
 __global__ void __launch_bounds__(WPC * 32)
     aggregate_kernel(const AggParams p, const __grid_constant__ CUtensorMap xmap, const int32_t *__restrict__ chunk_row,
                      const int32_t *__restrict__ chunk_begin, const int32_t *__restrict__ chunk_end, int64_t n_chunks,
+                     const int32_t *__restrict__ group_r0, const int32_t *__restrict__ group_r1, int64_t n_groups,
                      float *__restrict__ partial, int64_t pld) {
-    constexpr int EPV = 16 / (int)sizeof(T);
-    constexpr int GROUPS = 32 / LPG;
-    constexpr int R = LPG * VPT * 16;
-    constexpr int BOX = LPG * 16;  // bytes of one gathered box of a row
+    constexpr int EPL = VW / (int)sizeof(T);  // values of a row per lane per box
+    constexpr int BOX = 32 * VW;              // bytes of one gathered box of a row
+    constexpr int R = VPT * BOX;
+    static_assert(VW == 4 || VW == 8 || VW == 16, "lane piece of 4, 8 or 16 bytes");
     static_assert(BE <= 32 && BE % 4 == 0 && 32 % BE == 0, "whole groups of four entries inside one id window");
     static_assert(BOX % 128 == 0, "TMA destinations stay 128-byte aligned");
     using Ring = BulkRing<R, BE, NS>;
@@ -303,14 +377,13 @@ __global__ void __launch_bounds__(WPC * 32)
     // (the launch adds 128 bytes for this)
     uint8_t *smem_bulk = smem_raw + ((128u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 127u)) & 127u);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int g = lane / LPG, gl = lane % LPG;
     uint8_t *rows = smem_bulk + wib * Ring::kRowBytes;
     float *wring = reinterpret_cast<float *>(smem_bulk + WPC * Ring::kRowBytes) + wib * NS * BE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_bulk + WPC * Ring::kRowBytes + WPC * NS * BE * 4) + wib * NS;
 
     const int64_t W = (int64_t)gridDim.x * WPC;
     const int64_t w0 = (int64_t)blockIdx.x * WPC + wib;
-    const int64_t n_items = n_chunks + p.n_rows;
+    const int64_t n_items = n_chunks + n_groups;
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const T *__restrict__ X = static_cast<const T *>(p.X);
@@ -332,19 +405,20 @@ __global__ void __launch_bounds__(WPC * 32)
     // sit in registers (lane j holds entry wb + j in (ic0, iw0) and wb + 32 + j
     // in (ic1, iw1)); the next item with its first 32 ids is fetched one item
     // ahead.  Issuing a batch therefore never waits on an index load.
-    Item ci = Item{0, 0, 0, false, true}, ni = Item{0, 0, 0, false, true};
+    Item ci = Item{0, 0, 0, 0, false, true}, ni = Item{0, 0, 0, 0, false, true};
     int64_t it_i = w0 - W;
-    bool more = next_work_item(it_i, ci, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+    bool more = next_work_item(it_i, ci, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1,
+                               rowptr, n_rows);
     int64_t it_n = it_i;
-    bool nmore = more && next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr,
-                                        n_rows);
+    bool nmore = more && next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0,
+                                        group_r1, rowptr, n_rows);
     int32_t off_i = 0, wb = 0;
     uint32_t ic0, ic1, nc0;
     float iw0, iw1, nw0;
     fetch_window(ci, more, 0, colidx, wts, lane, pol_stream, ic0, iw0);
     fetch_window(ci, more, 32, colidx, wts, lane, pol_stream, ic1, iw1);
     fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);
-    int64_t s_i = 0;
+    uint32_t s_i = 0;
     bool ok = true;
 
 #define GNN_ISSUE_BATCH()                                                                                   \
@@ -388,7 +462,7 @@ __global__ void __launch_bounds__(WPC * 32)
                 iw0 = nw0;                                                                                  \
                 fetch_window(ci, true, 32, colidx, wts, lane, pol_stream, ic1, iw1);                        \
                 nmore = next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end,   \
-                                       rowptr, n_rows);                                                     \
+                                       group_r0, group_r1, rowptr, n_rows);                                 \
                 fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);                        \
             }                                                                                               \
         } else if (off_i >= wb + 32) {                                                                      \
@@ -403,100 +477,134 @@ __global__ void __launch_bounds__(WPC * 32)
     for (int s = 0; s < NS; ++s) GNN_ISSUE_BATCH();
 
     // ---- consume side ----
-    float acc[VPT][EPV];
+    const int64_t f_store = (f * (int64_t)sizeof(T) + 15) / 16 * 16 / (int64_t)sizeof(T);  // f, padded to 16 bytes
+    float acc[VPT][EPL];
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
-    int64_t s_c = 0;
+        for (int k = 0; k < EPL; ++k) acc[v][k] = 0.f;
+    uint32_t s_c = 0;
 #pragma unroll 1
     for (int64_t it_c = w0; it_c < n_items && ok; it_c += W) {
-        const Item x = load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, rowptr, n_rows);
+        const Item x =
+            load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1, rowptr, n_rows);
         if (x.skip) continue;
+        // rows [wbase, wbase + 32) of a group: lane i holds row wbase + i's end
+        // entry and its scale
+        int32_t r = x.r0, wbase = x.r0, rwin = x.e;
+        float swin = 1.f;
+        auto load_rows = [&](int32_t base) {
+            wbase = base;
+            rwin = x.e;
+            swin = 1.f;
+            if (!x.chunk && base + lane < x.r1) {
+                rwin = rowptr[base + lane + 1];
+                if (p.rowscale) swin = __ldg(p.rowscale + base + lane);
+            }
+        };
+        load_rows(x.r0);
+        int32_t rend = x.chunk ? x.e : __shfl_sync(0xffffffffu, rwin, 0);
+        // write row r (or the chunk's partial) and clear the accumulator
+        auto finish_row = [&]() {
+            if (r - wbase >= 32) load_rows(r);
+            if (x.chunk) {
+                float *dst = partial + it_c * pld;
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
+                    if (c0 < pld) {
+#pragma unroll
+                        for (int k = 0; k < EPL; ++k) dst[c0 + k] = acc[v][k];
+                    }
+                }
+            } else {
+                const float scale = __shfl_sync(0xffffffffu, swin, r - wbase);
+                T *out = static_cast<T *>(p.out) + (int64_t)r * p.ldo;
+                const T *selfrow = nullptr;
+                if (p.self_mode == SELF_COPY) selfrow = X + (int64_t)r * ldx;
+                if (p.self_mode == SELF_ADD && r < p.n_self)
+                    selfrow = static_cast<const T *>(p.self) + (int64_t)r * p.ld_self;
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
+                    if (c0 >= f_store) continue;
+                    const int f_left = (int)(f - c0 < EPL ? f - c0 : EPL);
+                    float o[EPL];
+#pragma unroll
+                    for (int k = 0; k < EPL; ++k) o[k] = acc[v][k] * scale;
+                    if (selfrow) {
+                        uint32_t q[VW / 4];
+                        float sv[EPL];
+                        ldg_words<VW>(selfrow + c0, q);
+                        words_to_vals<T, VW>(q, sv);
+                        if (p.self_mode == SELF_ADD) {
+#pragma unroll
+                            for (int k = 0; k < EPL; ++k) o[k] += sv[k];
+                        } else {
+                            vals_to_words<T, VW>(sv, f_left, q);
+                            stg_words<VW>(out + c0, q, pol_stream);
+                        }
+                    }
+                    uint32_t q[VW / 4];
+                    vals_to_words<T, VW>(o, f_left, q);
+                    stg_words<VW>(out + p.out_off + c0, q, pol_stream);
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) acc[v][k] = 0.f;
+        };
+        int32_t pos = x.b;
 #pragma unroll 1
         for (int32_t off = 0; off < x.e - x.b; off += BE) {
             const int slot = (int)(s_c % NS);
-            if (!bar_wait(&bars[slot], (uint32_t)((s_c / NS) & 1))) {
+            if (!bar_wait(&bars[slot], (s_c / NS) & 1u)) {
                 ok = false;
                 break;
             }
             const int32_t left = x.e - x.b - off;
             const int cnt = left < BE ? left : BE;
-            const uint8_t *sr = rows + slot * BE * R;
-            if (cnt == BE) {  // full batch: no per-row predicate
-#pragma unroll
-                for (int j = 0; j < BE; j += GROUPS)
-                    accumulate_row<T, LPG, VPT, BE>(acc, sr + (j + g) * BOX, wring[slot * BE + j + g], gl);
-            } else {
+            const uint8_t *sr = rows + slot * BE * R + lane * VW;  // this lane's piece of the slot's first row
+            const float *ws = wring + slot * BE;
+            int j = 0;
 #pragma unroll 1
-                for (int j = 0; j < cnt; j += GROUPS)
-                    if (j + g < cnt) accumulate_row<T, LPG, VPT, BE>(acc, sr + (j + g) * BOX, wring[slot * BE + j + g], gl);
+            while (j < cnt) {
+                // rows that end here (empty rows too) are written out first
+#pragma unroll 1
+                while (pos == rend) {
+                    finish_row();
+                    ++r;
+                    if (r - wbase >= 32) load_rows(r);
+                    rend = __shfl_sync(0xffffffffu, rwin, r - wbase);
+                }
+                const int run = rend - pos < cnt - j ? rend - pos : cnt - j;
+#pragma unroll 4
+                for (int k = 0; k < run; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + (j + k) * BOX, ws[j + k]);
+                j += run;
+                pos += run;
             }
             ++s_c;
             __syncwarp();
+            // the slot's rows were read through the generic proxy; the next
+            // TMA gather into it is an async-proxy write
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             GNN_ISSUE_BATCH();
         }
         if (!ok) break;
-        // finish the item: reduce the lane groups, write the row or the partial
-#pragma unroll
-        for (int o = LPG; o < 32; o <<= 1)
-#pragma unroll
-            for (int v = 0; v < VPT; ++v)
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) acc[v][k] += __shfl_xor_sync(0xffffffffu, acc[v][k], o);
-        if (g == 0) {
-            if (x.chunk) {
-                float *dst = partial + it_c * pld;
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-                    if (col < f) {
-#pragma unroll
-                        for (int k = 0; k < EPV; k += 4)
-                            *reinterpret_cast<float4 *>(dst + col + k) =
-                                make_float4(acc[v][k], acc[v][k + 1], acc[v][k + 2], acc[v][k + 3]);
-                    }
-                }
-            } else {
-                const float scale = p.rowscale ? __ldg(p.rowscale + x.r) : 1.f;
-                T *out = static_cast<T *>(p.out) + x.r * p.ldo;
-                const T *selfrow = nullptr;
-                if (p.self_mode == SELF_COPY) selfrow = X + x.r * ldx;
-                if (p.self_mode == SELF_ADD && x.r < p.n_self)
-                    selfrow = static_cast<const T *>(p.self) + x.r * p.ld_self;
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int64_t col = (int64_t)(v * LPG + gl) * EPV;
-                    if (col >= f) continue;
-                    float o[EPV];
-#pragma unroll
-                    for (int k = 0; k < EPV; ++k) o[k] = acc[v][k] * scale;
-                    if (selfrow) {
-                        float sv[EPV];
-                        unpack16(X, __ldg(reinterpret_cast<const uint4 *>(selfrow + col)), sv);
-                        if (p.self_mode == SELF_ADD) {
-#pragma unroll
-                            for (int k = 0; k < EPV; ++k) o[k] += sv[k];
-                        } else {
-                            store16(out + col, sv, (int)(f - col), pol_stream);
-                        }
-                    }
-                    store16(out + p.out_off + col, o, (int)(f - col), pol_stream);
-                }
-            }
+        // the last row, then any empty rows after it
+#pragma unroll 1
+        while (r < x.r1) {
+            finish_row();
+            ++r;
         }
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-#pragma unroll
-            for (int k = 0; k < EPV; ++k) acc[v][k] = 0.f;
     }
 #undef GNN_ISSUE_BATCH
     if (!ok) {
         // a copy never completed: report, then let every copy still in flight
         // land (bounded) before the warp's shared memory is released
         if (lane == 0 && p.err) atomicOr(p.err, 4);
-        for (int64_t s = s_c; s < s_i; ++s) bar_wait(&bars[s % NS], (uint32_t)((s / NS) & 1));
+        for (uint32_t s = s_c; s < s_i; ++s) bar_wait(&bars[s % NS], (s / NS) & 1u);
     }
 }
 
@@ -554,19 +662,19 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
     }
 }
 
-template <typename T, int LPG, int VPT, int BE, int NS, int WPC>
+template <typename T, int VW, int VPT, int BE, int NS, int WPC>
 gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
-    const int64_t items = sc.n_chunks + p.n_rows;
+    const int64_t items = sc.n_chunks + sc.n_groups;
     if (items > 0) {
-        constexpr int R = LPG * VPT * 16;
+        constexpr int R = 32 * VW * VPT;
         const int smem = WPC * BulkRing<R, BE, NS>::kBytes + 128;
-        // the gathered matrix, one row high boxes of LPG * 16 bytes (zero past column f)
+        // the gathered matrix, one row high boxes of 32 * VW bytes (zero past column f)
         CUtensorMap xmap;
         memset(&xmap, 0, sizeof(xmap));
         if (p.n_x > 0 && !make_map_rows(&xmap, sizeof(T) == 2, p.X, (uint64_t)p.f, (uint64_t)p.n_x,
-                                        (uint64_t)p.ldx * sizeof(T), (uint32_t)(LPG * 16 / (int)sizeof(T))))
+                                        (uint64_t)p.ldx * sizeof(T), (uint32_t)(32 * VW / (int)sizeof(T))))
             return GNN_ECUDA;
-        auto kern = aggregate_kernel<T, LPG, VPT, BE, NS, WPC>;
+        auto kern = aggregate_kernel<T, VW, VPT, BE, NS, WPC>;
         GNN_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         // persistent warps: as many blocks as fit on the GPU at once
         int per_sm = 0;
@@ -575,7 +683,8 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
         int64_t blocks = (int64_t)num_sms() * per_sm;
         if (blocks > ceil_div(items, WPC)) blocks = ceil_div(items, WPC);
         { kern<<<(unsigned)blocks, WPC * 32, smem, s>>>(p, xmap, sc.chunk_row, sc.chunk_begin, sc.chunk_end,
-                                                        sc.n_chunks, partial, pld); GNN_LAUNCHED(1); }
+                                                        sc.n_chunks, sc.group_r0, sc.group_r1, sc.n_groups, partial,
+                                                        pld); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
     if (sc.n_heavy > 0) {
@@ -593,15 +702,15 @@ gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, 
     // shared memory (8 warps per block) then sets the blocks per SM (MINB)
     const int64_t bytes = p.f * (int64_t)sizeof(T);
     // a warp keeps NS batches of BE rows in flight (8-16 KB of shared memory)
-    if (bytes <= 128) return launch_cfg<T, 8, 1, 32, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 256) return launch_cfg<T, 16, 1, 16, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 512) return launch_cfg<T, 32, 1, 8, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1024) return launch_cfg<T, 32, 2, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 32, 3, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 32, 4, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 32, 5, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 32, 6, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 32, 8, 4, 2, 2>(p, sc, partial, pld, s);
+    if (bytes <= 128) return launch_cfg<T, 4, 1, 32, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 256) return launch_cfg<T, 8, 1, 16, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 512) return launch_cfg<T, 16, 1, 8, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1024) return launch_cfg<T, 16, 2, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1536) return launch_cfg<T, 16, 3, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 16, 4, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 16, 5, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 16, 6, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 16, 8, 4, 2, 2>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 

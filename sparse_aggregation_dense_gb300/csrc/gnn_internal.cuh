@@ -19,6 +19,8 @@ constexpr int kWarp = 32;
 // fp32 partial; a fix-up pass adds the partials of a row in chunk order.
 constexpr int kHeavyNnz = 512;
 constexpr int kChunkNnz = 512;
+constexpr int kGroupNnz = 512;   // entry window of a row group
+constexpr int kGroupRows = 256;  // rows of a row group at most
 
 // Column ids of the graph's CSR copies carry a 5-bit "hotness tier" in bits
 // 27..31 (when the column count is below 2^27): tier t holds the columns of
@@ -41,6 +43,12 @@ struct Schedule {
     int32_t *chunk_row = nullptr;    // [n_chunks]
     int32_t *chunk_begin = nullptr;  // [n_chunks] entry range of the chunk
     int32_t *chunk_end = nullptr;    // [n_chunks]
+    // row groups: runs of consecutive light rows whose first entries fall in
+    // one kGroupNnz-entry window (at most kGroupRows rows); the aggregation
+    // streams a group's entries as one range
+    int64_t n_groups = 0;
+    int32_t *group_r0 = nullptr;     // [n_groups] first row of the group
+    int32_t *group_r1 = nullptr;     // [n_groups] one past its last row
 };
 
 }  // namespace gnn

@@ -1,7 +1,8 @@
 // loss.cu - training-harness helper (not a layer step): mean softmax
 // cross-entropy over the local rows and its gradient with respect to the
 // logits, G = (softmax - onehot) / n.  One warp per row; the mean is summed in
-// a fixed order by one block, so the loss is reproducible bit for bit.
+// a fixed order (fixed chunks, then the chunk sums in order), so the loss is
+// reproducible bit for bit.
 #include "gnn_internal.cuh"
 
 namespace gnn {
@@ -40,84 +41,180 @@ __global__ void softmax_ce_rows(const T *__restrict__ X, int64_t ld, int64_t n, 
     if (lane == 0) row_loss[i] = ok ? lse - ld_elem(x + y) : NAN;
 }
 
-// rows of up to 32 * CPL classes: each lane keeps its logits in registers, so a
-// row is read once
-template <typename T, int CPL>
-__global__ void softmax_ce_rows_reg(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
-                                    const int32_t *__restrict__ labels, T *__restrict__ G, int64_t ld_g,
-                                    float *__restrict__ row_loss) {
+__device__ __forceinline__ void unpack_vec(const uint4 &q, float (&o)[4]) {
+    o[0] = __uint_as_float(q.x);
+    o[1] = __uint_as_float(q.y);
+    o[2] = __uint_as_float(q.z);
+    o[3] = __uint_as_float(q.w);
+}
+__device__ __forceinline__ void unpack_vec(const uint4 &q, float (&o)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        o[2 * k] = __uint_as_float(w[k] << 16);
+        o[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack_vec(const float (&v)[4]) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+}
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a -> low half (first element)
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack_vec(const float (&v)[8]) {
+    return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
+}
+
+// Rows of up to 32 * VPL 16-byte vectors of classes, rows 16-byte aligned:
+// lane q loads vectors q, q + 32, ... of its row once, keeps them in
+// registers, and writes the gradient back with 16-byte stores (element stores
+// only for the vector that straddles C, so G's padding is left alone).
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
+                                                           const int32_t *__restrict__ labels, T *__restrict__ G,
+                                                           int64_t ld_g, float *__restrict__ row_loss) {
+    constexpr int EPV = 16 / (int)sizeof(T);
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= n) return;
     const T *x = X + i * ld;
-    float v[CPL];
+    float v[VPL][EPV];
     float mx = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        const int64_t c = lane + 32 * q;
-        v[q] = c < C ? ld_elem(x + c) : -INFINITY;
-        mx = fmaxf(mx, v[q]);
+    for (int q = 0; q < VPL; ++q) {
+        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+        if (c0 < C) {
+            unpack_vec(__ldcs(reinterpret_cast<const uint4 *>(x + c0)), v[q]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) v[q][k] = -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            if (c0 + k >= C) v[q][k] = -INFINITY;
+            mx = fmaxf(mx, v[q][k]);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float se = 0.f;
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        v[q] = lane + 32 * q < C ? expf(v[q] - mx) : 0.f;
-        se += v[q];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+    float se = 0.f, xy = 0.f;
     const int32_t y = labels[i];
-    const float inv_n = 1.0f / (float)n, inv_se = 1.0f / se;
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        const int64_t c = lane + 32 * q;
-        if (c < C) st_elem(G + i * ld_g + c, (v[q] * inv_se - (c == y ? 1.f : 0.f)) * inv_n);
+    for (int q = 0; q < VPL; ++q) {
+        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            if (c0 + k == y) xy = v[q][k];
+            v[q][k] = c0 + k < C ? expf(v[q][k] - mx) : 0.f;
+            se += v[q][k];
+        }
     }
-    if (lane == 0) row_loss[i] = (y >= 0 && y < C) ? mx + logf(se) - ld_elem(x + y) : NAN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        se += __shfl_xor_sync(0xffffffffu, se, o);
+        xy += __shfl_xor_sync(0xffffffffu, xy, o);
+    }
+    const float inv_n = 1.0f / (float)n, inv_se = 1.0f / se;
+    T *gr = G + i * ld_g;
+#pragma unroll
+    for (int q = 0; q < VPL; ++q) {
+        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+        if (c0 >= C) continue;
+        float o[EPV];
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) o[k] = (v[q][k] * inv_se - (c0 + k == y ? 1.f : 0.f)) * inv_n;
+        if (c0 + EPV <= C) {
+            __stcs(reinterpret_cast<uint4 *>(gr + c0), pack_vec(o));
+        } else {
+            for (int k = 0; k < EPV && c0 + k < C; ++k) st_elem(gr + c0 + k, o[k]);
+        }
+    }
+    if (lane == 0) row_loss[i] = (y >= 0 && y < C) ? mx + logf(se) - xy : NAN;
 }
 
-__global__ void mean_fixed_order(const float *__restrict__ v, int64_t n, float *out) {
-    __shared__ float part[1024];
-    float s = 0.f;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += v[i];
+// Deterministic mean of row_loss in two passes: block b sums the fixed chunk
+// [b * kLossChunk, (b + 1) * kLossChunk) in a fixed order and stores the sum
+// over the chunk's first element; one block then sums the chunk sums in order.
+constexpr int kLossThreads = 1024;
+constexpr int64_t kLossChunk = 8 * kLossThreads;
+
+__device__ __forceinline__ float block_sum_fixed(float s, float *part) {
     part[threadIdx.x] = s;
     __syncthreads();
-    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    for (int w = kLossThreads / 2; w > 0; w >>= 1) {
         if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) *out = n > 0 ? part[0] / (float)n : 0.f;
+    return part[0];
+}
+
+__global__ void __launch_bounds__(kLossThreads) loss_chunk_sums(float *__restrict__ v, int64_t n) {
+    __shared__ float part[kLossThreads];
+    const int64_t b0 = (int64_t)blockIdx.x * kLossChunk;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < (int)(kLossChunk / kLossThreads); ++k) {
+        const int64_t i = b0 + (int64_t)k * kLossThreads + threadIdx.x;
+        if (i < n) s += v[i];
+    }
+    const float tot = block_sum_fixed(s, part);
+    if (threadIdx.x == 0) v[b0] = tot;  // every read of the chunk is done (barriers above)
+}
+
+__global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float *__restrict__ v, int64_t n,
+                                                                     int64_t n_chunks, float *out) {
+    __shared__ float part[kLossThreads];
+    float s = 0.f;
+    for (int64_t c = threadIdx.x; c < n_chunks; c += kLossThreads) s += v[c * kLossChunk];
+    const float tot = block_sum_fixed(s, part);
+    if (threadIdx.x == 0) *out = n > 0 ? tot / (float)n : 0.f;
 }
 
 }  // namespace
 
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
                              int64_t ld_g, float *row_loss, float *loss, gnn_dtype dt, cudaStream_t s) {
-    if (n > 0 && C <= 256) {
+    const int es = dt == GNN_BF16 ? 2 : 4;
+    const int epv = 16 / es;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(G)) & 15u) == 0 &&
+                         ld % epv == 0 && ld_g % epv == 0;
+    if (n > 0) {
         const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
-        if (dt == GNN_BF16)
-            { softmax_ce_rows_reg<__nv_bfloat16, 8><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(logits), ld,
-                                                                          n, C, labels,
-                                                                          static_cast<__nv_bfloat16 *>(G), ld_g,
-                                                                          row_loss); GNN_LAUNCHED(1); }
-        else
-            { softmax_ce_rows_reg<float, 8><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C, labels,
-                                                                  static_cast<float *>(G), ld_g, row_loss); GNN_LAUNCHED(1); }
-        GNN_CUDA_TRY(cudaGetLastError());
-    } else if (n > 0) {
-        const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
-        if (dt == GNN_BF16)
+        if (aligned && C <= 32 * epv) {
+            if (dt == GNN_BF16)
+                { softmax_ce_rows_vec<__nv_bfloat16, 1><<<blocks, 256, 0, s>>>(
+                    static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
+                    ld_g, row_loss); GNN_LAUNCHED(1); }
+            else
+                { softmax_ce_rows_vec<float, 1><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
+                                                                      labels, static_cast<float *>(G), ld_g,
+                                                                      row_loss); GNN_LAUNCHED(1); }
+        } else if (aligned && C <= 64 * epv) {
+            if (dt == GNN_BF16)
+                { softmax_ce_rows_vec<__nv_bfloat16, 2><<<blocks, 256, 0, s>>>(
+                    static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
+                    ld_g, row_loss); GNN_LAUNCHED(1); }
+            else
+                { softmax_ce_rows_vec<float, 2><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
+                                                                      labels, static_cast<float *>(G), ld_g,
+                                                                      row_loss); GNN_LAUNCHED(1); }
+        } else if (dt == GNN_BF16) {
             { softmax_ce_rows<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(logits), ld, n,
                                                                    C, labels, static_cast<__nv_bfloat16 *>(G), ld_g,
                                                                    row_loss); GNN_LAUNCHED(1); }
-        else
+        } else {
             { softmax_ce_rows<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C, labels,
                                                           static_cast<float *>(G), ld_g, row_loss); GNN_LAUNCHED(1); }
+        }
         GNN_CUDA_TRY(cudaGetLastError());
     }
-    { mean_fixed_order<<<1, 1024, 0, s>>>(row_loss, n, loss); GNN_LAUNCHED(1); }
+    const int64_t n_chunks = ceil_div(n, kLossChunk);
+    if (n_chunks > 0) {
+        { loss_chunk_sums<<<(unsigned)n_chunks, kLossThreads, 0, s>>>(row_loss, n); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+    }
+    { loss_mean_of_chunks<<<1, kLossThreads, 0, s>>>(row_loss, n, n_chunks, loss); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

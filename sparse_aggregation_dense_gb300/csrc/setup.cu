@@ -421,7 +421,36 @@ __global__ void sched_fill_kernel(const int32_t *__restrict__ rowptr, int64_t n_
     }
 }
 
+// row r (light) starts a group when it is the first row, follows a heavy row,
+// starts in another kGroupNnz-entry window than row r - 1, or is a multiple of
+// kGroupRows
+__device__ __forceinline__ bool is_heavy_row(const int32_t *__restrict__ rowptr, int64_t r) {
+    return rowptr[r + 1] - rowptr[r] > kHeavyNnz;
+}
+__global__ void group_flag_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, int32_t *flag) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= n_rows) return;
+    int32_t f = 0;
+    if (!is_heavy_row(rowptr, r))
+        f = r == 0 || is_heavy_row(rowptr, r - 1) || rowptr[r] / kGroupNnz != rowptr[r - 1] / kGroupNnz ||
+            r % kGroupRows == 0;
+    flag[r] = f;
+}
+// flag: exclusive scan of the start flags (start flags recomputed here)
+__global__ void group_fill_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, const int32_t *__restrict__ gidx,
+                                  int32_t *group_r0, int32_t *group_r1) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= n_rows || is_heavy_row(rowptr, r)) return;
+    const bool start = gidx[r + 1] != gidx[r];
+    const int32_t g = start ? gidx[r] : gidx[r] - 1;  // the group row r belongs to
+    if (start) group_r0[g] = (int32_t)r;
+    const bool last = r + 1 == n_rows || is_heavy_row(rowptr, r + 1) || gidx[r + 2] != gidx[r + 1];
+    if (last) group_r1[g] = (int32_t)(r + 1);
+}
+
 void free_schedule(Schedule *sc) {
+    cudaFree(sc->group_r0);
+    cudaFree(sc->group_r1);
     cudaFree(sc->heavy_rows);
     cudaFree(sc->heavy_choff);
     cudaFree(sc->chunk_row);
@@ -462,6 +491,21 @@ gnn_status build_schedule(const int32_t *rowptr, int64_t n_rows, Schedule *sc, c
         int32_t nc = (int32_t)sc->n_chunks;
         GNN_CUDA_TRY(cudaMemcpyAsync(sc->heavy_choff + sc->n_heavy, &nc, sizeof(int32_t), cudaMemcpyHostToDevice, s));
         GNN_CUDA_TRY(cudaStreamSynchronize(s));
+    }
+    // row groups of the light rows (flag reused: start flags, then their exclusive scan)
+    { group_flag_kernel<<<b, 256, 0, s>>>(rowptr, n_rows, flag); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    st = exclusive_scan_i32(flag, flag, n_rows, true, s);
+    if (st != GNN_OK) return st;
+    int32_t ng = 0;
+    GNN_CUDA_TRY(cudaMemcpyAsync(&ng, flag + n_rows, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    GNN_CUDA_TRY(cudaStreamSynchronize(s));
+    sc->n_groups = ng;
+    if (ng > 0) {
+        GNN_CUDA_TRY(cudaMalloc((void **)&sc->group_r0, (size_t)ng * sizeof(int32_t)));
+        GNN_CUDA_TRY(cudaMalloc((void **)&sc->group_r1, (size_t)ng * sizeof(int32_t)));
+        { group_fill_kernel<<<b, 256, 0, s>>>(rowptr, n_rows, flag, sc->group_r0, sc->group_r1); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
     }
     GNN_CUDA_TRY(cudaFreeAsync(nch, s));
     GNN_CUDA_TRY(cudaFreeAsync(flag, s));

@@ -28,6 +28,8 @@ constexpr int kDRows = 128;  // dgrad rows per tile
 constexpr int kWRows = 64;   // wgrad rows per tile
 constexpr int kBoxD = kDRows * 128;  // one 64-column bf16 box of a dgrad tile
 constexpr int kBoxW = kWRows * 128;  // one 64-column bf16 box of a wgrad tile
+constexpr int kStageOut = 32 * 128;           // one 32-row x 64-column bf16 dZ tile (TMA store source)
+constexpr int kOutBytes = 4 * 2 * kStageOut;  // 4 epilogue warps x 2 buffers
 
 struct BarsB {
     uint64_t full[kMaxStagesB];
@@ -89,15 +91,16 @@ __device__ __forceinline__ void init_common(BarsB *bars, int stages, uint32_t te
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreadsB, 1)
     update_dgrad_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapH,
-                           const __grid_constant__ CUtensorMap mapW, __nv_bfloat16 *__restrict__ dZ, int64_t ld_dz,
-                           int64_t M, int Kp, int Kp_pad, int NC, int stages, int relu, int64_t n_tiles, int *err) {
+                           const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapO,
+                           int Kp_pad, int NC, int stages, int relu, int64_t n_tiles, int *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int w_chunk = Kp_pad * 128;
     uint8_t *sW = smem;
     uint8_t *sG = sW + NC * w_chunk;
     uint8_t *sH = sG + stages * kBoxD;
-    BarsB *bars = reinterpret_cast<BarsB *>(sH + (relu ? stages * kBoxD : 0));
+    uint8_t *sO = sH + (relu ? stages * kBoxD : 0);  // 1024-aligned: every region above is a multiple of 1 KB
+    BarsB *bars = reinterpret_cast<BarsB *>(sO + kOutBytes);
     volatile int *abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ncols = Kp_pad <= 128 ? 256u : 512u;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc::prefetch_tmap(&mapG);
         if (relu) tc::prefetch_tmap(&mapH);
         tc::prefetch_tmap(&mapW);
+        tc::prefetch_tmap(&mapO);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -219,34 +223,51 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             }
         }
     } else {
-        const int q = warp & 3;
-        int acc = 0;
+        // epilogue: TMEM -> bf16 -> swizzled 32 x 64 staging tile -> TMA store
+        // (rows and columns past dZ's edge are not written)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint8_t *stage_out = sO + (warp - 2) * 2 * kStageOut;
+        int acc = 0, ob = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
             if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, abort_flag)) break;
             tc::tc_fence_after();
-            const int64_t row = t * kDRows + q * 32 + lane;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride;
-            __nv_bfloat16 *orow = dZ + row * ld_dz;
-            for (int c = 0; c < Kp_pad; c += 16) {
-                uint32_t r[16];
-                tc::tmem_ld16(taddr + (uint32_t)c, r);
-                if (row < M && c < Kp) {
-                    if (c + 16 <= Kp) {
-                        uint4 lo = make_uint4(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                                              pack2(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                                              pack2(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                                              pack2(__uint_as_float(r[6]), __uint_as_float(r[7])));
-                        uint4 hi = make_uint4(pack2(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                                              pack2(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                                              pack2(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                                              pack2(__uint_as_float(r[14]), __uint_as_float(r[15])));
-                        reinterpret_cast<uint4 *>(orow + c)[0] = lo;
-                        reinterpret_cast<uint4 *>(orow + c)[1] = hi;
+            for (int cc = 0; cc < Kp_pad; cc += 64) {
+                // the TMA store that last read this buffer must be done with it
+                if (lane == 0) tc::bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t *buf = stage_out + ob * kStageOut;
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    const int c = cc + sub * 16;
+                    uint32_t r[16];
+                    if (c < Kp_pad) {
+                        tc::tmem_ld16(taddr + (uint32_t)c, r);
                     } else {
-                        for (int i = 0; i < 16 && c + i < Kp; ++i) orow[c + i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = 0u;
                     }
+                    // 16-byte chunks 2*sub and 2*sub+1 of this thread's 128-byte row, 128-byte swizzle
+                    uint4 lo = make_uint4(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                          pack2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                          pack2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                          pack2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+                    uint4 hi = make_uint4(pack2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                          pack2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                          pack2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                          pack2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+                    uint8_t *rowp = buf + lane * 128;
+                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub) ^ (lane & 7)) * 16)) = lo;
+                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub + 1) ^ (lane & 7)) * 16)) = hi;
                 }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(&mapO, cc, (int32_t)(t * kDRows + q * 32), buf);
+                    tc::bulk_commit();
+                }
+                ob ^= 1;
             }
             tc::tc_fence_before();
             __syncwarp();
@@ -256,6 +277,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) tc::bulk_wait<0>();
+        __syncwarp();
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -446,10 +469,10 @@ bool plan_bwd(int64_t Kp, int64_t N, int relu, BwdPlan *p) {
     // dgrad: resident W (NC chunks of Kp_pad x 64) + stages of G (+ H)
     const size_t wbytes = (size_t)p->NC * p->Kp_pad * 128;
     const size_t dstage = (size_t)kBoxD * (relu ? 2 : 1);
-    if (wbytes + 2 * dstage + bars > kSmemLimitB) return false;
-    int ds = (int)((kSmemLimitB - wbytes - bars) / dstage);
+    if (wbytes + 2 * dstage + kOutBytes + bars > kSmemLimitB) return false;
+    int ds = (int)((kSmemLimitB - wbytes - kOutBytes - bars) / dstage);
     p->dstages = ds > kMaxStagesB ? kMaxStagesB : ds;
-    p->dsmem = wbytes + p->dstages * dstage + bars;
+    p->dsmem = wbytes + p->dstages * dstage + kOutBytes + bars;
     // wgrad: stages of Z (2 MB boxes) + G (NC) (+ H (NC))
     const size_t wstage = (size_t)kBoxW * (2 * p->MB + p->NC * (relu ? 2 : 1));
     if (2 * wstage + bars > kSmemLimitB) return false;
@@ -514,13 +537,14 @@ gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, i
     if (!make_map_bf16_2d(&mW, Wk, (uint64_t)p.N_pad, (uint64_t)p.Kp_pad, (uint64_t)p.N_pad * 2, 64,
                           (uint32_t)p.Kp_pad))
         return GNN_ECUDA;
+    CUtensorMap mO;
+    if (!make_map_bf16_2d(&mO, dZ, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_dz * 2, 64, 32)) return GNN_ECUDA;
     GNN_CUDA_TRY(cudaFuncSetAttribute(update_dgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)p.dsmem));
     const int64_t dtiles = ceil_div(n, kDRows);
     const int64_t dgrid = dtiles < num_sms() ? dtiles : num_sms();
     { update_dgrad_tc_kernel<<<(unsigned)dgrid, kThreadsB, p.dsmem, s>>>(
-        mG, mH, mW, static_cast<__nv_bfloat16 *>(dZ), ld_dz, n, (int)Kp, (int)p.Kp_pad, (int)p.NC, p.dstages, relu,
-        dtiles, err); GNN_LAUNCHED(1); }
+        mG, mH, mW, mO, (int)p.Kp_pad, (int)p.NC, p.dstages, relu, dtiles, err); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

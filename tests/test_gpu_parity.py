@@ -490,3 +490,39 @@ def test_bad_csr_is_rejected():
     rowptr2 = torch.tensor([0, 3, 2], dtype=torch.int32, device="cuda")  # not monotone
     with pytest.raises(gnn.GnnError):
         gnn.graph_create(rowptr2, colidx[:2], 2, 2, None, "gcn")
+
+
+# ---------------------------------------------------------------------------
+# softmax cross-entropy (training-harness helper): G elementwise, the mean loss,
+# the padding of G left alone, a bad label giving a NaN loss
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("n,C", [(1, 1), (37, 7), (1000, 41), (33333, 172), (5000, 256), (3000, 300), (700, 520)])
+def test_softmax_ce(dt, n, C):
+    tdt = torch_dtype(dt)
+    X_h = gen_matrix(n, C, dt, SEED, 55)
+    X = to_device(X_h, dt, C)
+    y = synth.labels(n, C, SEED)
+    G = padded(n, C, tdt, "cuda", fill=None)
+    G.as_strided((n, G.stride(0)), (G.stride(0), 1)).fill_(7.0)
+    row_loss = torch.empty(n, dtype=torch.float32, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    gnn.softmax_ce(X, torch.from_numpy(y).cuda(), G, row_loss, loss)
+    ref_loss, ref_G = oracle.softmax_ce(widen(X_h, dt, C), y)
+    close(to_host(G), maybe_round(ref_G, dt), TOL[dt], "G")
+    assert abs(float(loss.item()) - ref_loss) <= 1e-5 * abs(ref_loss)  # fp32 sums of exact-input rows
+    pad = G.as_strided((n, G.stride(0)), (G.stride(0), 1))[:, C:]
+    assert bool(torch.all(pad == 7.0))
+
+
+def test_softmax_ce_bad_label_gives_nan():
+    n, C = 100, 16
+    X = to_device(gen_matrix(n, C, "f32", SEED, 56), "f32", C)
+    y = synth.labels(n, C, SEED)
+    y[17] = C  # out of range
+    G = padded(n, C, torch.float32, "cuda")
+    row_loss = torch.empty(n, dtype=torch.float32, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    gnn.softmax_ce(X, torch.from_numpy(y).cuda(), G, row_loss, loss)
+    assert np.isnan(float(loss.item()))
