@@ -170,25 +170,15 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Shared memory of one warp: NS slots of BE gathered rows (R bytes each), the
-// entries' weights and one mbarrier per slot.  A slot is laid out box-major:
+// entries' weights (each stored twice, as a packed-FMA operand) and one
+// mbarrier per slot.  A slot is laid out box-major:
 // box v (bytes [v * LPG * 16, (v + 1) * LPG * 16) of every row) holds the BE
 // rows one after another, as the TMA gathers deliver them.
 template <int R, int BE, int NS>
 struct BulkRing {
     static constexpr int kRowBytes = NS * BE * R;
-    static constexpr int kBytes = kRowBytes + NS * BE * 4 + NS * 8;
+    static constexpr int kBytes = kRowBytes + NS * BE * 8 + NS * 8;  // rows, weight pairs, mbarriers
 };
-
-// acc += w * row (this lane's VPT 16-byte vectors of a gathered row in shared
-// memory), two fp32 lanes per packed FMA
-__device__ __forceinline__ void fma2(float &a0, float &a1, float x0, float x1, float w) {
-    unsigned long long acc, xv, wv, d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x0), "f"(x1));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(wv) : "f"(w));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(wv), "l"(xv), "l"(acc));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
-}
 
 // One work item: a row group (consecutive light rows, one entry range) or one
 // chunk of a heavy row.  Rows at or past n_rows (halo rows of a transpose whose
@@ -244,27 +234,61 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[VW / 4
     }
 }
 
+// Accumulators and weights live as pairs of fp32 in one 64-bit register (low
+// half = the even column), the operand form of the packed FMA fma.rn.f32x2;
+// a bf16 pair is widened by placing each half in the top 16 bits of an fp32.
+template <typename T, int VW>
+struct Lane {
+    static constexpr int kWords = VW / 4;                                       // 32-bit words per piece
+    static constexpr int kPairs = sizeof(T) == 2 ? kWords : (kWords + 1) / 2;  // fp32 pairs per piece
+};
+
+// a += ww * (the values in words q), one packed FMA per pair
+template <typename T, int VW>
+__device__ __forceinline__ void fma_piece(unsigned long long (&a)[Lane<T, VW>::kPairs], const uint32_t (&q)[VW / 4],
+                                          unsigned long long ww) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int k = 0; k < VW / 4; ++k)
+            asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 x;\n\t"
+                "shl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\tmov.b64 x, {lo, hi};\n\t"
+                "fma.rn.f32x2 %0, x, %2, %0;\n\t}"
+                : "+l"(a[k])
+                : "r"(q[k]), "l"(ww));
+    } else if constexpr (VW >= 8) {
+#pragma unroll
+        for (int k = 0; k < VW / 8; ++k)
+            asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%1, %2};\n\tfma.rn.f32x2 %0, x, %3, %0;\n\t}"
+                : "+l"(a[k])
+                : "r"(q[2 * k]), "r"(q[2 * k + 1]), "l"(ww));
+    } else {
+        asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%1, 0};\n\tfma.rn.f32x2 %0, x, %2, %0;\n\t}"
+            : "+l"(a[0])
+            : "r"(q[0]), "l"(ww));
+    }
+}
+
 // acc += w * (this lane's VW-byte pieces of one gathered row); `row` points at
-// the lane's piece in box 0, box v sits v * BE * 32 * VW bytes further
+// the lane's piece in box 0, box v sits v * BE * 32 * VW bytes further; ww
+// holds the weight twice
 template <typename T, int VW, int VPT, int BE>
-__device__ __forceinline__ void accumulate_entry(float (&acc)[VPT][VW / sizeof(T)], const uint8_t *row, float w) {
+__device__ __forceinline__ void accumulate_entry(unsigned long long (&acc)[VPT][Lane<T, VW>::kPairs],
+                                                 const uint8_t *row, unsigned long long ww) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         uint32_t q[VW / 4];
         lds_words<VW>(row + v * (BE * 32 * VW), q);
-        if constexpr (sizeof(T) == 2) {
-#pragma unroll
-            for (int k = 0; k < VW / 4; ++k)
-                fma2(acc[v][2 * k], acc[v][2 * k + 1], __uint_as_float(q[k] << 16), __uint_as_float(q[k] & 0xffff0000u),
-                     w);
-        } else if constexpr (VW >= 8) {
-#pragma unroll
-            for (int k = 0; k < VW / 4; k += 2)
-                fma2(acc[v][k], acc[v][k + 1], __uint_as_float(q[k]), __uint_as_float(q[k + 1]), w);
-        } else {
-            acc[v][0] = fmaf(w, __uint_as_float(q[0]), acc[v][0]);
-        }
+        fma_piece<T, VW>(acc[v], q, ww);
     }
+}
+
+// the VW / sizeof(T) fp32 values held in a piece's pairs
+template <typename T, int VW>
+__device__ __forceinline__ void pairs_to_vals(const unsigned long long (&a)[Lane<T, VW>::kPairs],
+                                              float (&v)[VW / sizeof(T)]) {
+#pragma unroll
+    for (int k = 0; k < (int)(VW / sizeof(T)); ++k)
+        v[k] = __uint_as_float((uint32_t)(a[k / 2] >> (32 * (k & 1))));
 }
 
 // global <-> registers for this lane's VW bytes (VW / sizeof(T) values)
@@ -378,8 +402,9 @@ __global__ void __launch_bounds__(WPC * 32)
     uint8_t *smem_bulk = smem_raw + ((128u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 127u)) & 127u);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     uint8_t *rows = smem_bulk + wib * Ring::kRowBytes;
-    float *wring = reinterpret_cast<float *>(smem_bulk + WPC * Ring::kRowBytes) + wib * NS * BE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_bulk + WPC * Ring::kRowBytes + WPC * NS * BE * 4) + wib * NS;
+    unsigned long long *wring =
+        reinterpret_cast<unsigned long long *>(smem_bulk + WPC * Ring::kRowBytes) + wib * NS * BE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_bulk + WPC * Ring::kRowBytes + WPC * NS * BE * 8) + wib * NS;
 
     const int64_t W = (int64_t)gridDim.x * WPC;
     const int64_t w0 = (int64_t)blockIdx.x * WPC + wib;
@@ -432,7 +457,10 @@ __global__ void __launch_bounds__(WPC * 32)
         const int src = (off_i - wb + (lane < cnt ? lane : cnt - 1)) & 31;                                  \
         const uint32_t raw = __shfl_sync(0xffffffffu, ic0, src);                                            \
         const float wv = __shfl_sync(0xffffffffu, iw0, src);                                                \
-        if (lane < BE) wring[slot * BE + lane] = lane < cnt ? wv : 0.f;                                     \
+        if (lane < BE) {                                                                                    \
+            const uint32_t wb32 = __float_as_uint(lane < cnt ? wv : 0.f);                                   \
+            wring[slot * BE + lane] = ((unsigned long long)wb32 << 32) | wb32;                              \
+        }                                                                                                   \
         const int32_t col = (int32_t)(raw & colmask);                                                       \
         const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;                                \
         const uint32_t hot = __ballot_sync(0xffffffffu, lane < cnt && tier <= hot_tier);                    \
@@ -478,11 +506,12 @@ __global__ void __launch_bounds__(WPC * 32)
 
     // ---- consume side ----
     const int64_t f_store = (f * (int64_t)sizeof(T) + 15) / 16 * 16 / (int64_t)sizeof(T);  // f, padded to 16 bytes
-    float acc[VPT][EPL];
+    constexpr int NP = Lane<T, VW>::kPairs;
+    unsigned long long acc[VPT][NP];
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) acc[v][k] = 0.f;
+        for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
     uint32_t s_c = 0;
 #pragma unroll 1
     for (int64_t it_c = w0; it_c < n_items && ok; it_c += W) {
@@ -513,8 +542,10 @@ __global__ void __launch_bounds__(WPC * 32)
                 for (int v = 0; v < VPT; ++v) {
                     const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
                     if (c0 < pld) {
+                        float a[EPL];
+                        pairs_to_vals<T, VW>(acc[v], a);
 #pragma unroll
-                        for (int k = 0; k < EPL; ++k) dst[c0 + k] = acc[v][k];
+                        for (int k = 0; k < EPL; ++k) dst[c0 + k] = a[k];
                     }
                 }
             } else {
@@ -530,8 +561,9 @@ __global__ void __launch_bounds__(WPC * 32)
                     if (c0 >= f_store) continue;
                     const int f_left = (int)(f - c0 < EPL ? f - c0 : EPL);
                     float o[EPL];
+                    pairs_to_vals<T, VW>(acc[v], o);
 #pragma unroll
-                    for (int k = 0; k < EPL; ++k) o[k] = acc[v][k] * scale;
+                    for (int k = 0; k < EPL; ++k) o[k] *= scale;
                     if (selfrow) {
                         uint32_t q[VW / 4];
                         float sv[EPL];
@@ -553,7 +585,7 @@ __global__ void __launch_bounds__(WPC * 32)
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                for (int k = 0; k < EPL; ++k) acc[v][k] = 0.f;
+                for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
         };
         int32_t pos = x.b;
 #pragma unroll 1
@@ -566,23 +598,31 @@ __global__ void __launch_bounds__(WPC * 32)
             const int32_t left = x.e - x.b - off;
             const int cnt = left < BE ? left : BE;
             const uint8_t *sr = rows + slot * BE * R + lane * VW;  // this lane's piece of the slot's first row
-            const float *ws = wring + slot * BE;
-            int j = 0;
+            const unsigned long long *ws = wring + slot * BE;
+            if (cnt == BE && rend - pos >= BE) {
+                // the whole batch lies in the current row
+#pragma unroll
+                for (int k = 0; k < BE; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
+                pos += BE;
+            } else {
+                int j = 0;
 #pragma unroll 1
-            while (j < cnt) {
-                // rows that end here (empty rows too) are written out first
+                while (j < cnt) {
+                    // rows that end here (empty rows too) are written out first
 #pragma unroll 1
-                while (pos == rend) {
-                    finish_row();
-                    ++r;
-                    if (r - wbase >= 32) load_rows(r);
-                    rend = __shfl_sync(0xffffffffu, rwin, r - wbase);
+                    while (pos == rend) {
+                        finish_row();
+                        ++r;
+                        if (r - wbase >= 32) load_rows(r);
+                        rend = __shfl_sync(0xffffffffu, rwin, r - wbase);
+                    }
+                    const int run = rend - pos < cnt - j ? rend - pos : cnt - j;
+#pragma unroll 1
+                    for (int k = 0; k < run; ++k)
+                        accumulate_entry<T, VW, VPT, BE>(acc, sr + (j + k) * BOX, ws[j + k]);
+                    j += run;
+                    pos += run;
                 }
-                const int run = rend - pos < cnt - j ? rend - pos : cnt - j;
-#pragma unroll 4
-                for (int k = 0; k < run; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + (j + k) * BOX, ws[j + k]);
-                j += run;
-                pos += run;
             }
             ++s_c;
             __syncwarp();
