@@ -41,7 +41,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=gnu11", _SRC, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=gnu11", _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -78,6 +78,12 @@ def _L():
         L.oracle_sage_aggregate_backward.restype = None
         L.oracle_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64]
         L.oracle_softmax_ce.restype = ctypes.c_double
+        L.oracle_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        L.oracle_splitmix64.restype = ctypes.c_uint64
+        L.oracle_codec_quantize.argtypes = [vp, i64, i64, i64, vp, i32, ctypes.c_uint64, vp, i64, vp]
+        L.oracle_codec_quantize.restype = None
+        L.oracle_codec_dequantize.argtypes = [vp, i64, vp, i64, i64, i32, vp, i64]
+        L.oracle_codec_dequantize.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ctypes.c_int
         _lib = L
@@ -275,6 +281,48 @@ def softmax_ce(logits: np.ndarray, labels: np.ndarray):
     loss = _L().oracle_softmax_ce(_p(x), C, n, C, _p(lab), _p(G), C)
     return float(loss), G
 
+
+
+# --------------------------------------------------------------------------
+# Sylvie low-bit halo codec (Sylvie page, Quantizer / Dequantizer)
+# --------------------------------------------------------------------------
+
+def splitmix64(seed: int, k: int) -> int:
+    """k-th output of the SplitMix64 stream seeded with `seed` (k >= 1)."""
+    return int(_L().oracle_splitmix64(seed & (2**64 - 1), k & (2**64 - 1)))
+
+
+def codec_row_bytes(f: int, bits: int) -> int:
+    """Bytes of one packed row of f b-bit codes, padded to 16."""
+    return (f * bits + 127) // 128 * 16
+
+
+def quantize_rows(x: np.ndarray, ids: np.ndarray, bits: int, seed: int, ld_codes: Optional[int] = None):
+    """(codes uint8 n x ld_codes, scale_zero float32 n x 2) of the rows of x.
+
+    x holds values exactly representable in fp32 (fp32 or bf16 inputs); ids are
+    the rows' table ids (they select the stochastic-rounding draws)."""
+    xf = np.ascontiguousarray(x, dtype=np.float32)
+    n, f = xf.shape
+    ids64 = np.ascontiguousarray(ids, dtype=np.int64)
+    assert ids64.shape[0] == n and bits in (1, 2, 4, 8)
+    ldc = codec_row_bytes(f, bits) if ld_codes is None else ld_codes
+    codes = np.zeros((n, ldc), dtype=np.uint8)
+    sz = np.zeros((n, 2), dtype=np.float32)
+    if n:
+        _L().oracle_codec_quantize(_p(xf), f, n, f, _p(ids64), bits, seed & (2**64 - 1), _p(codes), ldc, _p(sz))
+    return codes, sz
+
+
+def dequantize_rows(codes: np.ndarray, scale_zero: np.ndarray, f: int, bits: int) -> np.ndarray:
+    """float32 n x f: code * scale + zero, row by row."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    sz = np.ascontiguousarray(scale_zero, dtype=np.float32)
+    n = c.shape[0]
+    y = np.zeros((n, f), dtype=np.float32)
+    if n:
+        _L().oracle_codec_dequantize(_p(c), c.shape[1], _p(sz), n, f, bits, _p(y), f)
+    return y
 
 # --------------------------------------------------------------------------
 # one layer and one epoch, composed step by step

@@ -337,6 +337,86 @@ double oracle_softmax_ce(const double *logits, int64_t ld_l, int64_t n, int64_t 
     return n > 0 ? total / (double)n : 0.0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Sylvie low-bit halo codec ("Sylvie: 3D-Adaptive and Universal System for  */
+/* Large-Scale Graph Neural Network Training" page, Quantizer and            */
+/* Dequantizer, Eq. 3-5 as described in the text around them).              */
+/* Per row h (f values): B = 2^b - 1 bins, zero point z = min(h),           */
+/* scale s = (max(h) - min(h)) / B; the code of h[c] is the stochastic       */
+/* rounding of (h[c] - z) / s, i.e. floor((h[c] - z) / s + u) with u         */
+/* uniform in [0, 1), kept in [0, B]; the recovered value is q * s + z.      */
+/* A constant row (s = 0) gets code 0 everywhere and is recovered exactly.  */
+/* The arithmetic is IEEE single precision, one rounding per operation      */
+/* (no fused multiply-add), so the codes are a pure function of the inputs. */
+/* ------------------------------------------------------------------------ */
+
+/* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number  */
+/* generators", OOPSLA 2014): the k-th output of the stream seeded with     */
+/* `seed` mixes seed + k * 0x9E3779B97F4A7C15.                               */
+uint64_t oracle_splitmix64(uint64_t seed, uint64_t k) {
+    uint64_t z = seed + k * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* the uniform u of element c of table row r: output k = r * 2^16 + c + 1,  */
+/* its top 24 bits scaled to [0, 1)                                          */
+static float codec_uniform(uint64_t seed, int64_t r, int64_t c) {
+    const uint64_t k = ((uint64_t)r << 16) + (uint64_t)c + 1u;
+    return (float)(oracle_splitmix64(seed, k) >> 40) * (1.0f / 16777216.0f);
+}
+
+/* Quantise n rows of f fp32 values (row i at x + i * ld_x, table id ids[i]) */
+/* to b-bit codes packed little-endian (code c in bits [c*b, c*b + b) of the */
+/* row's bytes, row i at codes + i * ld_codes) and per-row (scale, zero).    */
+void oracle_codec_quantize(const float *x, int64_t ld_x, int64_t n, int64_t f, const int64_t *ids, int bits,
+                           uint64_t seed, uint8_t *codes, int64_t ld_codes, float *scale_zero) {
+    const int B = (1 << bits) - 1;
+    for (int64_t i = 0; i < n; ++i) {
+        const float *h = x + i * ld_x;
+        uint8_t *row = codes + i * ld_codes;
+        float mn = h[0], mx = h[0];
+        for (int64_t c = 1; c < f; ++c) {
+            if (h[c] < mn) mn = h[c];
+            if (h[c] > mx) mx = h[c];
+        }
+        const float range = mx - mn;
+        const float s = range / (float)B;
+        memset(row, 0, (size_t)ld_codes);
+        for (int64_t c = 0; c < f; ++c) {
+            int q = 0;
+            if (s > 0.0f) {
+                const float t = (h[c] - mn) / s;
+                const float v = t + codec_uniform(seed, ids[i], c);
+                q = (int)floorf(v);
+                if (q < 0) q = 0;
+                if (q > B) q = B;
+            }
+            const int64_t bit = c * bits;
+            row[bit >> 3] |= (uint8_t)(q << (bit & 7));
+        }
+        scale_zero[2 * i] = s;
+        scale_zero[2 * i + 1] = mn;
+    }
+}
+
+/* y[i, c] = q * scale_i + zero_i for c < f */
+void oracle_codec_dequantize(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n, int64_t f,
+                             int bits, float *y, int64_t ld_y) {
+    const int B = (1 << bits) - 1;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint8_t *row = codes + i * ld_codes;
+        const float s = scale_zero[2 * i], z = scale_zero[2 * i + 1];
+        for (int64_t c = 0; c < f; ++c) {
+            const int64_t bit = c * bits;
+            const int q = (row[bit >> 3] >> (bit & 7)) & B;
+            const float qs = (float)q * s;
+            y[i * ld_y + c] = qs + z;
+        }
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);
