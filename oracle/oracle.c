@@ -360,11 +360,14 @@ uint64_t oracle_splitmix64(uint64_t seed, uint64_t k) {
     return z ^ (z >> 31);
 }
 
-/* the uniform u of element c of table row r: output k = r * 2^16 + c + 1,  */
-/* its top 24 bits scaled to [0, 1)                                          */
+/* the uniform u of element c of table row r: output k = r * 2^15 + c / 2 + 1 */
+/* serves elements 2j and 2j + 1, through its bits 40..63 and 16..39; 24    */
+/* bits scaled to [0, 1)                                                     */
 static float codec_uniform(uint64_t seed, int64_t r, int64_t c) {
-    const uint64_t k = ((uint64_t)r << 16) + (uint64_t)c + 1u;
-    return (float)(oracle_splitmix64(seed, k) >> 40) * (1.0f / 16777216.0f);
+    const uint64_t k = ((uint64_t)r << 15) + (uint64_t)(c >> 1) + 1u;
+    const uint64_t z = oracle_splitmix64(seed, k);
+    const uint32_t u24 = (c & 1) ? (uint32_t)((z >> 16) & 0xFFFFFFu) : (uint32_t)(z >> 40);
+    return (float)u24 * (1.0f / 16777216.0f);
 }
 
 /* Quantise n rows of f fp32 values (row i at x + i * ld_x, table id ids[i]) */
