@@ -144,7 +144,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha1()
-    for name in ("aggregate.cu", "gnn_internal.cuh"):
+    for name in ("aggregate.cu",):
         h.update(open(os.path.join(ROOT, "sparse_aggregation_dense_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:12]
 
@@ -459,6 +459,10 @@ def run_ours(args, rank, world, local_rank):
             "unit": "GB/s",
             "frac": achieved / hbm if hbm else None,
             "traffic": traffic,
+            "traffic_scope": "DRAM bytes of one step's aggregation launches (ncu summary in profiles/)",
+            "dram_achieved": (traffic / (agg_ms / args.steps / 1e3) / 1e9) if (traffic and agg_ms > 0) else None,
+            "dram_frac": (traffic / (agg_ms / args.steps / 1e3) / 1e9 / hbm) if (traffic and agg_ms > 0 and hbm)
+            else None,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
             "algorithmic_bytes_per_step": sum(fwd_b) + sum(bwd_b),
             "launch_groups": agg_launches,

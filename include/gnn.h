@@ -115,6 +115,41 @@ gnn_status gnn_halo_pull(gnn_graph *g, const void *table, int64_t ld_table, int6
 gnn_status gnn_halo_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, const int64_t *local_ids,
                          void *table, int64_t ld_table, int64_t n_table, gnn_dtype dtype, void *stream);
 
+/* Low-bit halo codec (Sylvie page, "Quantizer" / "Dequantizer"; its Eq. 3-5
+ * are stripped from the page text, this is the plainest reading of the prose
+ * around them): rows cross the table as b-bit codes plus a per-row scale and
+ * zero point, b = 1, 2, 4 or 8, B = 2^b - 1.
+ *
+ * Push with quantisation: for v < n_local, row h = H[v, 0:f] is stored at
+ * table row r = local_ids[v] as
+ *   scale_zero[2r] = s = (max h - min h) / B,  scale_zero[2r + 1] = min h,
+ *   code c = min(B, max(0, floor((h[c] - min h) / s + u))),  c < f,
+ * with u uniform in [0, 1) (stochastic rounding), or code 0 where s = 0.
+ * u of element c of row r is 24 bits of output k = r * 2^15 + floor(c/2) + 1
+ * of a SplitMix64 stream seeded with `seed` (bits 40..63 for even c, 16..39
+ * for odd c), so the codes are reproducible.  Arithmetic is IEEE fp32, one
+ * rounding per operation.
+ *   codes      device, n_table x ld_codes bytes; ld_codes a multiple of 16 and
+ *              at least b * ceil(f / 8); code c of a row sits in bits
+ *              [c b, c b + b) (little-endian); the row's remaining bytes are
+ *              written as 0
+ *   scale_zero device float[2 n_table]
+ * Ids are checked as in gnn_halo_push (repeated or out-of-range ids set
+ * GNN_EINDEX on the device; their rows are not written).  Uses the push claim
+ * array.  Returns GNN_EINVAL for another b or a bad ld_codes. */
+gnn_status gnn_halo_push_quantized(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, const int64_t *local_ids,
+                                   uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
+                                   uint64_t seed, gnn_dtype dtype, void *stream);
+
+/* Pull with dequantisation: for i < n_halo, with r = halo_ids[i],
+ *   H[n_local + i, c] = code(r, c) * scale_zero[2r] + scale_zero[2r + 1],
+ * fp32 multiply then add, rounded to dtype (bf16: round to nearest even);
+ * columns c >= f are not written.  An id outside [0, n_table) sets GNN_EINDEX
+ * on the device and leaves its row. */
+gnn_status gnn_halo_pull_quantized(gnn_graph *g, const uint8_t *codes, int64_t ld_codes, const float *scale_zero,
+                                   int64_t n_table, int bits, const int64_t *halo_ids, void *H, int64_t ld_h,
+                                   int64_t f, gnn_dtype dtype, void *stream);
+
 /* Column where the mean half of a GraphSAGE aggregation starts:
  * f rounded up to 4 (fp32) or 8 (bf16) elements.  The aggregation width K' of
  * a layer is f_in (GCN) or 2 * gnn_sage_half_offset(f_in) (GraphSAGE). */

@@ -322,6 +322,42 @@ gnn_status gnn_halo_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, c
                        as_stream(stream));
 }
 
+namespace {
+bool codec_args_ok(const void *codes, int64_t ld_codes, const float *scale_zero, int64_t n_table, int bits,
+                   int64_t f) {
+    if (bits != 1 && bits != 2 && bits != 4 && bits != 8) return false;
+    if (n_table < 0 || f <= 0 || ld_codes % 16 != 0 || ld_codes < (f + 7) / 8 * bits) return false;
+    if (n_table > 0 && (!codes || !scale_zero || (reinterpret_cast<uintptr_t>(codes) & 15u) ||
+                        (reinterpret_cast<uintptr_t>(scale_zero) & 7u)))
+        return false;
+    return true;
+}
+}  // namespace
+
+gnn_status gnn_halo_push_quantized(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, const int64_t *local_ids,
+                                   uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
+                                   uint64_t seed, gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || !codec_args_ok(codes, ld_codes, scale_zero, n_table, bits, f)) return GNN_EINVAL;
+    if (g->n_local == 0) return GNN_OK;
+    if (!local_ids || !operand_ok(H, g->n_local, ld_h, f, dtype)) return GNN_EINVAL;
+    gnn_status st = ensure_claim(g, n_table);  // a first push to a larger table allocates (synchronising)
+    if (st != GNN_OK) return st;
+    ProfScope prof(g, GNN_PROF_PUSH, as_stream(stream));
+    return launch_codec_push(g, H, ld_h, g->n_local, f, local_ids, codes, ld_codes, scale_zero, n_table, bits, seed,
+                             dtype, as_stream(stream));
+}
+
+gnn_status gnn_halo_pull_quantized(gnn_graph *g, const uint8_t *codes, int64_t ld_codes, const float *scale_zero,
+                                   int64_t n_table, int bits, const int64_t *halo_ids, void *H, int64_t ld_h,
+                                   int64_t f, gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || !codec_args_ok(codes, ld_codes, scale_zero, n_table, bits, f)) return GNN_EINVAL;
+    if (g->n_halo == 0) return GNN_OK;
+    if (!halo_ids || !operand_ok(H, g->n_local + g->n_halo, ld_h, f, dtype)) return GNN_EINVAL;
+    ProfScope prof(g, GNN_PROF_PULL, as_stream(stream));
+    return launch_codec_pull(codes, ld_codes, scale_zero, n_table, bits, halo_ids, g->n_halo, H, ld_h, g->n_local, f,
+                             dtype, g->err, as_stream(stream));
+}
+
 gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W, int64_t f_out,
                              int relu, void *Z, int64_t ld_z, void *H_out, int64_t ld_out, gnn_dtype dtype,
                              void *stream) {

@@ -1,0 +1,258 @@
+// codec.cu - the low-bit halo codec of the Sylvie page ("Sylvie: 3D-Adaptive
+// and Universal System for Large-Scale Graph Neural Network Training",
+// Quantizer and Dequantizer), fused into push and pull.
+//
+// Push side (quantiser): every pushed row h of f values becomes f b-bit codes
+// (b = 1, 2, 4 or 8, B = 2^b - 1 bins) plus two fp32 numbers, the scale
+// s = (max(h) - min(h)) / B and the zero point min(h).  A code is the
+// stochastic rounding of (h[c] - min) / s: floor of that value plus a uniform
+// draw u in [0, 1), kept in [0, B]; a row with s = 0 gets code 0 throughout.
+// Pull side (dequantiser): the halo row is recovered as code * s + min.
+//
+// The draws come from a counter-based generator, SplitMix64 (Steele, Lea and
+// Flood, OOPSLA 2014): element c of table row r uses output k = r * 2^15 +
+// c / 2 + 1 of the stream seeded with the caller's seed, bits 40..63 for even
+// c and 16..39 for odd c, as a 24-bit fraction.  All arithmetic is IEEE
+// single precision with one rounding per operation (explicit _rn intrinsics,
+// nothing fused), so the codes depend on the inputs and the seed only.
+//
+// Layout: codes of table row r at codes + r * ld_codes (bytes, a multiple of
+// 16), code c in bits [c * b, c * b + b) little-endian, bytes past the last
+// code zero; (scale, zero point) at scale_zero[2 r], scale_zero[2 r + 1].
+//
+// One warp per row; lane l owns the 8 consecutive values 8 l + 256 j of the
+// row, so its codes of a 256-value chunk are one b-byte word.
+#include "gnn_internal.cuh"
+
+namespace gnn {
+
+namespace {
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t k) {
+    uint64_t z = seed + k * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// the 8 values c0 .. c0 + 7 of a row as fp32 (exact widening); values at or
+// past f are not read and come back as 0
+__device__ __forceinline__ void load8(const float *row, int64_t c0, int64_t f, float (&v)[8]) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (c0 < f) a = __ldg(reinterpret_cast<const float4 *>(row + c0));
+    if (c0 + 4 < f) b = __ldg(reinterpret_cast<const float4 *>(row + c0 + 4));
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *row, int64_t c0, int64_t f, float (&v)[8]) {
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (c0 < f) q = __ldg(reinterpret_cast<const uint4 *>(row + c0));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+
+// store the values of c0 .. c0 + 7 that lie below f
+__device__ __forceinline__ void store8(float *row, int64_t c0, int64_t f, const float (&v)[8]) {
+    if (c0 + 8 <= f) {
+        reinterpret_cast<float4 *>(row + c0)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(row + c0)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+        for (int k = 0; k < 8 && c0 + k < f; ++k) row[c0 + k] = v[k];
+    }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *row, int64_t c0, int64_t f, const float (&v)[8]) {
+    if (c0 + 8 <= f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint4 *>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        for (int k = 0; k < 8 && c0 + k < f; ++k) row[c0 + k] = __float2bfloat16_rn(v[k]);
+    }
+}
+
+// the b-byte word holding the codes of 8 values (code k in bits k*b ..)
+template <int BITS>
+struct CodeWord;
+template <>
+struct CodeWord<1> {
+    using type = uint8_t;
+};
+template <>
+struct CodeWord<2> {
+    using type = uint16_t;
+};
+template <>
+struct CodeWord<4> {
+    using type = uint32_t;
+};
+template <>
+struct CodeWord<8> {
+    using type = unsigned long long;
+};
+
+// Quantise pushed rows: row v of H goes to table row ids[v] if the claim pass
+// saw that id exactly once (else the row is skipped and the error word set).
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H, int64_t ld_h,
+                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
+                                                         const uint32_t *__restrict__ claim, uint32_t gen,
+                                                         uint8_t *__restrict__ codes, int64_t ld_codes,
+                                                         float *__restrict__ scale_zero, int64_t f, uint64_t seed,
+                                                         int *err) {
+    using W = typename CodeWord<BITS>::type;
+    constexpr int B = (1 << BITS) - 1;
+    const int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (v >= n) return;
+    const int64_t id = ids[v];
+    if (id < 0 || id >= n_table) return;  // reported by the claim pass
+    if (claim[id] != ((gen << 2) | 1u)) {
+        if (lane == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
+        return;
+    }
+    const T *h = H + v * ld_h;
+    // min and max of the row
+    float mn = INFINITY, mx = -INFINITY;
+    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+        float x[8];
+        load8(h, c0, f, x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (c0 + k < f) {
+                mn = fminf(mn, x[k]);
+                mx = fmaxf(mx, x[k]);
+            }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)B);
+    uint8_t *crow = codes + id * ld_codes;
+    const int64_t used = (f + 7) / 8 * BITS;  // code bytes of the row (whole 8-value words)
+    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+        float x[8];
+        load8(h, c0, f, x);
+        W word = 0;
+        if (s > 0.f) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t c = c0 + 2 * j;
+                const uint64_t z = splitmix64(seed, ((uint64_t)id << 15) + (uint64_t)(c >> 1) + 1u);
+                const float u[2] = {(float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f),
+                                    (float)(uint32_t)((z >> 16) & 0xFFFFFFu) * (1.0f / 16777216.0f)};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (c + e >= f) continue;
+                    const float t = __fdiv_rn(__fsub_rn(x[2 * j + e], mn), s);
+                    int q = (int)floorf(__fadd_rn(t, u[e]));
+                    q = q < 0 ? 0 : (q > B ? B : q);
+                    word |= (W)q << ((2 * j + e) * BITS);
+                }
+            }
+        }
+        *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = word;
+    }
+    // bytes past the codes are zero
+    for (int64_t b = used + lane; b < ld_codes; b += 32) crow[b] = 0;
+    if (lane == 0) {
+        scale_zero[2 * id] = s;
+        scale_zero[2 * id + 1] = mn;
+    }
+}
+
+// Dequantise halo rows: H[row0 + i] = code * scale + zero of table row ids[i].
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256) codec_pull_kernel(const uint8_t *__restrict__ codes, int64_t ld_codes,
+                                                         const float *__restrict__ scale_zero, int64_t n_table,
+                                                         const int64_t *__restrict__ ids, int64_t n, T *__restrict__ H,
+                                                         int64_t ld_h, int64_t row0, int64_t f, int *err) {
+    using W = typename CodeWord<BITS>::type;
+    constexpr int B = (1 << BITS) - 1;
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (i >= n) return;
+    const int64_t id = ids[i];
+    if (id < 0 || id >= n_table) {
+        if (lane == 0) atomicOr(err, 1);
+        return;
+    }
+    const float s = __ldg(scale_zero + 2 * id), z = __ldg(scale_zero + 2 * id + 1);
+    const uint8_t *crow = codes + id * ld_codes;
+    T *out = H + (row0 + i) * ld_h;
+    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+        const W word = __ldg(reinterpret_cast<const W *>(crow + c0 / 8 * BITS));
+        float y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int q = (int)((word >> (k * BITS)) & (W)B);
+            y[k] = __fadd_rn(__fmul_rn((float)q, s), z);
+        }
+        store8(out, c0, f, y);
+    }
+}
+
+template <typename F>
+gnn_status dispatch_bits(int bits, F &&fn) {
+    switch (bits) {
+        case 1: return fn(std::integral_constant<int, 1>());
+        case 2: return fn(std::integral_constant<int, 2>());
+        case 4: return fn(std::integral_constant<int, 4>());
+        case 8: return fn(std::integral_constant<int, 8>());
+    }
+    return GNN_EINVAL;
+}
+
+}  // namespace
+
+gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
+                             uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
+                             uint64_t seed, gnn_dtype dt, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    uint32_t gen = 0;
+    gnn_status st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
+    if (st != GNN_OK) return st;
+    const unsigned blocks = (unsigned)ceil_div(n_rows * 32, 256);
+    return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
+        constexpr int BITS = decltype(Bc)::value;
+        if (dt == GNN_BF16)
+            { codec_push_kernel<__nv_bfloat16, BITS><<<blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16 *>(H), ld_h, ids, n_rows, n_table, g->claim, gen, codes, ld_codes,
+                scale_zero, f, seed, g->err); GNN_LAUNCHED(1); }
+        else
+            { codec_push_kernel<float, BITS><<<blocks, 256, 0, s>>>(static_cast<const float *>(H), ld_h, ids, n_rows,
+                                                                   n_table, g->claim, gen, codes, ld_codes, scale_zero,
+                                                                   f, seed, g->err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+gnn_status launch_codec_pull(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n_table,
+                             int bits, const int64_t *ids, int64_t n_ids, void *H, int64_t ld_h, int64_t row0,
+                             int64_t f, gnn_dtype dt, int *err, cudaStream_t s) {
+    if (n_ids == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)ceil_div(n_ids * 32, 256);
+    return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
+        constexpr int BITS = decltype(Bc)::value;
+        if (dt == GNN_BF16)
+            { codec_pull_kernel<__nv_bfloat16, BITS><<<blocks, 256, 0, s>>>(
+                codes, ld_codes, scale_zero, n_table, ids, n_ids, static_cast<__nv_bfloat16 *>(H), ld_h, row0, f,
+                err); GNN_LAUNCHED(1); }
+        else
+            { codec_pull_kernel<float, BITS><<<blocks, 256, 0, s>>>(codes, ld_codes, scale_zero, n_table, ids, n_ids,
+                                                                   static_cast<float *>(H), ld_h, row0, f, err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+}  // namespace gnn

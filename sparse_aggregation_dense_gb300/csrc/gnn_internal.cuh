@@ -137,6 +137,17 @@ gnn_status launch_entry_weights(const int32_t *rowptr, const int32_t *colidx, in
 gnn_status launch_pull(const void *table, int64_t ld_t, int64_t n_table, const int64_t *ids, int64_t n_ids,
                        void *H, int64_t ld_h, int64_t row0, int64_t f, int es, int *err, cudaStream_t s);
 gnn_status ensure_claim(gnn_graph *g, int64_t n_table);
+// claim pass of a push: marks each table id with a generation-stamped count
+// (ids seen more than once are reported and skipped by the copy)
+gnn_status launch_push_claim(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, uint32_t *gen_out,
+                             cudaStream_t s);
+// low-bit halo codec (quantise on push, dequantise on pull)
+gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
+                             uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
+                             uint64_t seed, gnn_dtype dt, cudaStream_t s);
+gnn_status launch_codec_pull(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n_table,
+                             int bits, const int64_t *ids, int64_t n_ids, void *H, int64_t ld_h, int64_t row0,
+                             int64_t f, gnn_dtype dt, int *err, cudaStream_t s);
 gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                        void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s);
 

@@ -16,8 +16,10 @@ constexpr uint32_t kCountMask = 3u;  // low bits of a claim word: 0, 1 or 2 (= r
 constexpr int kRowsPerGroup = 8;  // rows a lane group moves at once (their loads are all in flight)
 
 // Copy rows src_row(k) -> dst_row(k) for the kRowsPerGroup rows of a lane
-// group; a row with a null source or destination is skipped.  Full 16-byte
-// vectors first (all rows' loads issued before the stores), then the tail.
+// group; a row with a null destination is not written (its source, when
+// given, is still read, so the loads need not wait for the destination's
+// checks), a row with a null source is skipped.  Full 16-byte vectors first
+// (all rows' loads issued before the stores), then the tail.
 template <int LPR>
 __device__ __forceinline__ void copy_rows(const char *const (&src)[kRowsPerGroup], char *const (&dst)[kRowsPerGroup],
                                           int64_t nbytes, int es, int sub) {
@@ -26,7 +28,7 @@ __device__ __forceinline__ void copy_rows(const char *const (&src)[kRowsPerGroup
         uint4 v[kRowsPerGroup];
 #pragma unroll
         for (int k = 0; k < kRowsPerGroup; ++k)
-            if (src[k] && dst[k]) v[k] = __ldg(reinterpret_cast<const uint4 *>(src[k]) + q);
+            if (src[k]) v[k] = __ldg(reinterpret_cast<const uint4 *>(src[k]) + q);
 #pragma unroll
         for (int k = 0; k < kRowsPerGroup; ++k)
             if (src[k] && dst[k]) reinterpret_cast<uint4 *>(dst[k])[q] = v[k];
@@ -114,13 +116,13 @@ __global__ void __launch_bounds__(256) push_copy_kernel(const char *__restrict__
         dst[k] = nullptr;
         const int64_t v = v0 + k;
         if (v >= n) continue;
+        src[k] = H + v * row_bytes_h;  // a local row: read whatever its id turns out to be
         const int64_t id = __ldg(ids + v);
         if (id < 0 || id >= n_table) continue;  // reported by the claim pass
         if (claim[id] != ((gen << 2) | 1u)) {
             if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
             continue;
         }
-        src[k] = H + v * row_bytes_h;
         dst[k] = table + id * row_bytes_t;
     }
     copy_rows<LPR>(src, dst, nbytes, es, sub);
@@ -177,9 +179,8 @@ gnn_status ensure_claim(gnn_graph *g, int64_t n_table) {
     return GNN_OK;
 }
 
-gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
-                       void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
-    if (n_rows == 0) return GNN_OK;
+gnn_status launch_push_claim(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, uint32_t *gen_out,
+                             cudaStream_t s) {
     gnn_status st = ensure_claim(g, n_table);
     if (st != GNN_OK) return st;
     g->claim_gen += 1;
@@ -190,6 +191,16 @@ gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows
     const uint32_t gen = g->claim_gen;
     { push_claim_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, s>>>(ids, n_rows, n_table, g->claim, gen, g->err); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
+    *gen_out = gen;
+    return GNN_OK;
+}
+
+gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
+                       void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    uint32_t gen = 0;
+    gnn_status st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
+    if (st != GNN_OK) return st;
     const int64_t nbytes = f * es;
     const int lpr = lanes_per_row(nbytes);
     return dispatch_lpr(lpr, [&](auto L) -> gnn_status {

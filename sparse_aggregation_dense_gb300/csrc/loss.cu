@@ -67,70 +67,87 @@ __device__ __forceinline__ uint4 pack_vec(const float (&v)[8]) {
 }
 
 // Rows of up to 32 * VPL 16-byte vectors of classes, rows 16-byte aligned:
-// lane q loads vectors q, q + 32, ... of its row once, keeps them in
-// registers, and writes the gradient back with 16-byte stores (element stores
-// only for the vector that straddles C, so G's padding is left alone).
-template <typename T, int VPL>
+// a warp takes RPW consecutive rows and loads all of them first (lane q holds
+// vectors q, q + 32, ... of each row), so RPW rows' loads are in flight at
+// once; then each row is reduced from registers and its gradient written back
+// with 16-byte stores (element stores only for the vector that straddles C,
+// so G's padding is left alone).
+template <typename T, int VPL, int RPW>
 __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
                                                            const int32_t *__restrict__ labels, T *__restrict__ G,
                                                            int64_t ld_g, float *__restrict__ row_loss) {
     constexpr int EPV = 16 / (int)sizeof(T);
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW;
     const int lane = threadIdx.x & 31;
-    if (i >= n) return;
-    const T *x = X + i * ld;
-    float v[VPL][EPV];
-    float mx = -INFINITY;
+    if (i0 >= n) return;
+    float v[RPW][VPL][EPV];
+    int32_t yl[RPW];
 #pragma unroll
-    for (int q = 0; q < VPL; ++q) {
-        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
-        if (c0 < C) {
-            unpack_vec(__ldcs(reinterpret_cast<const uint4 *>(x + c0)), v[q]);
-        } else {
+    for (int r = 0; r < RPW; ++r) {
+        const int64_t i = i0 + r;
+        yl[r] = i < n ? labels[i] : -1;
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) v[q][k] = -INFINITY;
-        }
+        for (int q = 0; q < VPL; ++q) {
+            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            if (i < n && c0 < C) {
+                unpack_vec(__ldcs(reinterpret_cast<const uint4 *>(X + i * ld + c0)), v[r][q]);
+            } else {
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            if (c0 + k >= C) v[q][k] = -INFINITY;
-            mx = fmaxf(mx, v[q][k]);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float se = 0.f, xy = 0.f;
-    const int32_t y = labels[i];
-#pragma unroll
-    for (int q = 0; q < VPL; ++q) {
-        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            if (c0 + k == y) xy = v[q][k];
-            v[q][k] = c0 + k < C ? expf(v[q][k] - mx) : 0.f;
-            se += v[q][k];
+                for (int k = 0; k < EPV; ++k) v[r][q][k] = -INFINITY;
+            }
         }
     }
+    const float inv_n = 1.0f / (float)n;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        se += __shfl_xor_sync(0xffffffffu, se, o);
-        xy += __shfl_xor_sync(0xffffffffu, xy, o);
-    }
-    const float inv_n = 1.0f / (float)n, inv_se = 1.0f / se;
-    T *gr = G + i * ld_g;
+    for (int r = 0; r < RPW; ++r) {
+        const int64_t i = i0 + r;
+        if (i >= n) break;
+        float mx = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < VPL; ++q) {
-        const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
-        if (c0 >= C) continue;
-        float o[EPV];
+        for (int q = 0; q < VPL; ++q) {
+            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) o[k] = (v[q][k] * inv_se - (c0 + k == y ? 1.f : 0.f)) * inv_n;
-        if (c0 + EPV <= C) {
-            __stcs(reinterpret_cast<uint4 *>(gr + c0), pack_vec(o));
-        } else {
-            for (int k = 0; k < EPV && c0 + k < C; ++k) st_elem(gr + c0 + k, o[k]);
+            for (int k = 0; k < EPV; ++k) {
+                if (c0 + k >= C) v[r][q][k] = -INFINITY;
+                mx = fmaxf(mx, v[r][q][k]);
+            }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float se = 0.f, xy = 0.f;
+        const int32_t y = yl[r];
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) {
+                if (c0 + k == y) xy = v[r][q][k];
+                v[r][q][k] = c0 + k < C ? expf(v[r][q][k] - mx) : 0.f;
+                se += v[r][q][k];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            se += __shfl_xor_sync(0xffffffffu, se, o);
+            xy += __shfl_xor_sync(0xffffffffu, xy, o);
+        }
+        const float inv_se = 1.0f / se;
+        T *gr = G + i * ld_g;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            if (c0 >= C) continue;
+            float o[EPV];
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) o[k] = (v[r][q][k] * inv_se - (c0 + k == y ? 1.f : 0.f)) * inv_n;
+            if (c0 + EPV <= C) {
+                __stcs(reinterpret_cast<uint4 *>(gr + c0), pack_vec(o));
+            } else {
+                for (int k = 0; k < EPV && c0 + k < C; ++k) st_elem(gr + c0 + k, o[k]);
+            }
+        }
+        if (lane == 0) row_loss[i] = (y >= 0 && y < C) ? mx + logf(se) - xy : NAN;
     }
-    if (lane == 0) row_loss[i] = (y >= 0 && y < C) ? mx + logf(se) - xy : NAN;
 }
 
 // Deterministic mean of row_loss in two passes: block b sums the fixed chunk
@@ -173,6 +190,8 @@ __global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float 
 
 }  // namespace
 
+constexpr int kRowsPerWarp = 4;
+
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
                              int64_t ld_g, float *row_loss, float *loss, gnn_dtype dt, cudaStream_t s) {
     const int es = dt == GNN_BF16 ? 2 : 4;
@@ -181,22 +200,23 @@ gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t 
                          ld % epv == 0 && ld_g % epv == 0;
     if (n > 0) {
         const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
+        const unsigned vblocks = (unsigned)ceil_div(ceil_div(n, kRowsPerWarp) * 32, 256);
         if (aligned && C <= 32 * epv) {
             if (dt == GNN_BF16)
-                { softmax_ce_rows_vec<__nv_bfloat16, 1><<<blocks, 256, 0, s>>>(
+                { softmax_ce_rows_vec<__nv_bfloat16, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
                     static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
                     ld_g, row_loss); GNN_LAUNCHED(1); }
             else
-                { softmax_ce_rows_vec<float, 1><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
+                { softmax_ce_rows_vec<float, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
                                                                       labels, static_cast<float *>(G), ld_g,
                                                                       row_loss); GNN_LAUNCHED(1); }
         } else if (aligned && C <= 64 * epv) {
             if (dt == GNN_BF16)
-                { softmax_ce_rows_vec<__nv_bfloat16, 2><<<blocks, 256, 0, s>>>(
+                { softmax_ce_rows_vec<__nv_bfloat16, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
                     static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
                     ld_g, row_loss); GNN_LAUNCHED(1); }
             else
-                { softmax_ce_rows_vec<float, 2><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
+                { softmax_ce_rows_vec<float, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
                                                                       labels, static_cast<float *>(G), ld_g,
                                                                       row_loss); GNN_LAUNCHED(1); }
         } else if (dt == GNN_BF16) {

@@ -28,7 +28,8 @@ GNN_AGG_GCN_SYM, GNN_AGG_SAGE_MEAN = 0, 1
 EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
     "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
-    "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+    "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_halo_push_quantized",
+    "gnn_halo_pull_quantized", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc",
 )
 
@@ -58,6 +59,8 @@ def _lib():
         L.gnn_graph_destroy.argtypes = [vp]
         L.gnn_halo_pull.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
         L.gnn_halo_push.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
+        L.gnn_halo_push_quantized.argtypes = [vp, vp, i64, i64, vp, vp, i64, vp, i64, i32, ctypes.c_uint64, i32, vp]
+        L.gnn_halo_pull_quantized.argtypes = [vp, vp, i64, vp, i64, i32, vp, vp, i64, i64, i32, vp]
         L.gnn_sage_half_offset.argtypes = [i64, i32]
         L.gnn_sage_half_offset.restype = i64
         L.gnn_layer_forward.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
@@ -224,6 +227,36 @@ def halo_push(g: Graph, H: torch.Tensor, local_ids: torch.Tensor, table: torch.T
     assert local_ids.dtype == torch.int64 and table.dtype == H.dtype
     _check(_lib().gnn_halo_push(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(local_ids), _ptr(table), ld_t,
                                 table.shape[0], _dtype(H), ctypes.c_void_p(_stream())), "gnn_halo_push")
+
+
+def codec_row_bytes(f: int, bits: int) -> int:
+    """Bytes of one row of f packed b-bit codes, padded to 16."""
+    return (f * bits + 127) // 128 * 16
+
+
+def halo_push_quantized(g: Graph, H: torch.Tensor, local_ids: torch.Tensor, codes: torch.Tensor,
+                        scale_zero: torch.Tensor, bits: int, seed: int):
+    """Quantise the local rows of H's view (b-bit stochastic rounding, per-row scale and zero point) into
+    codes[local_ids[v]] and scale_zero[local_ids[v]] (codes: uint8 n_table x ld_codes, scale_zero: float32
+    n_table x 2)."""
+    ld_h, f = _mat(H)
+    assert local_ids.dtype == torch.int64 and codes.dtype == torch.uint8 and scale_zero.dtype == torch.float32
+    assert codes.dim() == 2 and codes.stride(1) == 1 and scale_zero.is_contiguous()
+    _check(_lib().gnn_halo_push_quantized(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(local_ids), _ptr(codes),
+                                          codes.stride(0), _ptr(scale_zero), codes.shape[0], int(bits),
+                                          ctypes.c_uint64(seed & (2**64 - 1)), _dtype(H), ctypes.c_void_p(_stream())),
+           "gnn_halo_push_quantized")
+
+
+def halo_pull_quantized(g: Graph, codes: torch.Tensor, scale_zero: torch.Tensor, bits: int, halo_ids: torch.Tensor,
+                        H: torch.Tensor):
+    """H[n_local + i] = dequantised codes[halo_ids[i]] over the columns of H's view."""
+    ld_h, f = _mat(H)
+    assert halo_ids.dtype == torch.int64 and codes.dtype == torch.uint8 and scale_zero.dtype == torch.float32
+    assert codes.dim() == 2 and codes.stride(1) == 1 and scale_zero.is_contiguous()
+    _check(_lib().gnn_halo_pull_quantized(ctypes.c_void_p(g.handle), _ptr(codes), codes.stride(0), _ptr(scale_zero),
+                                          codes.shape[0], int(bits), _ptr(halo_ids), _ptr(H), ld_h, f, _dtype(H),
+                                          ctypes.c_void_p(_stream())), "gnn_halo_pull_quantized")
 
 
 def layer_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, Z: torch.Tensor, H_out: torch.Tensor):

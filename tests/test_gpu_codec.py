@@ -1,0 +1,134 @@
+"""Parity of the low-bit halo codec (Sylvie page, Quantizer / Dequantizer)
+through the C ABI with the oracle: codes, scales and zero points bit for bit,
+dequantised rows bit for bit (after the same bf16 rounding), on the tiny
+workloads for every bit width and on sampled rows of the full-size partition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth.configs import TINY, WORKLOADS
+from sparse_aggregation_dense_gb300 import gnn, padded
+from tests._gpu import assert_ok, gen_matrix, to_device, torch_dtype, widen
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0
+_cache = {}
+
+
+def problem(name, size):
+    key = (name, size)
+    if key not in _cache:
+        w = (TINY if size == "tiny" else WORKLOADS)[name]
+        part = w.make(SEED)
+        deg = None if part.deg is None else torch.from_numpy(part.deg).cuda()
+        g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(),
+                             part.n_local, part.n_halo, deg, w.agg)
+        _cache[key] = (w, part, g)
+    return _cache[key]
+
+
+def _values(host, dt, f):
+    """fp32 values of a generator matrix (bf16 bits widened exactly)."""
+    return widen(host, dt, f).astype(np.float32)
+
+
+@pytest.mark.parametrize("name", ["er5k", "rmat16m", "sage2m"])
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_push_quantized_matches_oracle(name, bits):
+    w, part, g = problem(name, "tiny")
+    dt, f = w.dtype, w.widths[1]
+    H_h = gen_matrix(part.n_local, f, dt, SEED, 300 + bits)
+    H = to_device(H_h, dt, f)
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.full((part.n_table, ldc), 0xAB, dtype=torch.uint8, device="cuda")
+    sz = torch.full((part.n_table, 2), -7.0, dtype=torch.float32, device="cuda")
+    seed = 0x5EED + bits
+    gnn.halo_push_quantized(g, H, torch.from_numpy(part.local_ids).cuda(), codes, sz, bits, seed)
+    assert_ok(g)
+    ref_c, ref_sz = oracle.quantize_rows(_values(H_h, dt, f), part.local_ids, bits, seed, ldc)
+    got_c, got_sz = codes.cpu().numpy(), sz.cpu().numpy()
+    np.testing.assert_array_equal(got_c[part.local_ids], ref_c)
+    np.testing.assert_array_equal(got_sz[part.local_ids].view(np.uint32), ref_sz.view(np.uint32))
+    other = np.setdiff1d(np.arange(part.n_table), part.local_ids)
+    assert np.all(got_c[other] == 0xAB) and np.all(got_sz[other] == -7.0)
+
+
+@pytest.mark.parametrize("name", ["er5k", "rmat16m", "powerlaw233k"])
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_pull_quantized_matches_oracle(name, bits):
+    w, part, g = problem(name, "tiny")
+    dt, f = w.dtype, w.widths[0]
+    T_h = gen_matrix(part.n_table, f, dt, SEED, 400 + bits)
+    ldc = gnn.codec_row_bytes(f, bits)
+    c, s = oracle.quantize_rows(_values(T_h, dt, f), np.arange(part.n_table), bits, 99, ldc)
+    H = padded(part.n_total, f, torch_dtype(dt), "cuda")
+    gnn.halo_pull_quantized(g, torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), bits,
+                            torch.from_numpy(part.halo_ids).cuda(), H)
+    assert_ok(g)
+    ref = oracle.dequantize_rows(c[part.halo_ids], s[part.halo_ids], f, bits)
+    got = H[part.n_local:].float().cpu().numpy()
+    if dt == "bf16":
+        ref = oracle.round_bf16(ref.astype(np.float64)).astype(np.float32)
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+    # local rows untouched (zero)
+    assert float(H[:part.n_local].abs().max()) == 0.0
+
+
+def test_round_trip_full_size_sampled():
+    # the bench partition: push all 8.4M local rows at 1 bit, pull the 4.2M
+    # halo rows back; sampled rows against the oracle
+    w, part, g = problem("rmat16m", "full")
+    f, bits, seed = w.widths[1], 1, 2024
+    H = padded(part.n_local, f, torch.bfloat16, "cuda")
+    H.copy_(torch.randn(part.n_local, f, device="cuda", generator=torch.Generator("cuda").manual_seed(3)))
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.zeros((part.n_table, ldc), dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((part.n_table, 2), dtype=torch.float32, device="cuda")
+    lid = torch.from_numpy(part.local_ids).cuda()
+    gnn.halo_push_quantized(g, H, lid, codes, sz, bits, seed)
+    assert_ok(g)
+    rng = np.random.default_rng(1)
+    rows = rng.choice(part.n_local, 2000, replace=False)
+    hv = H[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    ref_c, ref_sz = oracle.quantize_rows(hv, part.local_ids[rows], bits, seed, ldc)
+    tid = torch.from_numpy(part.local_ids[rows]).cuda()
+    np.testing.assert_array_equal(codes[tid].cpu().numpy(), ref_c)
+    np.testing.assert_array_equal(sz[tid].cpu().numpy().view(np.uint32), ref_sz.view(np.uint32))
+    Hin = padded(part.n_total, f, torch.bfloat16, "cuda")
+    gnn.halo_pull_quantized(g, codes, sz, bits, torch.from_numpy(part.halo_ids).cuda(), Hin)
+    assert_ok(g)
+    hs = rng.choice(part.n_halo, 2000, replace=False)
+    hid = part.halo_ids[hs]
+    ref = oracle.dequantize_rows(codes[torch.from_numpy(hid).cuda()].cpu().numpy(),
+                                 sz[torch.from_numpy(hid).cuda()].cpu().numpy(), f, bits)
+    ref = oracle.round_bf16(ref.astype(np.float64)).astype(np.float32)
+    got = Hin[part.n_local + torch.from_numpy(hs).cuda()].float().cpu().numpy()
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_codec_bad_ids_and_arguments():
+    w, part, g = problem("er5k", "tiny")
+    f, bits = w.widths[1], 2
+    H = to_device(gen_matrix(part.n_local, f, "f32", SEED, 5), "f32", f)
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.zeros((part.n_table, ldc), dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((part.n_table, 2), dtype=torch.float32, device="cuda")
+    ids = part.local_ids.copy()
+    ids[3] = ids[4]  # repeated id: both rows skipped, error word set
+    gnn.halo_push_quantized(g, H, torch.from_numpy(ids).cuda(), codes, sz, bits, 1)
+    assert gnn.get_error(g) == gnn.GNN_EINDEX
+    assert int(codes[ids[4]].abs().sum()) == 0
+    hids = part.halo_ids.copy()
+    hids[0] = part.n_table  # outside the table
+    Hin = padded(part.n_total, f, torch.float32, "cuda")
+    gnn.halo_pull_quantized(g, codes, sz, bits, torch.from_numpy(hids).cuda(), Hin)
+    assert gnn.get_error(g) == gnn.GNN_EINDEX
+    with pytest.raises(gnn.GnnError):
+        gnn.halo_push_quantized(g, H, torch.from_numpy(part.local_ids).cuda(), codes, sz, 3, 1)
+    with pytest.raises(gnn.GnnError):
+        narrow = torch.zeros((part.n_table, 8), dtype=torch.uint8, device="cuda")  # row pitch not a multiple of 16
+        gnn.halo_pull_quantized(g, narrow, sz, bits, torch.from_numpy(part.halo_ids).cuda(), Hin)
+    assert_ok(g)
