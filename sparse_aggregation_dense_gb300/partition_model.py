@@ -42,8 +42,15 @@ class PartitionModel:
     widths: [f_0, ..., f_L]; agg "gcn" | "sage"; dtype torch.float32 | torch.bfloat16.
     """
 
-    def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda"):
+    def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda",
+                 overlap: bool = False):
         self.widths = list(widths)
+        # overlap: pulls and pushes run on a second stream, concurrently with the layers (DIGEST
+        # system design, Fig. 1c: the table traffic is decoupled from the computation).  The rows a
+        # partition pulls (its halo) and pushes (its local vertices) are disjoint, so the schedule
+        # computes exactly what the sequential one does.
+        self.overlap = overlap
+        self.side = torch.cuda.Stream(device=device) if overlap else None
         self.L = len(widths) - 1
         self.agg = agg
         self.dtype = dtype
@@ -92,12 +99,38 @@ class PartitionModel:
 
     # ---- one epoch --------------------------------------------------------
     def forward(self):
+        if self.overlap:
+            return self._forward_overlapped()
         for l in range(self.L):
             if self.n_halo:
                 gnn.halo_pull(self.graph, self.tables[l], self.halo_ids, self.H[l])
             gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
             if l + 1 < self.L:
                 gnn.halo_push(self.graph, self.layer_out(l), self.local_ids, self.tables[l + 1])
+
+    def _forward_overlapped(self):
+        main = torch.cuda.current_stream(self.device)
+        start = torch.cuda.Event()
+        start.record(main)  # everything before this epoch (earlier readers of the halo rows) is done
+        pulled = [torch.cuda.Event() for _ in range(self.L)]
+        with torch.cuda.stream(self.side):
+            self.side.wait_event(start)
+            for l in range(self.L):
+                if self.n_halo:
+                    gnn.halo_pull(self.graph, self.tables[l], self.halo_ids, self.H[l])
+                pulled[l].record(self.side)
+        for l in range(self.L):
+            main.wait_event(pulled[l])
+            gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
+            if l + 1 < self.L:
+                done = torch.cuda.Event()
+                done.record(main)
+                with torch.cuda.stream(self.side):
+                    self.side.wait_event(done)
+                    gnn.halo_push(self.graph, self.layer_out(l), self.local_ids, self.tables[l + 1])
+        pushed = torch.cuda.Event()
+        pushed.record(self.side)
+        main.wait_event(pushed)  # the epoch ends when its pushes have landed
 
     def loss_grad(self):
         gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)

@@ -526,3 +526,26 @@ def test_softmax_ce_bad_label_gives_nan():
     loss = torch.empty(1, dtype=torch.float32, device="cuda")
     gnn.softmax_ce(X, torch.from_numpy(y).cuda(), G, row_loss, loss)
     assert np.isnan(float(loss.item()))
+
+
+# ---------------------------------------------------------------------------
+# overlapped schedule: pulls and pushes on a second stream give the same epoch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [(n, "tiny") for n in ALL] + [("rmat131k", "full")], ids=case_id)
+def test_overlapped_epoch_matches_sequential(case):
+    name, size = case
+    w, part, _ = problem(name, size)
+    results = []
+    for overlap in (False, True):
+        m, _, _, _ = _load_model(w, part)
+        if overlap:
+            m.overlap, m.side = True, torch.cuda.Stream()
+        for _ in range(2):  # the second epoch reads the tables the first one pushed
+            m.step()
+        m.check_errors()
+        torch.cuda.synchronize()
+        results.append([m.loss.cpu(), m.out_last.float().cpu()] + [d.cpu() for d in m.dW] +
+                       [t.float().cpu() for t in m.tables[1:]])
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
