@@ -7,6 +7,7 @@
 // training algorithm that works on directed graphs; entries of a transpose row
 // are ordered by ascending source row, so every later pass is deterministic.
 #include <atomic>
+#include <cstdlib>
 
 #include "gnn_internal.cuh"
 
@@ -600,7 +601,14 @@ int hot_tier_for(const Schedule &sc, int64_t row_bytes) {
         int dev = 0, l2 = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-        budget = (int64_t)((l2 > 0 ? l2 : 64 << 20) * 0.55);
+        // share of L2 given to rows gathered with evict_last: 0.55 by default,
+        // GNN_L2_KEEP_SHARE (0 .. 1) overrides it for tuning
+        double share = 0.55;
+        if (const char *e = getenv("GNN_L2_KEEP_SHARE")) {
+            const double v = atof(e);
+            if (v >= 0.0 && v <= 1.0) share = v;
+        }
+        budget = (int64_t)((l2 > 0 ? l2 : 64 << 20) * share);
     }
     int64_t rows = 0;
     int hot = -1;
