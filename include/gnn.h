@@ -202,6 +202,34 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
 gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
                           int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream);
 
+/* As gnn_softmax_ce, but the mean (and the gradient's 1/n) divides by n_mean
+ * >= n instead of n: the share of these n rows in the mean over n_mean rows
+ * spread over several partitions (summing the partitions' losses gives the
+ * whole mean, and their G together are the gradient of it). */
+gnn_status gnn_softmax_ce_partial(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels,
+                                  void *G, int64_t ld_g, float *row_loss, float *loss, int64_t n_mean,
+                                  gnn_dtype dtype, void *stream);
+
+/* Halo-gradient return (Sylvie page, backward propagation and Alg. 2: the
+ * feature gradients J of a partition's HALO vertices go back to the owning
+ * partitions and are added to their gradients), through an fp32 gradient table
+ * indexed by global vertex id (gtable device float, n_table x ld_gt, ld_gt a
+ * multiple of 4; the caller zeroes it before the first send of a layer).
+ * Send:    gtable[halo_ids[i], 0:f] += dH[n_local + i, 0:f]   for i < n_halo
+ *          (dH as written by gnn_layer_backward with want_halo_grad).  The halo
+ *          ids of one graph are distinct: a repeated id sets GNN_EINDEX on the
+ *          device and its rows are not sent; an id outside [0, n_table) too.
+ *          Uses the push claim array.
+ * Receive: dH[v, 0:f] += gtable[local_ids[v], 0:f]            for v < n_local
+ *          (fp32 sum, rounded to dtype).
+ * Sends of several graphs into one table, issued in order on one stream, add
+ * in that order: the sums are reproducible bit for bit. */
+gnn_status gnn_halo_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
+                              float *gtable, int64_t ld_gt, int64_t n_table, gnn_dtype dtype, void *stream);
+gnn_status gnn_halo_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, int64_t n_table,
+                              const int64_t *local_ids, void *dH, int64_t ld_dh, int64_t f, gnn_dtype dtype,
+                              void *stream);
+
 /* Synchronise the device, then return and clear the graph's device error word
  * (GNN_OK or GNN_EINDEX); GNN_ECUDA if the synchronisation itself failed. */
 gnn_status gnn_get_error(gnn_graph *g);

@@ -6,3 +6,4 @@ binding and ``partition_model`` drives one partition's epoch through it.
 """
 from . import gnn  # noqa: F401
 from .partition_model import PartitionModel, ld_for, padded  # noqa: F401
+from .multi_partition import MultiPartitionTrainer  # noqa: F401

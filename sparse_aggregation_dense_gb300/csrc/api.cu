@@ -495,7 +495,38 @@ gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, 
                           int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream) {
     if (!dtype_ok(dtype) || n < 0 || C <= 0 || !loss) return GNN_EINVAL;
     if (n > 0 && (!logits || !labels || !G || !row_loss || ld < C || ld_g < C)) return GNN_EINVAL;
-    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, dtype, as_stream(stream));
+    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n, dtype, as_stream(stream));
+}
+
+gnn_status gnn_softmax_ce_partial(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels,
+                                  void *G, int64_t ld_g, float *row_loss, float *loss, int64_t n_mean,
+                                  gnn_dtype dtype, void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || C <= 0 || !loss || n_mean < n || n_mean <= 0) return GNN_EINVAL;
+    if (n > 0 && (!logits || !labels || !G || !row_loss || ld < C || ld_g < C)) return GNN_EINVAL;
+    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n_mean, dtype, as_stream(stream));
+}
+
+gnn_status gnn_halo_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
+                              float *gtable, int64_t ld_gt, int64_t n_table, gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f <= 0 || n_table < 0) return GNN_EINVAL;
+    if (g->n_halo == 0) return GNN_OK;
+    if (!halo_ids || !operand_ok(dH, g->n_local + g->n_halo, ld_dh, f, dtype) ||
+        !operand_ok(gtable, n_table > 0 ? 1 : 0, ld_gt, f, GNN_F32))
+        return GNN_EINVAL;
+    gnn_status st = ensure_claim(g, n_table);
+    if (st != GNN_OK) return st;
+    return launch_grad_send(g, dH, ld_dh, f, halo_ids, gtable, ld_gt, n_table, dtype, as_stream(stream));
+}
+
+gnn_status gnn_halo_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, int64_t n_table,
+                              const int64_t *local_ids, void *dH, int64_t ld_dh, int64_t f, gnn_dtype dtype,
+                              void *stream) {
+    if (!g || !dtype_ok(dtype) || f <= 0 || n_table < 0) return GNN_EINVAL;
+    if (g->n_local == 0) return GNN_OK;
+    if (!local_ids || !operand_ok(dH, g->n_local, ld_dh, f, dtype) ||
+        !operand_ok(gtable, n_table > 0 ? 1 : 0, ld_gt, f, GNN_F32))
+        return GNN_EINVAL;
+    return launch_grad_recv(g, gtable, ld_gt, n_table, local_ids, dH, ld_dh, f, dtype, as_stream(stream));
 }
 
 }  // extern "C"

@@ -141,6 +141,12 @@ gnn_status ensure_claim(gnn_graph *g, int64_t n_table);
 // (ids seen more than once are reported and skipped by the copy)
 gnn_status launch_push_claim(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, uint32_t *gen_out,
                              cudaStream_t s);
+// halo-gradient return: send J rows into an fp32 gradient table, receive the sums
+gnn_status launch_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
+                            float *gtable, int64_t ld_gt, int64_t n_table, gnn_dtype dt, cudaStream_t s);
+gnn_status launch_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, int64_t n_table,
+                            const int64_t *local_ids, void *dH, int64_t ld_dh, int64_t f, gnn_dtype dt,
+                            cudaStream_t s);
 // low-bit halo codec (quantise on push, dequantise on pull)
 gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                              uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
@@ -219,6 +225,7 @@ gnn_status launch_update_bwd(const void *G, int64_t ld_g, const void *Hout, int6
 size_t update_bwd_ws_bytes(int64_t n, int64_t Kp, int64_t N, gnn_dtype dt);
 
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                             int64_t ld_g, float *row_loss, float *loss, gnn_dtype dt, cudaStream_t s);
+                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt,
+                             cudaStream_t s);
 
 }  // namespace gnn

@@ -17,7 +17,7 @@ __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v) { *p = __floa
 template <typename T>
 __global__ void softmax_ce_rows(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
                                 const int32_t *__restrict__ labels, T *__restrict__ G, int64_t ld_g,
-                                float *__restrict__ row_loss) {
+                                float *__restrict__ row_loss, float inv_n) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= n) return;
@@ -33,7 +33,6 @@ __global__ void softmax_ce_rows(const T *__restrict__ X, int64_t ld, int64_t n, 
     const float lse = mx + logf(se);
     const int32_t y = labels[i];
     const bool ok = y >= 0 && y < C;
-    const float inv_n = 1.0f / (float)n;
     for (int64_t c = lane; c < C; c += 32) {
         float p = expf(ld_elem(x + c) - lse);
         st_elem(G + i * ld_g + c, (p - (c == y ? 1.f : 0.f)) * inv_n);
@@ -75,7 +74,7 @@ __device__ __forceinline__ uint4 pack_vec(const float (&v)[8]) {
 template <typename T, int VPL, int RPW>
 __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
                                                            const int32_t *__restrict__ labels, T *__restrict__ G,
-                                                           int64_t ld_g, float *__restrict__ row_loss) {
+                                                           int64_t ld_g, float *__restrict__ row_loss, float inv_n) {
     constexpr int EPV = 16 / (int)sizeof(T);
     const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW;
     const int lane = threadIdx.x & 31;
@@ -97,7 +96,6 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
             }
         }
     }
-    const float inv_n = 1.0f / (float)n;
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         const int64_t i = i0 + r;
@@ -179,13 +177,13 @@ __global__ void __launch_bounds__(kLossThreads) loss_chunk_sums(float *__restric
     if (threadIdx.x == 0) v[b0] = tot;  // every read of the chunk is done (barriers above)
 }
 
-__global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float *__restrict__ v, int64_t n,
+__global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float *__restrict__ v, int64_t n_mean,
                                                                      int64_t n_chunks, float *out) {
     __shared__ float part[kLossThreads];
     float s = 0.f;
     for (int64_t c = threadIdx.x; c < n_chunks; c += kLossThreads) s += v[c * kLossChunk];
     const float tot = block_sum_fixed(s, part);
-    if (threadIdx.x == 0) *out = n > 0 ? tot / (float)n : 0.f;
+    if (threadIdx.x == 0) *out = n_mean > 0 ? tot / (float)n_mean : 0.f;
 }
 
 }  // namespace
@@ -193,7 +191,9 @@ __global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float 
 constexpr int kRowsPerWarp = 4;
 
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                             int64_t ld_g, float *row_loss, float *loss, gnn_dtype dt, cudaStream_t s) {
+                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt,
+                             cudaStream_t s) {
+    const float inv_n = n_mean > 0 ? 1.0f / (float)n_mean : 0.f;
     const int es = dt == GNN_BF16 ? 2 : 4;
     const int epv = 16 / es;
     const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(G)) & 15u) == 0 &&
@@ -205,27 +205,24 @@ gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t 
             if (dt == GNN_BF16)
                 { softmax_ce_rows_vec<__nv_bfloat16, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
                     static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
-                    ld_g, row_loss); GNN_LAUNCHED(1); }
+                    ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
             else
                 { softmax_ce_rows_vec<float, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
-                                                                      labels, static_cast<float *>(G), ld_g,
-                                                                      row_loss); GNN_LAUNCHED(1); }
+                                                                      labels, static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
         } else if (aligned && C <= 64 * epv) {
             if (dt == GNN_BF16)
                 { softmax_ce_rows_vec<__nv_bfloat16, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
                     static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
-                    ld_g, row_loss); GNN_LAUNCHED(1); }
+                    ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
             else
                 { softmax_ce_rows_vec<float, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
-                                                                      labels, static_cast<float *>(G), ld_g,
-                                                                      row_loss); GNN_LAUNCHED(1); }
+                                                                      labels, static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
         } else if (dt == GNN_BF16) {
             { softmax_ce_rows<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(logits), ld, n,
-                                                                   C, labels, static_cast<__nv_bfloat16 *>(G), ld_g,
-                                                                   row_loss); GNN_LAUNCHED(1); }
+                                                                   C, labels, static_cast<__nv_bfloat16 *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
         } else {
             { softmax_ce_rows<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C, labels,
-                                                          static_cast<float *>(G), ld_g, row_loss); GNN_LAUNCHED(1); }
+                                                          static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
         }
         GNN_CUDA_TRY(cudaGetLastError());
     }
@@ -234,7 +231,7 @@ gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t 
         { loss_chunk_sums<<<(unsigned)n_chunks, kLossThreads, 0, s>>>(row_loss, n); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
-    { loss_mean_of_chunks<<<1, kLossThreads, 0, s>>>(row_loss, n, n_chunks, loss); GNN_LAUNCHED(1); }
+    { loss_mean_of_chunks<<<1, kLossThreads, 0, s>>>(row_loss, n_mean, n_chunks, loss); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

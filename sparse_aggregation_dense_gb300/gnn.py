@@ -29,7 +29,7 @@ EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
     "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
     "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_halo_push_quantized",
-    "gnn_halo_pull_quantized", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+    "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc",
 )
 
@@ -67,6 +67,9 @@ def _lib():
         L.gnn_layer_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp, i64, i32,
                                          i32, vp]
         L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, vp]
+        L.gnn_softmax_ce_partial.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp]
+        L.gnn_halo_grad_send.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
+        L.gnn_halo_grad_recv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
         L.gnn_get_error.argtypes = [vp]
         L.gnn_graph_sizes.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.gnn_graph_copy_transpose.argtypes = [vp, vp, vp, vp, vp]
@@ -292,3 +295,33 @@ def softmax_ce(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_
     ld_g, _ = _mat(G)
     _check(_lib().gnn_softmax_ce(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g, _ptr(row_loss),
                                  _ptr(loss), _dtype(logits), ctypes.c_void_p(_stream())), "gnn_softmax_ce")
+
+
+def softmax_ce_partial(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_loss: torch.Tensor,
+                       loss: torch.Tensor, n_mean: int):
+    """softmax_ce whose mean (and gradient) divides by n_mean >= the rows of logits."""
+    ld, C = _mat(logits)
+    ld_g, _ = _mat(G)
+    _check(_lib().gnn_softmax_ce_partial(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g,
+                                         _ptr(row_loss), _ptr(loss), int(n_mean), _dtype(logits),
+                                         ctypes.c_void_p(_stream())), "gnn_softmax_ce_partial")
+
+
+def halo_grad_send(g: Graph, dH: torch.Tensor, halo_ids: torch.Tensor, gtable: torch.Tensor):
+    """gtable[halo_ids[i]] += dH[n_local + i] over the columns of dH's view (gtable: float32)."""
+    ld_h, f = _mat(dH)
+    ld_t, _ = _mat(gtable)
+    assert halo_ids.dtype == torch.int64 and gtable.dtype == torch.float32
+    _check(_lib().gnn_halo_grad_send(ctypes.c_void_p(g.handle), _ptr(dH), ld_h, f, _ptr(halo_ids), _ptr(gtable),
+                                     ld_t, gtable.shape[0], _dtype(dH), ctypes.c_void_p(_stream())),
+           "gnn_halo_grad_send")
+
+
+def halo_grad_recv(g: Graph, gtable: torch.Tensor, local_ids: torch.Tensor, dH: torch.Tensor):
+    """dH[v] += gtable[local_ids[v]] for the local rows, over the columns of dH's view."""
+    ld_h, f = _mat(dH)
+    ld_t, _ = _mat(gtable)
+    assert local_ids.dtype == torch.int64 and gtable.dtype == torch.float32
+    _check(_lib().gnn_halo_grad_recv(ctypes.c_void_p(g.handle), _ptr(gtable), ld_t, gtable.shape[0],
+                                     _ptr(local_ids), _ptr(dH), ld_h, f, _dtype(dH), ctypes.c_void_p(_stream())),
+           "gnn_halo_grad_recv")
