@@ -109,26 +109,38 @@ def workload_by_name(name: str):
 # ---------------------------------------------------------------------------
 
 def edge_feat_per_step(part, w) -> int:
-    """Entries x feature width summed over the step's aggregations (forward on
-    every layer; backward, over the transpose, on every layer but the first)."""
+    """Entries x feature width summed over the step's aggregations of the layer in
+    its textbook order (forward on every layer at its input width; backward, over
+    the transpose, on every layer but the first): a fixed property of the workload,
+    whatever order the library multiplies in."""
     fwd = sum(part.nnz * f for f in w.widths[:-1])
     bwd = sum(part.nnz * f for f in w.widths[1:-1])
     return int(fwd + bwd)
 
 
-def aggregation_bytes(part, w, elem: int):
+def narrow_layers(w, enabled: bool = False):
+    """Layers the partition model runs with the multiplication first (--narrow: GCN, output narrower than input)."""
+    return [enabled and w.agg != "sage" and w.widths[l + 1] < w.widths[l] for l in range(w.layers)]
+
+
+def aggregation_bytes(part, w, elem: int, narrow: bool = False):
     """Compulsory bytes of each aggregation launch of one step, in launch order
     (forward layers 0..L-1, then backward layers L-1..1): row pointers, column
-    ids, the normalisation vector, every input row once and every output row once."""
+    ids, the normalisation vector, every input row once and every output row once.
+    A narrow layer aggregates at its output width (T = H W forward, dY backward),
+    and its backward aggregation also runs on the first layer."""
     nL, nT, nnz = part.n_local, part.n_total, part.nnz
     sage = w.agg == "sage"
+    nar = narrow_layers(w, narrow)
     fwd, bwd = [], []
     for l in range(w.layers):
-        f = w.widths[l]
+        f = w.widths[l + 1] if nar[l] else w.widths[l]
         out_cols = 2 * f if sage else f
         fwd.append(4 * (nL + 1) + 4 * nnz + 4 * (nL if sage else nT) + nT * f * elem + nL * out_cols * elem)
-    for l in range(w.layers - 1, 0, -1):
-        f = w.widths[l]
+    for l in range(w.layers - 1, -1, -1):
+        if l == 0 and not nar[l]:
+            continue
+        f = w.widths[l + 1] if nar[l] else w.widths[l]
         in_cols = 2 * f if sage else f
         bwd.append(4 * (nT + 1) + 4 * nnz + 4 * (nL if sage else nT) + nL * in_cols * elem + nT * f * elem)
     return fwd, bwd
@@ -414,7 +426,7 @@ def run_ours(args, rank, world, local_rank):
     part = w.make(SEED + rank)
     t_gen = time.time() - t_gen
     t_create = time.time()
-    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda", overlap=not args.sequential)
+    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda", overlap=not args.sequential, narrow=args.narrow)
     torch.cuda.synchronize()
     t_create = time.time() - t_create
     for l in range(w.layers):
@@ -471,7 +483,7 @@ def run_ours(args, rank, world, local_rank):
 
     # dominant kernel: the aggregation (forward + backward launches)
     hbm, bf16_tf, peak_kind = measured_peaks()
-    fwd_b, bwd_b = aggregation_bytes(part, w, 2 if bf else 4)
+    fwd_b, bwd_b = aggregation_bytes(part, w, 2 if bf else 4, args.narrow)
     alg_bytes = (sum(fwd_b) + sum(bwd_b)) * args.steps
     agg_ms = prof["agg_fwd"][0] + prof["agg_bwd"][0]
     agg_launches = prof["agg_fwd"][1] + prof["agg_bwd"][1]
@@ -545,6 +557,7 @@ def run_ours(args, rank, world, local_rank):
             "l2": ("inputs larger than L2 (no flush)" if flush is None
                    else "L2 flushed before every timed step (512 MiB written); steps timed one by one"),
             "seed": SEED,
+            "layer_order": "multiplication first on narrowing GCN layers" if args.narrow else "aggregation first",
         },
         "roofline": {
             "bound": "hbm",
@@ -621,6 +634,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work timed for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=3.0, help="oracle work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--narrow", action="store_true",
+                    help="GCN layers whose output is narrower than their input multiply first: A (H W)")
     ap.add_argument("--sequential", action="store_true",
                     help="pulls and pushes in line on the compute stream instead of on a second stream")
     args = ap.parse_args(argv)

@@ -192,6 +192,33 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
                               float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
                               gnn_dtype dtype, void *stream);
 
+/* The same GCN layer with the multiplication first, for layers whose output
+ * is narrower than their input (f_out < f_in): A_hat (H W) = (A_hat H) W, so
+ * the aggregations run at width f_out instead of f_in (fewer bytes gathered);
+ * the results agree with gnn_layer_forward / gnn_layer_backward up to
+ * rounding (bf16 storage rounds T and P instead of Z and dZ).  GCN only
+ * (GraphSAGE: GNN_EUNSUPPORTED).
+ * Forward:
+ *   T     = H W                          device (n_local + n_halo) x ld_t, dtype
+ *                                        (work; every row, local and halo)
+ *   H_out = relu ? max(A_hat_block T, 0) : A_hat_block T    (n_local rows)
+ * Backward (T is not needed; the layer input H is):
+ *   dY = relu ? G * 1[H_out > 0] : G
+ *   P  = A_hat_block^T dY               device (n_local + n_halo) x ld_p, dtype
+ *                                        (work; every row)
+ *   dW = H^T P                           device float[f_in x f_out], overwritten
+ *   dH = P W^T                           device (n_local + n_halo) x ld_dh, dtype,
+ *                                        every row (the halo rows are Sylvie's
+ *                                        J), or NULL to skip
+ * The other arguments are as for gnn_layer_forward / gnn_layer_backward. */
+gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
+                                    int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
+                                    gnn_dtype dtype, void *stream);
+gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                                     const void *H, int64_t ld_h, const float *W, int64_t f_in, int64_t f_out,
+                                     int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
+                                     gnn_dtype dtype, void *stream);
+
 /* Training-harness helper (not a layer step): mean softmax cross-entropy over
  * n rows of C logits with integer labels.
  *   logits  device n x ld, dtype;  labels device int32[n] in [0, C)

@@ -577,6 +577,10 @@ __global__ void __launch_bounds__(WPC * 32)
                             stg_words<VW>(out + c0, q, pol_stream);
                         }
                     }
+                    if (p.relu) {
+#pragma unroll
+                        for (int k = 0; k < EPL; ++k) o[k] = o[k] > 0.f ? o[k] : 0.f;
+                    }
                     uint32_t q[VW / 4];
                     vals_to_words<T, VW>(o, f_left, q);
                     stg_words<VW>(out + p.out_off + c0, q, pol_stream);
@@ -693,6 +697,12 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
                 if (col + 3 >= f) sv.w = 0.f;
                 store4(out + col, sv);
             }
+        }
+        if (p.relu) {
+            o.x = o.x > 0.f ? o.x : 0.f;
+            o.y = o.y > 0.f ? o.y : 0.f;
+            o.z = o.z > 0.f ? o.z : 0.f;
+            o.w = o.w > 0.f ? o.w : 0.f;
         }
         if (col + 0 >= f) o.x = 0.f;
         if (col + 1 >= f) o.y = 0.f;

@@ -52,6 +52,17 @@ __global__ void unpack_dw_kernel(const float *__restrict__ dWp, int64_t N, int64
     dW[x] = dWp[kp * N + j];
 }
 
+// dY = G * 1[H_out > 0] (ReLU'(0) = 0), element by element
+template <typename T>
+__global__ void relu_mask_kernel(const T *__restrict__ G, int64_t ld_g, const T *__restrict__ Hout, int64_t ld_h,
+                                 int64_t n, int64_t f, T *__restrict__ Y, int64_t ld_y) {
+    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= n * f) return;
+    const int64_t r = x / f, c = x % f;
+    const T h = Hout[r * ld_h + c];
+    Y[r * ld_y + c] = (float)h > 0.f ? G[r * ld_g + c] : T(0.f);
+}
+
 }  // namespace
 
 namespace gnn {
@@ -489,6 +500,140 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     }
     ProfScope prof(g, GNN_PROF_AGG_BWD, s);
     return launch_aggregate(p, g->bwd, dtype, partial, s);
+}
+
+gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
+                                    int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
+                                    gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W) return GNN_EINVAL;
+    if (g->agg != GNN_AGG_GCN_SYM) return GNN_EUNSUPPORTED;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    if (!operand_ok(H, nT, ld_h, f_in, dtype) || !operand_ok(T, nT, ld_t, f_out, dtype) ||
+        !operand_ok(H_out, nL, ld_out, f_out, dtype))
+        return GNN_EINVAL;
+    if (f_out * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    if (nL == 0) return GNN_OK;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const bool use_tc = dtype == GNN_BF16 && update_fwd_tc_supported(f_in, f_out) && !force_simt_update();
+    const size_t wp_bytes = align_up((size_t)f_in * ldw * sizeof(float));
+    const size_t wt_bytes = use_tc ? align_up(update_tc_wt_bytes(f_in, f_out)) : 0;
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->fwd, f_out));
+    gnn_status st = ensure_workspace(g, wp_bytes + wt_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    float *Wp = static_cast<float *>(g->ws);
+    void *wt = static_cast<char *>(g->ws) + wp_bytes;
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(g->ws) + wp_bytes + wt_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(f_in * ldw, 256), 256, 0, s>>>(W, f_in, f_out, f_in, f_in, 0, f_in, Wp, ldw,
+                                                                        dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    {
+        // T = H W over every row, local and halo (the multiplication first)
+        ProfScope prof(g, GNN_PROF_UPD_FWD, s);
+        st = use_tc ? launch_update_fwd_tc(H, ld_h, nT, f_in, Wp, ldw, f_out, 0, T, ld_t, wt, g->err, s)
+                    : launch_update_fwd(H, ld_h, nT, f_in, Wp, ldw, f_out, 0, T, ld_t, dtype, s);
+    }
+    if (st != GNN_OK) return st;
+    AggParams p{};
+    p.err = g->err;
+    p.rowptr = g->rowptr;
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
+    p.wts = g->wfwd;
+    p.rowscale = g->colw;
+    p.n_rows = nL;
+    p.colmask = g->fwd.tagged ? kColMask : 0xffffffffu;
+    p.hot_tier = hot_tier_for(g->fwd, round_up(f_out * elem_size(dtype), 32));
+    p.X = T;
+    p.ldx = ld_t;
+    p.n_x = nT;
+    p.f = f_out;
+    p.self_mode = SELF_NONE;
+    p.out = H_out;
+    p.ldo = ld_out;
+    p.out_off = 0;
+    p.relu = relu;
+    ProfScope prof(g, GNN_PROF_AGG_FWD, s);
+    return launch_aggregate(p, g->fwd, dtype, partial, s);
+}
+
+gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                                     const void *H, int64_t ld_h, const float *W, int64_t f_in, int64_t f_out,
+                                     int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
+                                     gnn_dtype dtype, void *stream) {
+    if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W || !dW) return GNN_EINVAL;
+    if (g->agg != GNN_AGG_GCN_SYM) return GNN_EUNSUPPORTED;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    if (!operand_ok(G, nL, ld_g, f_out, dtype) || !operand_ok(H, nT, ld_h, f_in, dtype) ||
+        !operand_ok(P, nT, ld_p, f_out, dtype))
+        return GNN_EINVAL;
+    if (relu && !operand_ok(H_out, nL, ld_out, f_out, dtype)) return GNN_EINVAL;
+    if (dH && !operand_ok(dH, nT, ld_dh, f_in, dtype)) return GNN_EINVAL;
+    if (f_out * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const int64_t ldy = round_up(f_out, elems_per_16b(dtype));
+    const bool use_tc = dtype == GNN_BF16 && update_bwd_tc_supported(f_in, f_out) && !force_simt_update();
+    const size_t wp_bytes = align_up((size_t)f_in * ldw * sizeof(float));
+    const size_t y_bytes = relu ? align_up((size_t)nL * ldy * elem_size(dtype)) : 0;
+    const size_t wg_bytes = align_up(use_tc ? update_bwd_tc_ws_bytes(nT, f_in, f_out)
+                                            : update_bwd_ws_bytes(nT, f_in, f_out, dtype));
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->bwd, f_out));
+    gnn_status st = ensure_workspace(g, wp_bytes + y_bytes + wg_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    char *base = static_cast<char *>(g->ws);
+    float *Wp = reinterpret_cast<float *>(base);
+    void *Y = base + wp_bytes;
+    float *wg = reinterpret_cast<float *>(base + wp_bytes + y_bytes);
+    float *partial = reinterpret_cast<float *>(base + wp_bytes + y_bytes + wg_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(f_in * ldw, 256), 256, 0, s>>>(W, f_in, f_out, f_in, f_in, 0, f_in, Wp, ldw,
+                                                                        dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    // dY = G (masked by the ReLU), then P = A_hat^T dY over every row, local and halo
+    const void *dY = G;
+    int64_t ld_y = ld_g;
+    if (relu && nL > 0) {
+        const unsigned blocks = (unsigned)ceil_div(nL * f_out, 256);
+        if (dtype == GNN_BF16)
+            { relu_mask_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(G), ld_g,
+                                                                     static_cast<const __nv_bfloat16 *>(H_out), ld_out,
+                                                                     nL, f_out, static_cast<__nv_bfloat16 *>(Y), ldy); GNN_LAUNCHED(1); }
+        else
+            { relu_mask_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(G), ld_g,
+                                                             static_cast<const float *>(H_out), ld_out, nL, f_out,
+                                                             static_cast<float *>(Y), ldy); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        dY = Y;
+        ld_y = ldy;
+    }
+    {
+        AggParams p{};
+        p.err = g->err;
+        p.rowptr = g->rowptrT;
+        p.colidx = reinterpret_cast<const uint32_t *>(g->colidxT);
+        p.wts = g->wbwd;
+        p.rowscale = g->colw;
+        p.n_rows = nT;
+        p.colmask = g->bwd.tagged ? kColMask : 0xffffffffu;
+        p.hot_tier = hot_tier_for(g->bwd, round_up(f_out * elem_size(dtype), 32));
+        p.X = dY;
+        p.ldx = ld_y;
+        p.n_x = nL;
+        p.f = f_out;
+        p.self_mode = SELF_NONE;
+        p.out = P;
+        p.ldo = ld_p;
+        p.out_off = 0;
+        ProfScope prof(g, GNN_PROF_AGG_BWD, s);
+        st = launch_aggregate(p, g->bwd, dtype, partial, s);
+    }
+    if (st != GNN_OK) return st;
+    // dW = H^T P and dH = P W^T over every row
+    ProfScope prof(g, GNN_PROF_UPD_BWD, s);
+    if (use_tc)
+        return launch_update_bwd_tc(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, wg,
+                                    g->err, s);
+    return launch_update_bwd(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, dtype, wg,
+                             wg_bytes, s);
 }
 
 gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,

@@ -185,6 +185,7 @@ struct AggParams {
     const void *self;        // SELF_ADD source (row stride ld_self)
     int64_t ld_self;
     int64_t n_self;
+    int relu;                // 1: the aggregated values are written as max(x, 0)
     int *err;                // device error word
 };
 gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s);

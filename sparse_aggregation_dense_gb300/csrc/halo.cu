@@ -15,41 +15,51 @@ constexpr uint32_t kCountMask = 3u;  // low bits of a claim word: 0, 1 or 2 (= r
 
 constexpr int kRowsPerGroup = 8;  // rows a lane group moves at once (their loads are all in flight)
 
-// Copy rows src_row(k) -> dst_row(k) for the kRowsPerGroup rows of a lane
-// group; a row with a null destination is not written (its source, when
-// given, is still read, so the loads need not wait for the destination's
-// checks), a row with a null source is skipped.  Full 16-byte vectors first
-// (all rows' loads issued before the stores), then the tail.
-template <int LPR>
-__device__ __forceinline__ void copy_rows(const char *const (&src)[kRowsPerGroup], char *const (&dst)[kRowsPerGroup],
+// Copy kRowsPerGroup rows of a lane group: row k goes from src + sidx(k) *
+// sbytes to dst + didx(k) * dbytes.  One of the two indices is computed from
+// the group's first row, the other comes from an id array (held as int64 in
+// `ix`, -1 = skip the row).  Full 16-byte vectors first, every row's load
+// issued before the stores, then (when nbytes is not a multiple of 16) the
+// element tail.  GATHER: the ids index the source (pull); else the
+// destination (push).
+template <int LPR, bool GATHER>
+__device__ __forceinline__ void copy_rows(const char *__restrict__ src, int64_t sbytes, char *__restrict__ dst,
+                                          int64_t dbytes, int64_t first, const int64_t (&ix)[kRowsPerGroup],
                                           int64_t nbytes, int es, int sub) {
     const int64_t nvec = nbytes / 16;
     for (int64_t q = sub; q < nvec; q += LPR) {
         uint4 v[kRowsPerGroup];
 #pragma unroll
-        for (int k = 0; k < kRowsPerGroup; ++k)
-            if (src[k]) v[k] = __ldg(reinterpret_cast<const uint4 *>(src[k]) + q);
-#pragma unroll
-        for (int k = 0; k < kRowsPerGroup; ++k)
-            if (src[k] && dst[k]) reinterpret_cast<uint4 *>(dst[k])[q] = v[k];
-    }
-    if (sub == 0) {
-        const int64_t tail0 = nvec * 16;
         for (int k = 0; k < kRowsPerGroup; ++k) {
-            if (!src[k] || !dst[k]) continue;
+            const int64_t si = GATHER ? ix[k] : first + k;
+            if (ix[k] >= 0) v[k] = __ldg(reinterpret_cast<const uint4 *>(src + si * sbytes) + q);
+        }
+#pragma unroll
+        for (int k = 0; k < kRowsPerGroup; ++k) {
+            const int64_t di = GATHER ? first + k : ix[k];
+            if (ix[k] >= 0) reinterpret_cast<uint4 *>(dst + di * dbytes)[q] = v[k];
+        }
+    }
+    if (sub == 0 && nvec * 16 < nbytes) {
+        const int64_t tail0 = nvec * 16;
+#pragma unroll
+        for (int k = 0; k < kRowsPerGroup; ++k) {
+            if (ix[k] < 0) continue;
+            const char *s = src + (GATHER ? ix[k] : first + k) * sbytes;
+            char *d = dst + (GATHER ? first + k : ix[k]) * dbytes;
             if (es == 4) {
                 for (int64_t b = tail0; b < nbytes; b += 4)
-                    *reinterpret_cast<uint32_t *>(dst[k] + b) = *reinterpret_cast<const uint32_t *>(src[k] + b);
+                    *reinterpret_cast<uint32_t *>(d + b) = *reinterpret_cast<const uint32_t *>(s + b);
             } else {
                 for (int64_t b = tail0; b < nbytes; b += 2)
-                    *reinterpret_cast<uint16_t *>(dst[k] + b) = *reinterpret_cast<const uint16_t *>(src[k] + b);
+                    *reinterpret_cast<uint16_t *>(d + b) = *reinterpret_cast<const uint16_t *>(s + b);
             }
         }
     }
 }
 
 template <int LPR>
-__global__ void __launch_bounds__(256) pull_kernel(const char *__restrict__ table, int64_t row_bytes_t, int64_t n_table,
+__global__ void __launch_bounds__(256, 3) pull_kernel(const char *__restrict__ table, int64_t row_bytes_t, int64_t n_table,
                                                    const int64_t *__restrict__ ids, int64_t n_ids,
                                                    char *__restrict__ H, int64_t row_bytes_h, int64_t row0,
                                                    int64_t nbytes, int es, int *err) {
@@ -57,24 +67,21 @@ __global__ void __launch_bounds__(256) pull_kernel(const char *__restrict__ tabl
     const int64_t i0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
     if (i0 >= n_ids) return;
-    const char *src[kRowsPerGroup];
-    char *dst[kRowsPerGroup];
+    int64_t ix[kRowsPerGroup];
 #pragma unroll
     for (int k = 0; k < kRowsPerGroup; ++k) {
-        src[k] = nullptr;
-        dst[k] = nullptr;
+        ix[k] = -1;
         const int64_t i = i0 + k;
         if (i < n_ids) {
             const int64_t id = __ldg(ids + i);
             if (id < 0 || id >= n_table) {
                 if (sub == 0) atomicOr(err, 1);
             } else {
-                src[k] = table + id * row_bytes_t;
-                dst[k] = H + (row0 + i) * row_bytes_h;
+                ix[k] = id;
             }
         }
     }
-    copy_rows<LPR>(src, dst, nbytes, es, sub);
+    copy_rows<LPR, true>(table, row_bytes_t, H, row_bytes_h, row0 + i0, ix, nbytes, es, sub);
 }
 
 // claim word = (generation << 2) | min(count, 2)
@@ -99,7 +106,7 @@ __global__ void push_claim_kernel(const int64_t *__restrict__ ids, int64_t n, in
 }
 
 template <int LPR>
-__global__ void __launch_bounds__(256) push_copy_kernel(const char *__restrict__ H, int64_t row_bytes_h,
+__global__ void __launch_bounds__(256, 3) push_copy_kernel(const char *__restrict__ H, int64_t row_bytes_h,
                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
                                                         const uint32_t *__restrict__ claim, uint32_t gen,
                                                         char *__restrict__ table, int64_t row_bytes_t, int64_t nbytes,
@@ -108,24 +115,21 @@ __global__ void __launch_bounds__(256) push_copy_kernel(const char *__restrict__
     const int64_t v0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
     if (v0 >= n) return;
-    const char *src[kRowsPerGroup];
-    char *dst[kRowsPerGroup];
+    int64_t ix[kRowsPerGroup];
 #pragma unroll
     for (int k = 0; k < kRowsPerGroup; ++k) {
-        src[k] = nullptr;
-        dst[k] = nullptr;
+        ix[k] = -1;
         const int64_t v = v0 + k;
         if (v >= n) continue;
-        src[k] = H + v * row_bytes_h;  // a local row: read whatever its id turns out to be
         const int64_t id = __ldg(ids + v);
         if (id < 0 || id >= n_table) continue;  // reported by the claim pass
         if (claim[id] != ((gen << 2) | 1u)) {
             if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
             continue;
         }
-        dst[k] = table + id * row_bytes_t;
+        ix[k] = id;
     }
-    copy_rows<LPR>(src, dst, nbytes, es, sub);
+    copy_rows<LPR, false>(H, row_bytes_h, table, row_bytes_t, v0, ix, nbytes, es, sub);
 }
 
 int lanes_per_row(int64_t nbytes) {

@@ -29,7 +29,8 @@ EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
     "gnn_layer_forward", "gnn_layer_backward", "gnn_softmax_ce", "gnn_get_error", "gnn_graph_sizes",
     "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_halo_push_quantized",
-    "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
+    "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv",
+    "gnn_layer_forward_narrow", "gnn_layer_backward_narrow", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc",
 )
 
@@ -67,6 +68,9 @@ def _lib():
         L.gnn_layer_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp, i64, i32,
                                          i32, vp]
         L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, vp]
+        L.gnn_layer_forward_narrow.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
+        L.gnn_layer_backward_narrow.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp,
+                                                i64, i32, vp]
         L.gnn_softmax_ce_partial.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp]
         L.gnn_halo_grad_send.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
         L.gnn_halo_grad_recv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
@@ -260,6 +264,31 @@ def halo_pull_quantized(g: Graph, codes: torch.Tensor, scale_zero: torch.Tensor,
     _check(_lib().gnn_halo_pull_quantized(ctypes.c_void_p(g.handle), _ptr(codes), codes.stride(0), _ptr(scale_zero),
                                           codes.shape[0], int(bits), _ptr(halo_ids), _ptr(H), ld_h, f, _dtype(H),
                                           ctypes.c_void_p(_stream())), "gnn_halo_pull_quantized")
+
+
+def layer_forward_narrow(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, T: torch.Tensor,
+                         H_out: torch.Tensor):
+    """T = H W (every row), H_out = act(A_block T): the GCN layer with the multiplication first."""
+    ld_h, f_in = _mat(H)
+    ld_t, _ = _mat(T)
+    ld_o, f_out = _mat(H_out)
+    assert W.dtype == torch.float32 and W.is_contiguous() and W.shape == (f_in, f_out)
+    _check(_lib().gnn_layer_forward_narrow(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f_in, _ptr(W), f_out, int(relu),
+                                           _ptr(T), ld_t, _ptr(H_out), ld_o, _dtype(H), ctypes.c_void_p(_stream())),
+           "gnn_layer_forward_narrow")
+
+
+def layer_backward_narrow(g: Graph, G: torch.Tensor, H_out: torch.Tensor, H: torch.Tensor, W: torch.Tensor,
+                          relu: bool, dW: torch.Tensor, P: torch.Tensor, dH: Optional[torch.Tensor] = None):
+    """P = A_block^T dY (every row), dW = H^T P, dH = P W^T (every row; skipped when dH is None)."""
+    ld_g, f_out = _mat(G)
+    ld_o, _ = _mat(H_out)
+    ld_h, f_in = _mat(H)
+    ld_p, _ = _mat(P)
+    ld_dh = _mat(dH)[0] if dH is not None else 0
+    _check(_lib().gnn_layer_backward_narrow(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(H),
+                                            ld_h, _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(P), ld_p, _ptr(dH),
+                                            ld_dh, _dtype(G), ctypes.c_void_p(_stream())), "gnn_layer_backward_narrow")
 
 
 def layer_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, Z: torch.Tensor, H_out: torch.Tensor):

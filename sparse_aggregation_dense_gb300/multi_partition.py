@@ -38,7 +38,7 @@ from .partition_model import PartitionModel, ld_for
 
 class MultiPartitionTrainer:
     def __init__(self, parts, widths: Sequence[int], agg: str, dtype: torch.dtype, n_table: int,
-                 mode: str = "sync", sync_every: int = 0, device="cuda"):
+                 mode: str = "sync", sync_every: int = 0, device="cuda", narrow: bool = False):
         assert mode in ("sync", "stale")
         self.parts = list(parts)
         self.widths = list(widths)
@@ -46,7 +46,8 @@ class MultiPartitionTrainer:
         self.mode, self.sync_every = mode, sync_every
         self.dtype = dtype
         self.n_table = n_table
-        self.models: List[PartitionModel] = [PartitionModel(p, widths, agg, dtype, device) for p in self.parts]
+        self.models: List[PartitionModel] = [PartitionModel(p, widths, agg, dtype, device, narrow=narrow)
+                                             for p in self.parts]
         self.n_rows = sum(m.n_local for m in self.models)
         dev = torch.device(device)
         # representation tables (current and, for the stale schedule, next) and gradient tables
@@ -108,7 +109,7 @@ class MultiPartitionTrainer:
             for m in ms:
                 if m.n_halo:
                     gnn.halo_pull(m.graph, self.tables[l], m.halo_ids, m.H[l])
-                gnn.layer_forward(m.graph, m.H[l], m.W[l], l < self.L - 1, m.Z[l], m.layer_out(l))
+                m.layer_forward(l)
             if l + 1 < self.L:
                 for m in ms:
                     gnn.halo_push(m.graph, m.layer_out(l), m.local_ids, self.tables[l + 1])
@@ -133,7 +134,7 @@ class MultiPartitionTrainer:
             for l in range(self.L):
                 if m.n_halo:
                     gnn.halo_pull(m.graph, self.tables[l], m.halo_ids, m.H[l])
-                gnn.layer_forward(m.graph, m.H[l], m.W[l], l < self.L - 1, m.Z[l], m.layer_out(l))
+                m.layer_forward(l)
                 if l + 1 < self.L:
                     gnn.halo_push(m.graph, m.layer_out(l), m.local_ids, self.tables_next[l + 1])
         self._loss()
@@ -150,12 +151,7 @@ class MultiPartitionTrainer:
         self.gtables, self.gtables_next = self.gtables_next, self.gtables
 
     def _backward_layer(self, m: PartitionModel, l: int):
-        if l > 0:
-            gnn.layer_backward(m.graph, m.grad_out(l), m.layer_out(l), m.Z[l], m.W[l], l < self.L - 1, m.dW[l],
-                               self.widths[l], dZ=m.dZ_view(l), dH=m.dH[l], want_halo_grad=True)
-        else:
-            gnn.layer_backward(m.graph, m.grad_out(l), m.layer_out(l), m.Z[l], m.W[l], l < self.L - 1, m.dW[l],
-                               self.widths[l])
+        m.layer_backward(l, want_halo_grad=True)
 
     def check_errors(self):
         for m in self.models:

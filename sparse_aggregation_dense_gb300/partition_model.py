@@ -43,7 +43,7 @@ class PartitionModel:
     """
 
     def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda",
-                 overlap: bool = False):
+                 overlap: bool = False, narrow: bool = False):
         self.widths = list(widths)
         # overlap: pulls and pushes run on a second stream, concurrently with the layers (DIGEST
         # system design, Fig. 1c: the table traffic is decoupled from the computation).  The rows a
@@ -70,7 +70,13 @@ class PartitionModel:
         # layer inputs H[l] (local + halo rows); the local rows of H[l+1] are layer l's output
         self.H = [padded(nT, widths[l], dtype, dev) for l in range(self.L)]
         self.out_last = padded(nL, widths[-1], dtype, dev)
-        self.Z = [padded(nL, self.Kp[l], dtype, dev) for l in range(self.L)]
+        # narrow layers (GCN, output narrower than input) multiply first: A (H W), so their aggregations run
+        # at the output width; they keep T = H W (all rows) instead of Z
+        self.narrow = [narrow and not sage and widths[l + 1] < widths[l] for l in range(self.L)]
+        self.Z = [None if self.narrow[l] else padded(nL, self.Kp[l], dtype, dev) for l in range(self.L)]
+        self.T = [padded(nT, widths[l + 1], dtype, dev) if self.narrow[l] else None for l in range(self.L)]
+        self.P = padded(nT, max([widths[l + 1] for l in range(self.L) if self.narrow[l]] + [1]), dtype, dev) \
+            if any(self.narrow) else None
         self.dZ = padded(nL, max(self.Kp[1:] + [1]), dtype, dev)
         self.dH = [None] + [padded(nT, widths[l], dtype, dev) for l in range(1, self.L)]
         self.G_last = padded(nL, widths[-1], dtype, dev)
@@ -104,7 +110,7 @@ class PartitionModel:
         for l in range(self.L):
             if self.n_halo:
                 gnn.halo_pull(self.graph, self.tables[l], self.halo_ids, self.H[l])
-            gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
+            self._layer_forward(l)
             if l + 1 < self.L:
                 gnn.halo_push(self.graph, self.layer_out(l), self.local_ids, self.tables[l + 1])
 
@@ -121,7 +127,7 @@ class PartitionModel:
                 pulled[l].record(self.side)
         for l in range(self.L):
             main.wait_event(pulled[l])
-            gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
+            self._layer_forward(l)
             if l + 1 < self.L:
                 done = torch.cuda.Event()
                 done.record(main)
@@ -132,19 +138,38 @@ class PartitionModel:
         pushed.record(self.side)
         main.wait_event(pushed)  # the epoch ends when its pushes have landed
 
+    def layer_forward(self, l: int):
+        """Forward of layer l from H[l] (pulled halo rows included) into its output."""
+        self._layer_forward(l)
+
+    def _layer_forward(self, l: int):
+        if self.narrow[l]:
+            gnn.layer_forward_narrow(self.graph, self.H[l], self.W[l], l < self.L - 1, self.T[l], self.layer_out(l))
+        else:
+            gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
+
     def loss_grad(self):
         gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)
 
     def backward(self, want_halo_grad: bool = True):
         for l in reversed(range(self.L)):
-            if l > 0:
-                gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
-                                   l < self.L - 1, self.dW[l], self.widths[l], dZ=self.dZ_view(l),
-                                   dH=self.dH[l] if want_halo_grad else self.dH[l][:self.n_local],
-                                   want_halo_grad=want_halo_grad)
-            else:
-                gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
-                                   l < self.L - 1, self.dW[l], self.widths[l])
+            self.layer_backward(l, want_halo_grad)
+
+    def layer_backward(self, l: int, want_halo_grad: bool = True):
+        """Backward of layer l: dW[l], and for l > 0 the gradient dH[l] of its input (halo rows too when
+        want_halo_grad; a narrow layer always writes them)."""
+        if self.narrow[l]:
+            P = self.P[:, :self.widths[l + 1]]
+            gnn.layer_backward_narrow(self.graph, self.grad_out(l), self.layer_out(l), self.H[l], self.W[l],
+                                      l < self.L - 1, self.dW[l], P, self.dH[l] if l > 0 else None)
+        elif l > 0:
+            gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
+                               l < self.L - 1, self.dW[l], self.widths[l], dZ=self.dZ_view(l),
+                               dH=self.dH[l] if want_halo_grad else self.dH[l][:self.n_local],
+                               want_halo_grad=want_halo_grad)
+        else:
+            gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
+                               l < self.L - 1, self.dW[l], self.widths[l])
 
     def step(self):
         self.forward()

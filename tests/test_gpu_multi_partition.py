@@ -49,11 +49,16 @@ def _trainer(parts, X, Ws, y, dtype, **kw):
     return t
 
 
-@pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-4), (torch.bfloat16, 2e-2)])
+# bf16 runs the layers in the textbook order, where its rounding points are the
+# oracle's (the multiplication-first order rounds H W instead of A H, which can
+# flip a ReLU decision near zero and move whole gradient rows: chained-layer
+# parity, not an exchange error); fp32 runs both orders
+@pytest.mark.parametrize("dtype,tol,narrow", [(torch.float32, 1e-4, True), (torch.float32, 1e-4, False),
+                                              (torch.bfloat16, 2e-2, False)])
 @pytest.mark.parametrize("P", [2, 3])
-def test_sync_epoch_equals_whole_graph(P, dtype, tol):
+def test_sync_epoch_equals_whole_graph(P, dtype, tol, narrow):
     A, parts, full, X, Ws, y = _setup(P, 10 + P, dtype)
-    t = _trainer(parts, X, Ws, y, dtype, mode="sync")
+    t = _trainer(parts, X, Ws, y, dtype, mode="sync", narrow=narrow)
     t.epoch()
     t.check_errors()
     tables = [X] + [np.zeros((N, f)) for f in WIDTHS[1:-1]]

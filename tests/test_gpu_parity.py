@@ -549,3 +549,46 @@ def test_overlapped_epoch_matches_sequential(case):
                        [t.float().cpu() for t in m.tables[1:]])
     for a, b in zip(*results):
         assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# narrow layers (multiplication first: A (H W)) against the textbook order
+# ---------------------------------------------------------------------------
+
+NARROW_CASES = [(n, "tiny", l) for n in ["er5k", "rmat131k", "powerlaw233k", "rmat16m"]
+                for l in range(TINY[n].layers) if TINY[n].widths[l + 1] < TINY[n].widths[l]]
+
+
+@pytest.mark.parametrize("case", NARROW_CASES, ids=lambda c: f"{c[0]}-{c[1]}-L{c[2]}")
+def test_narrow_layer_matches_oracle(case):
+    name, size, l = case
+    w, part, g = problem(name, size)
+    dt = w.dtype
+    tdt = torch_dtype(dt)
+    f_in, f_out = w.widths[l], w.widths[l + 1]
+    relu = l < w.layers - 1
+    nL, nT = part.n_local, part.n_total
+    H_h = gen_matrix(nT, f_in, dt, SEED, 500 + l)
+    W = synth.glorot(f_in, f_out, SEED, synth.STREAM_WEIGHT + l)
+    Wr = maybe_round(W.astype(np.float64), dt)
+    H = to_device(H_h, dt, f_in)
+    T = padded(nT, f_out, tdt, "cuda")
+    Hout = padded(nL, f_out, tdt, "cuda")
+    gnn.layer_forward_narrow(g, H, torch.from_numpy(W).cuda(), relu, T, Hout)
+    assert_ok(g)
+    Hw = widen(H_h, dt, f_in)
+    Zr, Hr = oracle.layer_forward(part, Hw, Wr, "gcn", relu)
+    close(to_host(Hout), Hr, TOL[dt], "H_out")
+    close(to_host(T), Hw @ Wr, TOL[dt], "T = H W")
+    # backward with the GPU's H_out on both sides (the same ReLU mask)
+    G_h = gen_matrix(nL, f_out, dt, SEED, 600 + l)
+    G = to_device(G_h, dt, f_out)
+    P = padded(nT, f_out, tdt, "cuda")
+    dH = padded(nT, f_in, tdt, "cuda")
+    dW = torch.zeros((f_in, f_out), dtype=torch.float32, device="cuda")
+    gnn.layer_backward_narrow(g, G, Hout, H, torch.from_numpy(W).cuda(), relu, dW, P, dH)
+    assert_ok(g)
+    dWr, _, dHr = oracle.layer_backward(part, oracle.transpose(part), widen(G_h, dt, f_out), to_host(Hout), Zr, Wr,
+                                        "gcn", relu, want_dh=True)
+    close(dW.cpu().numpy().astype(np.float64), dWr, TOL[dt], "dW")
+    close(to_host(dH), dHr, TOL[dt], "dH (local and halo rows)")
