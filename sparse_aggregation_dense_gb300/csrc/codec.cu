@@ -20,8 +20,11 @@
 // 16), code c in bits [c * b, c * b + b) little-endian, bytes past the last
 // code zero; (scale, zero point) at scale_zero[2 r], scale_zero[2 r + 1].
 //
-// One warp per row; lane l owns the 8 consecutive values 8 l + 256 j of the
-// row, so its codes of a 256-value chunk are one b-byte word.
+// One warp per row (the pull's grid of 16 blocks per SM loops over the rows);
+// lane l owns the 8 consecutive values 8 l + 256 j of the row, so its codes of
+// a 256-value chunk are one b-byte word.
+#include <algorithm>
+
 #include "gnn_internal.cuh"
 
 namespace gnn {
@@ -97,27 +100,13 @@ struct CodeWord<8> {
     using type = unsigned long long;
 };
 
-// Quantise pushed rows: row v of H goes to table row ids[v] if the claim pass
-// saw that id exactly once (else the row is skipped and the error word set).
+// quantise one row h into its codes and (scale, zero point); one warp
 template <typename T, int BITS>
-__global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H, int64_t ld_h,
-                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
-                                                         const uint32_t *__restrict__ claim, uint32_t gen,
-                                                         uint8_t *__restrict__ codes, int64_t ld_codes,
-                                                         float *__restrict__ scale_zero, int64_t f, uint64_t seed,
-                                                         int *err) {
+__device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id, uint8_t *__restrict__ crow,
+                                             int64_t ld_codes, float *__restrict__ sz, int64_t f, uint64_t seed,
+                                             int lane) {
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
-    const int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (v >= n) return;
-    const int64_t id = ids[v];
-    if (id < 0 || id >= n_table) return;  // reported by the claim pass
-    if (claim[id] != ((gen << 2) | 1u)) {
-        if (lane == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
-        return;
-    }
-    const T *h = H + v * ld_h;
     // min and max of the row
     float mn = INFINITY, mx = -INFINITY;
     for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
@@ -136,7 +125,6 @@ __global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)B);
-    uint8_t *crow = codes + id * ld_codes;
     const int64_t used = (f + 7) / 8 * BITS;  // code bytes of the row (whole 8-value words)
     for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
         float x[8];
@@ -164,8 +152,30 @@ __global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H
     // bytes past the codes are zero
     for (int64_t b = used + lane; b < ld_codes; b += 32) crow[b] = 0;
     if (lane == 0) {
-        scale_zero[2 * id] = s;
-        scale_zero[2 * id + 1] = mn;
+        sz[0] = s;
+        sz[1] = mn;
+    }
+}
+
+// Quantise pushed rows: row v of H goes to table row ids[v] if the claim pass
+// saw that id exactly once (else the row is skipped and the error word set).
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H, int64_t ld_h,
+                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
+                                                         const uint32_t *__restrict__ claim, uint32_t gen,
+                                                         uint8_t *__restrict__ codes, int64_t ld_codes,
+                                                         float *__restrict__ scale_zero, int64_t f, uint64_t seed,
+                                                         int *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n; v += nw) {
+        const int64_t id = ids[v];
+        if (id < 0 || id >= n_table) continue;  // reported by the claim pass
+        if (claim[id] != ((gen << 2) | 1u)) {
+            if (lane == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
+            continue;
+        }
+        quantize_row<T, BITS>(H + v * ld_h, id, codes + id * ld_codes, ld_codes, scale_zero + 2 * id, f, seed, lane);
     }
 }
 
@@ -177,26 +187,27 @@ __global__ void __launch_bounds__(256) codec_pull_kernel(const uint8_t *__restri
                                                          int64_t ld_h, int64_t row0, int64_t f, int *err) {
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (i >= n) return;
-    const int64_t id = ids[i];
-    if (id < 0 || id >= n_table) {
-        if (lane == 0) atomicOr(err, 1);
-        return;
-    }
-    const float s = __ldg(scale_zero + 2 * id), z = __ldg(scale_zero + 2 * id + 1);
-    const uint8_t *crow = codes + id * ld_codes;
-    T *out = H + (row0 + i) * ld_h;
-    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
-        const W word = __ldg(reinterpret_cast<const W *>(crow + c0 / 8 * BITS));
-        float y[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int q = (int)((word >> (k * BITS)) & (W)B);
-            y[k] = __fadd_rn(__fmul_rn((float)q, s), z);
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        const int64_t id = ids[i];
+        if (id < 0 || id >= n_table) {
+            if (lane == 0) atomicOr(err, 1);
+            continue;
         }
-        store8(out, c0, f, y);
+        const float s = __ldg(scale_zero + 2 * id), z = __ldg(scale_zero + 2 * id + 1);
+        const uint8_t *crow = codes + id * ld_codes;
+        T *out = H + (row0 + i) * ld_h;
+        for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+            const W word = __ldg(reinterpret_cast<const W *>(crow + c0 / 8 * BITS));
+            float y[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int q = (int)((word >> (k * BITS)) & (W)B);
+                y[k] = __fadd_rn(__fmul_rn((float)q, s), z);
+            }
+            store8(out, c0, f, y);
+        }
     }
 }
 
@@ -220,6 +231,8 @@ gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
     uint32_t gen = 0;
     gnn_status st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
     if (st != GNN_OK) return st;
+    // one warp per row: the quantisation is arithmetic-heavy and a bounded
+    // grid looping over the rows measured slower
     const unsigned blocks = (unsigned)ceil_div(n_rows * 32, 256);
     return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
         constexpr int BITS = decltype(Bc)::value;
@@ -240,7 +253,7 @@ gnn_status launch_codec_pull(const uint8_t *codes, int64_t ld_codes, const float
                              int bits, const int64_t *ids, int64_t n_ids, void *H, int64_t ld_h, int64_t row0,
                              int64_t f, gnn_dtype dt, int *err, cudaStream_t s) {
     if (n_ids == 0) return GNN_OK;
-    const unsigned blocks = (unsigned)ceil_div(n_ids * 32, 256);
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n_ids * 32, 256), (int64_t)num_sms() * 16);
     return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
         constexpr int BITS = decltype(Bc)::value;
         if (dt == GNN_BF16)

@@ -11,7 +11,10 @@
 // repeated id is reported and its rows skipped), so one send launch has no
 // conflicting updates; sends of several partitions are ordered on the stream,
 // so the sums are formed in a fixed order (no atomics, reproducible bits).
-// One warp per row, 4 columns per lane per step.
+// One warp per row (16 blocks per SM loop over the rows), 4 columns per lane
+// per step.
+#include <algorithm>
+
 #include "gnn_internal.cuh"
 
 namespace gnn {
@@ -47,23 +50,24 @@ __global__ void __launch_bounds__(256) grad_send_kernel(const T *__restrict__ dH
                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
                                                         const uint32_t *__restrict__ claim, uint32_t gen,
                                                         float *__restrict__ gt, int64_t ld_gt, int64_t f, int *err) {
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (i >= n) return;
-    const int64_t id = ids[i];
-    if (id < 0 || id >= n_table) return;  // reported by the claim pass
-    if (claim[id] != ((gen << 2) | 1u)) {
-        if (lane == 0) atomicOr(err, 1);  // repeated id: its rows are not sent
-        return;
-    }
-    const T *src = dH + (row0 + i) * ld_dh;
-    float *dst = gt + id * ld_gt;
-    for (int64_t c = (int64_t)lane * 4; c < f; c += 128) {
-        if (c + 4 <= f) {
-            const float4 a = load4v(dst + c), b = load4v(src + c);
-            store4v(dst + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
-        } else {
-            for (int64_t k = c; k < f; ++k) dst[k] += elem(src + k);
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        const int64_t id = ids[i];
+        if (id < 0 || id >= n_table) continue;  // reported by the claim pass
+        if (claim[id] != ((gen << 2) | 1u)) {
+            if (lane == 0) atomicOr(err, 1);  // repeated id: its rows are not sent
+            continue;
+        }
+        const T *src = dH + (row0 + i) * ld_dh;
+        float *dst = gt + id * ld_gt;
+        for (int64_t c = (int64_t)lane * 4; c < f; c += 128) {
+            if (c + 4 <= f) {
+                const float4 a = load4v(dst + c), b = load4v(src + c);
+                store4v(dst + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+            } else {
+                for (int64_t k = c; k < f; ++k) dst[k] += elem(src + k);
+            }
         }
     }
 }
@@ -72,22 +76,23 @@ template <typename T>
 __global__ void __launch_bounds__(256) grad_recv_kernel(const float *__restrict__ gt, int64_t ld_gt, int64_t n_table,
                                                         const int64_t *__restrict__ ids, int64_t n,
                                                         T *__restrict__ dH, int64_t ld_dh, int64_t f, int *err) {
-    const int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (v >= n) return;
-    const int64_t id = ids[v];
-    if (id < 0 || id >= n_table) {
-        if (lane == 0) atomicOr(err, 1);
-        return;
-    }
-    const float *src = gt + id * ld_gt;
-    T *dst = dH + v * ld_dh;
-    for (int64_t c = (int64_t)lane * 4; c < f; c += 128) {
-        if (c + 4 <= f) {
-            const float4 a = load4v(dst + c), b = load4v(src + c);
-            store4v(dst + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
-        } else {
-            for (int64_t k = c; k < f; ++k) set_elem(dst + k, elem(dst + k) + src[k]);
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n; v += nw) {
+        const int64_t id = ids[v];
+        if (id < 0 || id >= n_table) {
+            if (lane == 0) atomicOr(err, 1);
+            continue;
+        }
+        const float *src = gt + id * ld_gt;
+        T *dst = dH + v * ld_dh;
+        for (int64_t c = (int64_t)lane * 4; c < f; c += 128) {
+            if (c + 4 <= f) {
+                const float4 a = load4v(dst + c), b = load4v(src + c);
+                store4v(dst + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+            } else {
+                for (int64_t k = c; k < f; ++k) set_elem(dst + k, elem(dst + k) + src[k]);
+            }
         }
     }
 }
@@ -101,7 +106,7 @@ gnn_status launch_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t
     uint32_t gen = 0;
     gnn_status st = launch_push_claim(g, halo_ids, n, n_table, &gen, s);
     if (st != GNN_OK) return st;
-    const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n * 32, 256), (int64_t)num_sms() * 16);
     if (dt == GNN_BF16)
         { grad_send_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(dH), ld_dh,
                                                                  g->n_local, halo_ids, n, n_table, g->claim, gen,
@@ -118,7 +123,7 @@ gnn_status launch_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, in
                             cudaStream_t s) {
     const int64_t n = g->n_local;
     if (n == 0) return GNN_OK;
-    const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n * 32, 256), (int64_t)num_sms() * 16);
     if (dt == GNN_BF16)
         { grad_recv_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(gtable, ld_gt, n_table, local_ids, n,
                                                                  static_cast<__nv_bfloat16 *>(dH), ld_dh, f, g->err); GNN_LAUNCHED(1); }
