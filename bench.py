@@ -156,7 +156,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha1()
-    for name in ("aggregate.cu",):
+    for name in ("aggregate.cu", "setup.cu"):  # the kernel, and the entry order and tiers it streams
         h.update(open(os.path.join(ROOT, "sparse_aggregation_dense_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:12]
 

@@ -176,6 +176,7 @@ static void destroy_graph(gnn_graph *g) {
     cudaFree(g->colidx);
     cudaFree(g->rowptrT);
     cudaFree(g->colidxT);
+    cudaFree(g->colidxTa);
     cudaFree(g->permT);
     cudaFree(g->colw);
     cudaFree(g->wfwd);
@@ -260,6 +261,28 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     // transpose row length), backward columns (local rows) by their row length
     TRY(tag_tiers(g->colidx, nnz, g->rowptrT, nT, &g->fwd, s));
     TRY(tag_tiers(g->colidxT, nnz, g->rowptr, n_local, &g->bwd, s));
+    // each row's entries hottest tier first (stable), so the four rows of a
+    // gather mostly share one L2 policy; the block's own copy is reordered in
+    // place, the transpose gets a second copy (colidxT stays the stable
+    // transpose that gnn_graph_copy_transpose hands out)
+    if (nnz > 0 && (g->fwd.tagged || g->bwd.tagged)) {
+        int32_t *tc = nullptr;
+        float *tw = nullptr;
+        TRY_CUDA(cudaMallocAsync((void **)&tc, (size_t)nnz * sizeof(int32_t), s));
+        TRY_CUDA(cudaMallocAsync((void **)&tw, (size_t)nnz * sizeof(float), s));
+        if (g->fwd.tagged) {
+            TRY_CUDA(cudaMemcpyAsync(tc, g->colidx, (size_t)nnz * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+            TRY_CUDA(cudaMemcpyAsync(tw, g->wfwd, (size_t)nnz * sizeof(float), cudaMemcpyDeviceToDevice, s));
+            TRY(sort_rows_by_tier(g->rowptr, n_local, tc, tw, g->colidx, g->wfwd, s));
+        }
+        if (g->bwd.tagged) {
+            TRY_CUDA(cudaMalloc((void **)&g->colidxTa, (size_t)nnz * sizeof(int32_t)));
+            TRY_CUDA(cudaMemcpyAsync(tw, g->wbwd, (size_t)nnz * sizeof(float), cudaMemcpyDeviceToDevice, s));
+            TRY(sort_rows_by_tier(g->rowptrT, nT, g->colidxT, tw, g->colidxTa, g->wbwd, s));
+        }
+        TRY_CUDA(cudaFreeAsync(tc, s));
+        TRY_CUDA(cudaFreeAsync(tw, s));
+    }
     TRY_CUDA(cudaStreamSynchronize(s));
     TRY_CUDA(cudaGetLastError());
 #undef TRY
@@ -476,7 +499,7 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     AggParams p{};
     p.err = g->err;
     p.rowptr = g->rowptrT;
-    p.colidx = reinterpret_cast<const uint32_t *>(g->colidxT);
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidxTa ? g->colidxTa : g->colidxT);
     p.wts = g->wbwd;
     p.rowscale = sage ? nullptr : g->colw;
     p.n_rows = out_rows;
@@ -609,7 +632,7 @@ gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, 
         AggParams p{};
         p.err = g->err;
         p.rowptr = g->rowptrT;
-        p.colidx = reinterpret_cast<const uint32_t *>(g->colidxT);
+        p.colidx = reinterpret_cast<const uint32_t *>(g->colidxTa ? g->colidxTa : g->colidxT);
         p.wts = g->wbwd;
         p.rowscale = g->colw;
         p.n_rows = nT;

@@ -63,7 +63,11 @@ struct gnn_graph {
     int32_t *rowptrT = nullptr, *colidxT = nullptr, *permT = nullptr;
     // GCN: dinv over n_local + n_halo columns; GraphSAGE: inverse neighbour counts of local rows
     float *colw = nullptr;
-    // per-entry weights of the block (forward) and of its transpose (backward)
+    // the transpose's tagged column ids in the aggregation's order (each row
+    // hottest tier first); null when untagged, and colidxT is used instead
+    int32_t *colidxTa = nullptr;
+    // per-entry weights of the block (forward) and of its transpose (backward),
+    // in the aggregation's order
     float *wfwd = nullptr, *wbwd = nullptr;
     gnn::Schedule fwd, bwd;
     int *err = nullptr;  // device error word
@@ -120,6 +124,10 @@ gnn_status tag_tiers(int32_t *colidx, int64_t nnz, const int32_t *ptr, int64_t n
 int hot_tier_for(const Schedule &sc, int64_t row_bytes);
 // Copy column ids without their tier bits.
 gnn_status copy_untagged(const int32_t *src, int32_t *dst, int64_t n, uint32_t mask, cudaStream_t s);
+// every row's entries (tagged column ids and weights), out of place, in a
+// stable order by tier, hottest first
+gnn_status sort_rows_by_tier(const int32_t *rowptr, int64_t n_rows, const int32_t *col_in, const float *w_in,
+                             int32_t *col_out, float *w_out, cudaStream_t s);
 void free_schedule(Schedule *sc);
 
 // ---- kernels launched by the API ------------------------------------------

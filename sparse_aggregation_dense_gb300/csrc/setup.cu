@@ -6,6 +6,7 @@
 // Communication in Graph Neural Network Training", GNN section) prescribes for a
 // training algorithm that works on directed graphs; entries of a transpose row
 // are ordered by ascending source row, so every later pass is deterministic.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 
@@ -591,6 +592,69 @@ gnn_status tag_tiers(int32_t *colidx, int64_t nnz, const int32_t *ptr, int64_t n
     GNN_CUDA_TRY(cudaFreeAsync(tob, s));
     GNN_CUDA_TRY(cudaStreamSynchronize(s));
     sc->tagged = true;
+    return GNN_OK;
+}
+
+// Stable counting sort of every row's entries by tier, hottest first, the
+// weights moved with their entries.  With a row's hot entries next to each
+// other, the four rows of one gather mostly share a tier and so an L2 policy
+// (a gather takes one policy for its four rows).  One warp per row: a pass
+// counts the tiers, a scan over the 32 tiers gives each its first slot, a
+// second pass scatters (ranks inside a 32-entry window by match_any).
+__global__ void __launch_bounds__(256) tier_sort_rows_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows,
+                                                             const uint32_t *__restrict__ col_in,
+                                                             const float *__restrict__ w_in,
+                                                             uint32_t *__restrict__ col_out,
+                                                             float *__restrict__ w_out) {
+    __shared__ int32_t slot[8][kTiers];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int64_t nw = (int64_t)gridDim.x * 8;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + wib; r < n_rows; r += nw) {
+        const int32_t b = rowptr[r], e = rowptr[r + 1];
+        slot[wib][lane] = 0;
+        __syncwarp();
+        for (int32_t i = b; i < e; i += 32) {
+            const bool in = i + lane < e;
+            const uint32_t t = in ? col_in[i + lane] >> kTierShift : 0u;
+            const unsigned peers = __match_any_sync(0xffffffffu, in ? t : (uint32_t)kTiers);
+            if (in && lane == __ffs(peers) - 1) slot[wib][t] += __popc(peers);
+            __syncwarp();
+        }
+        // exclusive scan of the counts: lane t gets the first slot of tier t
+        const int32_t c = slot[wib][lane];
+        int32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncwarp();
+        slot[wib][lane] = b + incl - c;
+        __syncwarp();
+        for (int32_t i = b; i < e; i += 32) {
+            const bool in = i + lane < e;
+            const uint32_t col = in ? col_in[i + lane] : 0u;
+            const uint32_t t = col >> kTierShift;
+            const unsigned peers = __match_any_sync(0xffffffffu, in ? t : (uint32_t)kTiers);
+            if (in) {
+                const int32_t dst = slot[wib][t] + __popc(peers & ((1u << lane) - 1u));
+                col_out[dst] = col;
+                w_out[dst] = w_in[i + lane];
+            }
+            __syncwarp();
+            if (in && lane == __ffs(peers) - 1) slot[wib][t] += __popc(peers);
+            __syncwarp();
+        }
+    }
+}
+
+gnn_status sort_rows_by_tier(const int32_t *rowptr, int64_t n_rows, const int32_t *col_in, const float *w_in,
+                             int32_t *col_out, float *w_out, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n_rows, 8), (int64_t)num_sms() * 32);
+    { tier_sort_rows_kernel<<<blocks, 256, 0, s>>>(rowptr, n_rows, reinterpret_cast<const uint32_t *>(col_in), w_in,
+                                                    reinterpret_cast<uint32_t *>(col_out), w_out); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }
 
