@@ -31,8 +31,10 @@ namespace gnn {
 
 namespace {
 
-__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t k) {
-    uint64_t z = seed + k * 0x9E3779B97F4A7C15ull;
+// SplitMix64 (Steele, Lea and Flood): draw k of the stream `seed` is the
+// finaliser applied to seed + k * gamma
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+__device__ __forceinline__ uint64_t splitmix64_mix(uint64_t z) {
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
@@ -40,13 +42,13 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t k) {
 
 // the 8 values c0 .. c0 + 7 of a row as fp32 (exact widening); values at or
 // past f are not read and come back as 0
-__device__ __forceinline__ void load8(const float *row, int64_t c0, int64_t f, float (&v)[8]) {
+__device__ __forceinline__ void load8(const float *row, int c0, int f, float (&v)[8]) {
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (c0 < f) a = __ldg(reinterpret_cast<const float4 *>(row + c0));
     if (c0 + 4 < f) b = __ldg(reinterpret_cast<const float4 *>(row + c0 + 4));
     v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
 }
-__device__ __forceinline__ void load8(const __nv_bfloat16 *row, int64_t c0, int64_t f, float (&v)[8]) {
+__device__ __forceinline__ void load8(const __nv_bfloat16 *row, int c0, int f, float (&v)[8]) {
     uint4 q = make_uint4(0u, 0u, 0u, 0u);
     if (c0 < f) q = __ldg(reinterpret_cast<const uint4 *>(row + c0));
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -58,7 +60,7 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *row, int64_t c0, int6
 }
 
 // store the values of c0 .. c0 + 7 that lie below f
-__device__ __forceinline__ void store8(float *row, int64_t c0, int64_t f, const float (&v)[8]) {
+__device__ __forceinline__ void store8(float *row, int c0, int f, const float (&v)[8]) {
     if (c0 + 8 <= f) {
         reinterpret_cast<float4 *>(row + c0)[0] = make_float4(v[0], v[1], v[2], v[3]);
         reinterpret_cast<float4 *>(row + c0)[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -66,7 +68,7 @@ __device__ __forceinline__ void store8(float *row, int64_t c0, int64_t f, const 
         for (int k = 0; k < 8 && c0 + k < f; ++k) row[c0 + k] = v[k];
     }
 }
-__device__ __forceinline__ void store8(__nv_bfloat16 *row, int64_t c0, int64_t f, const float (&v)[8]) {
+__device__ __forceinline__ void store8(__nv_bfloat16 *row, int c0, int f, const float (&v)[8]) {
     if (c0 + 8 <= f) {
         uint32_t w[4];
 #pragma unroll
@@ -100,16 +102,46 @@ struct CodeWord<8> {
     using type = unsigned long long;
 };
 
+// RN(a / s) for a >= 0, s > 0, given r = RN(1 / s) and that s lies in
+// [2^-64, 2^64) (`fast`).  A reciprocal-based candidate with one correction
+// step (Markstein: q0 = RN(a r), q = RN(q0 + r RN(a - q0 s))) is accepted
+// only when one more fma proves it: the remainder a - q s (exact here, or
+// rounded by at most 2^-24 of itself) must lie inside s times the half-gap
+// to q's neighbour on that side (ulp(q) / 2; ulp(q) / 4 below a power of
+// two), shrunk by 2^-22 to absorb that rounding.  Everything the test does
+// not settle (near-ties, out-of-range operands) takes the IEEE division, so
+// the result is the correctly rounded quotient in every case.
+__device__ __forceinline__ float div_rn(float a, float s, float r, bool fast) {
+    const uint32_t ab = __float_as_uint(a);
+    if (fast && ab >= 0x1f800000u && ab < 0x5f800000u) {  // a in [2^-64, 2^64)
+        const float q0 = __fmul_rn(a, r);
+        const float q = __fmaf_rn(__fmaf_rn(-q0, s, a), r, q0);
+        const uint32_t qb = __float_as_uint(q);
+        const uint32_t eq = qb >> 23;  // biased exponent of q (q >= 0)
+        if (eq >= 26u && eq <= 254u) {
+            const float rem = __fmaf_rn(-q, s, a);
+            float h = __fmul_rn(__fmul_rn(__uint_as_float((eq - 24u) << 23), s),  // 2^(E(q) - 24) s
+                                __uint_as_float(0x3f7ffffcu));                      // x (1 - 2^-22)
+            if ((qb & 0x7fffffu) == 0u && rem < 0.f) h = __fmul_rn(h, 0.5f);
+            if (fabsf(rem) < h) return q;
+        }
+    } else if (fast && ab == 0u) {
+        return 0.f;
+    }
+    return __fdiv_rn(a, s);
+}
+
 // quantise one row h into its codes and (scale, zero point); one warp
 template <typename T, int BITS>
 __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id, uint8_t *__restrict__ crow,
-                                             int64_t ld_codes, float *__restrict__ sz, int64_t f, uint64_t seed,
+                                             int64_t ld_codes, float *__restrict__ sz, int64_t f64, uint64_t seed,
                                              int lane) {
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
+    const int f = (int)f64;  // a row's width fits 32 bits
     // min and max of the row
     float mn = INFINITY, mx = -INFINITY;
-    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+    for (int c0 = lane * 8; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);
 #pragma unroll
@@ -125,27 +157,34 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)B);
-    const int64_t used = (f + 7) / 8 * BITS;  // code bytes of the row (whole 8-value words)
-    for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+    const uint32_t sb = __float_as_uint(s);
+    const bool fast = sb >= 0x1f800000u && sb < 0x5f800000u;  // s in [2^-64, 2^64)
+    const float r = fast ? __frcp_rn(s) : 0.f;
+    const int used = (f + 7) / 8 * BITS;  // code bytes of the row (whole 8-value words)
+    // value pair c / 2 of the row takes draw (id << 15) + c / 2 + 1
+    const uint64_t z_row = seed + (((uint64_t)id << 15) + 1u) * kGamma;
+    for (int c0 = lane * 8; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);
         W word = 0;
         if (s > 0.f) {
+            const uint64_t z0 = z_row + (uint64_t)(c0 >> 1) * kGamma;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t c = c0 + 2 * j;
-                const uint64_t z = splitmix64(seed, ((uint64_t)id << 15) + (uint64_t)(c >> 1) + 1u);
+                const uint64_t z = splitmix64_mix(z0 + (uint64_t)j * kGamma);
                 const float u[2] = {(float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f),
                                     (float)(uint32_t)((z >> 16) & 0xFFFFFFu) * (1.0f / 16777216.0f)};
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    if (c + e >= f) continue;
-                    const float t = __fdiv_rn(__fsub_rn(x[2 * j + e], mn), s);
+                    const float t = div_rn(__fsub_rn(x[2 * j + e], mn), s, r, fast);
                     int q = (int)floorf(__fadd_rn(t, u[e]));
                     q = q < 0 ? 0 : (q > B ? B : q);
                     word |= (W)q << ((2 * j + e) * BITS);
                 }
             }
+            // codes of the values past f (computed from zeros) are cleared
+            const int valid = f - c0;
+            if (valid < 8) word &= (W)(((W)1 << (valid * BITS)) - 1);
         }
         *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = word;
     }
@@ -198,7 +237,7 @@ __global__ void __launch_bounds__(256) codec_pull_kernel(const uint8_t *__restri
         const float s = __ldg(scale_zero + 2 * id), z = __ldg(scale_zero + 2 * id + 1);
         const uint8_t *crow = codes + id * ld_codes;
         T *out = H + (row0 + i) * ld_h;
-        for (int64_t c0 = (int64_t)lane * 8; c0 < f; c0 += 256) {
+        for (int c0 = lane * 8; c0 < (int)f; c0 += 256) {
             const W word = __ldg(reinterpret_cast<const W *>(crow + c0 / 8 * BITS));
             float y[8];
 #pragma unroll
@@ -206,7 +245,7 @@ __global__ void __launch_bounds__(256) codec_pull_kernel(const uint8_t *__restri
                 const int q = (int)((word >> (k * BITS)) & (W)B);
                 y[k] = __fadd_rn(__fmul_rn((float)q, s), z);
             }
-            store8(out, c0, f, y);
+            store8(out, c0, (int)f, y);
         }
     }
 }

@@ -72,13 +72,14 @@ __device__ __forceinline__ uint4 pack_vec(const float (&v)[8]) {
 // with 16-byte stores (element stores only for the vector that straddles C,
 // so G's padding is left alone).
 template <typename T, int VPL, int RPW>
-__global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
+__global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C64,
                                                            const int32_t *__restrict__ labels, T *__restrict__ G,
                                                            int64_t ld_g, float *__restrict__ row_loss, float inv_n) {
     constexpr int EPV = 16 / (int)sizeof(T);
     const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW;
     const int lane = threadIdx.x & 31;
     if (i0 >= n) return;
+    const int C = (int)C64;  // at most 32 * VPL * EPV classes
     float v[RPW][VPL][EPV];
     int32_t yl[RPW];
 #pragma unroll
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
         yl[r] = i < n ? labels[i] : -1;
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
-            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            const int c0 = (lane + 32 * q) * EPV;
             if (i < n && c0 < C) {
                 unpack_vec(__ldcs(reinterpret_cast<const uint4 *>(X + i * ld + c0)), v[r][q]);
             } else {
@@ -103,10 +104,10 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
         float mx = -INFINITY;
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
-            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            const int left = C - (lane + 32 * q) * EPV;  // classes of this vector inside the row
 #pragma unroll
             for (int k = 0; k < EPV; ++k) {
-                if (c0 + k >= C) v[r][q][k] = -INFINITY;
+                if (k >= left) v[r][q][k] = -INFINITY;
                 mx = fmaxf(mx, v[r][q][k]);
             }
         }
@@ -116,11 +117,11 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
         const int32_t y = yl[r];
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
-            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            const int yk = y - (lane + 32 * q) * EPV;  // the label's slot in this vector, if any
 #pragma unroll
             for (int k = 0; k < EPV; ++k) {
-                if (c0 + k == y) xy = v[r][q][k];
-                v[r][q][k] = c0 + k < C ? expf(v[r][q][k] - mx) : 0.f;
+                if (k == yk) xy = v[r][q][k];
+                v[r][q][k] = __expf(v[r][q][k] - mx);  // exp(-inf) = 0 past the row's end
                 se += v[r][q][k];
             }
         }
@@ -133,11 +134,12 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
         T *gr = G + i * ld_g;
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
-            const int64_t c0 = (int64_t)(lane + 32 * q) * EPV;
+            const int c0 = (lane + 32 * q) * EPV;
             if (c0 >= C) continue;
+            const int yk = y - c0;
             float o[EPV];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) o[k] = (v[r][q][k] * inv_se - (c0 + k == y ? 1.f : 0.f)) * inv_n;
+            for (int k = 0; k < EPV; ++k) o[k] = (v[r][q][k] * inv_se - (k == yk ? 1.f : 0.f)) * inv_n;
             if (c0 + EPV <= C) {
                 __stcs(reinterpret_cast<uint4 *>(gr + c0), pack_vec(o));
             } else {

@@ -56,6 +56,55 @@ def test_push_quantized_matches_oracle(name, bits):
     assert np.all(got_c[other] == 0xAB) and np.all(got_sz[other] == -7.0)
 
 
+def _special_rows(n, f, rng):
+    """Rows that reach every branch of the quantiser's division: magnitudes
+    far below and above the reciprocal test's range, integer rows (exact
+    quotients), rows whose quotients are powers of two, constant rows (zero
+    scale), two-valued rows and numerators just above zero."""
+    H = np.empty((n, f), np.float32)
+    for i in range(n):
+        kind = i % 8
+        x = rng.standard_normal(f)
+        if kind == 0:
+            x = x * 2.0 ** -70
+        elif kind == 1:
+            x = x * 2.0 ** 70
+        elif kind == 2:
+            x = x * 2.0 ** -58
+        elif kind == 3:
+            x = rng.integers(0, 256, f).astype(np.float64)
+        elif kind == 4:
+            x = 2.0 ** rng.integers(-3, 9, f)
+            x[0] = 0.0
+        elif kind == 5:
+            x = np.full(f, 1.5)
+        elif kind == 6:
+            x = np.where(rng.random(f) < 0.5, -3.0, 5.0)
+        else:  # values a hair above the minimum: tiny numerators
+            x = np.abs(x)
+            x[:3] = [0.0, 2.0 ** -70, 2.0 ** -64]
+        H[i] = x.astype(np.float32)
+    return H
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_push_quantized_special_magnitudes(bits):
+    w, part, g = problem("er5k", "tiny")
+    f = w.widths[1]
+    Hv = _special_rows(part.n_local, f, np.random.default_rng(bits))
+    H = padded(part.n_local, f, torch.float32, "cuda")
+    H.copy_(torch.from_numpy(Hv).cuda())
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.zeros((part.n_table, ldc), dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((part.n_table, 2), dtype=torch.float32, device="cuda")
+    seed = 77 + bits
+    gnn.halo_push_quantized(g, H, torch.from_numpy(part.local_ids).cuda(), codes, sz, bits, seed)
+    assert_ok(g)
+    ref_c, ref_sz = oracle.quantize_rows(Hv, part.local_ids, bits, seed, ldc)
+    np.testing.assert_array_equal(codes.cpu().numpy()[part.local_ids], ref_c)
+    np.testing.assert_array_equal(sz.cpu().numpy()[part.local_ids].view(np.uint32), ref_sz.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["er5k", "rmat16m", "powerlaw233k"])
 @pytest.mark.parametrize("bits", [1, 2, 4, 8])
 def test_pull_quantized_matches_oracle(name, bits):
