@@ -312,6 +312,24 @@ def oracle_sample(part, w, target_s: float, seed: int, batch_rows: int = 4096, m
     return ef, secs, desc
 
 
+def cpu_baseline_entry(part, w, seconds: float):
+    """The oracle on all host cores (about `seconds` of work) and, on a quarter of
+    that, on one thread."""
+    import oracle
+
+    cef, csec, desc = oracle_sample(part, w, seconds, SEED)
+    cpu = {"value": cef / csec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+           "seconds": round(csec, 2)}
+    n_all = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        sef, ssec, sdesc = oracle_sample(part, w, seconds / 4, SEED + 5, max_batches=16)
+    finally:
+        oracle.set_num_threads(n_all)
+    cpu["single_thread"] = {"value": sef / ssec, "unit": UNIT, "seconds": round(ssec, 2), "sample": sdesc}
+    return cpu
+
+
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
@@ -529,11 +547,7 @@ def run_ours(args, rank, world, local_rank):
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cef, csec, desc = oracle_sample(part, w, args.cpu_seconds, SEED)
-        import oracle
-
-        cpu = {"value": cef / csec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
-               "seconds": round(csec, 2)}
+        cpu = cpu_baseline_entry(part, w, args.cpu_seconds)
     line = {
         "metric": METRIC,
         "value": value,

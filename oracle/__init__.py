@@ -86,6 +86,8 @@ def _L():
         L.oracle_codec_dequantize.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        L.oracle_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -104,6 +106,11 @@ def _i64(a) -> Optional[np.ndarray]:
 
 def num_threads() -> int:
     return int(_L().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads of the oracle's parallel loops from now on (n > 0)."""
+    _L().oracle_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------------

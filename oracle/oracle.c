@@ -420,6 +420,15 @@ void oracle_codec_dequantize(const uint8_t *codes, int64_t ld_codes, const float
     }
 }
 
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);
