@@ -621,9 +621,21 @@ __global__ void __launch_bounds__(WPC * 32)
                         rend = __shfl_sync(0xffffffffu, rwin, r - wbase);
                     }
                     const int run = rend - pos < cnt - j ? rend - pos : cnt - j;
+                    const uint8_t *rp = sr + j * BOX;
+                    const unsigned long long *wp = ws + j;
+                    if constexpr (VPT <= 2) {
+                        // short rows: the run two entries at a time, then the odd one
+                        int k = run;
 #pragma unroll 1
-                    for (int k = 0; k < run; ++k)
-                        accumulate_entry<T, VW, VPT, BE>(acc, sr + (j + k) * BOX, ws[j + k]);
+                        for (; k >= 2; k -= 2, rp += 2 * BOX, wp += 2) {
+                            accumulate_entry<T, VW, VPT, BE>(acc, rp, wp[0]);
+                            accumulate_entry<T, VW, VPT, BE>(acc, rp + BOX, wp[1]);
+                        }
+                        if (k) accumulate_entry<T, VW, VPT, BE>(acc, rp, wp[0]);
+                    } else {
+#pragma unroll 1
+                        for (int k = 0; k < run; ++k) accumulate_entry<T, VW, VPT, BE>(acc, rp + k * BOX, wp[k]);
+                    }
                     j += run;
                     pos += run;
                 }
