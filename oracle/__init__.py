@@ -12,11 +12,13 @@ functions and composes them in the order the pages give:
   Z  = A_block H            aggregation (CAGNET page, GNN section; Sylvie Alg. 1)
   H' = sigma(Z W)           update      (CAGNET page, GNN section)
   push local rows to the table          (DIGEST page, Fig. 1c)
-  backward by the chain rule            (CAGNET page: "same computational
-                                         primitives"; derivation not in the text)
+  backward by the chain rule            (CAGNET page, GNN section: the backward
+                                         reuses the forward's SpMM and GEMM;
+                                         the derivation is not in the text)
 
-Parity status of each function is recorded in the design doc; every function here is
-pinned by a ``-m "not gpu"`` test in ``tests/test_oracle_pins.py``.
+Every function here is pinned by a ``-m "not gpu"`` test against facts fixed
+outside the oracle (``tests/test_oracle_pins.py``, ``tests/test_codec_pins.py``);
+none is unpinned.
 """
 from __future__ import annotations
 
