@@ -81,8 +81,15 @@ typedef enum {
  *           for GraphSAGE, whose mean counts the entries u != v of row v.)
  * The graph copies the CSR, validates it on the device, computes the
  * normalisation, builds the transpose (entries of a transpose row ordered by
- * ascending source row) and the load-balance schedules.  Synchronous: returns
- * after the stream's work is done.  Errors: GNN_EINVAL (sizes, NULL),
+ * ascending source row) and the load-balance schedules.  For the aggregation
+ * it also keeps, for both directions, each row's entries ordered by how often
+ * their column is gathered (most first), so the order in which a row's terms
+ * are summed is the library's, not the caller's; the exported transpose
+ * (gnn_graph_copy_transpose) is the stable one above.  Device memory held:
+ * about 24 bytes per entry and 12 bytes per vertex, plus the schedules and a
+ * workspace that later calls grow as they need; up to 16 bytes per entry more
+ * while the transpose is built.  Synchronous: returns after the stream's work
+ * is done.  Errors: GNN_EINVAL (sizes, NULL),
  * GNN_EINDEX (CSR fails validation), GNN_ENOMEM, GNN_ECUDA.  On error *out is
  * set to NULL. */
 gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, int64_t n_halo,
