@@ -98,6 +98,26 @@ def _check(status: int, what: str):
         raise GnnError(status, what)
 
 
+def _need(cond: bool, what: str, why: str):
+    """Host-side check of what the C ABI cannot see (buffer rows, widths and
+    dtypes against the graph): a failure is reported like the library's own
+    GNN_EINVAL, before any device work is issued."""
+    if not cond:
+        raise GnnError(GNN_EINVAL, f"{what} ({why})")
+
+
+def _rows(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.shape[0])
+
+
+def _width(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.shape[1])
+
+
+def _numel(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.numel())
+
+
 def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
@@ -129,6 +149,22 @@ def agg_code(agg: str) -> int:
     return {"gcn": GNN_AGG_GCN_SYM, "sage": GNN_AGG_SAGE_MEAN}[agg]
 
 
+def _k(g, f_in: int) -> int:
+    """Rows of W: the update's input width (twice f_in for the GraphSAGE concat)."""
+    return 2 * f_in if g.agg == "sage" else f_in
+
+
+def _z_width(g, f_in: int, dtype: torch.dtype) -> int:
+    """Columns the aggregation writes: f_in, or both GraphSAGE halves (the mean
+    starting at its 16-byte aligned offset)."""
+    return 2 * sage_half_offset(f_in, dtype) if g.agg == "sage" else f_in
+
+
+def _weights(what: str, W: torch.Tensor, K: int, f_out: int):
+    _need(W.dtype == torch.float32 and W.is_contiguous() and tuple(W.shape) == (K, f_out), what,
+          f"weights must be a contiguous float32 ({K} x {f_out}) matrix")
+
+
 class Graph:
     """Owner of a ``gnn_graph*``; freed by :func:`graph_destroy` or on collection."""
 
@@ -151,10 +187,12 @@ class Graph:
 
 def graph_create(rowptr: torch.Tensor, colidx: torch.Tensor, n_local: int, n_halo: int,
                  deg: Optional[torch.Tensor] = None, agg: str = "gcn") -> Graph:
-    assert rowptr.dtype == torch.int32 and colidx.dtype == torch.int32
-    assert rowptr.numel() == n_local + 1
+    what = "gnn_graph_create"
+    _need(rowptr.dtype == torch.int32 and colidx.dtype == torch.int32, what, "rowptr and colidx must be int32")
+    _need(rowptr.numel() == n_local + 1, what, "rowptr must hold n_local + 1 entries")
     if deg is not None:
-        assert deg.dtype == torch.float32 and deg.numel() == n_local + n_halo
+        _need(deg.dtype == torch.float32 and deg.numel() == n_local + n_halo, what,
+              "deg must be float32 with n_local + n_halo entries")
     out = ctypes.c_void_p()
     nnz = colidx.numel()
     _check(_lib().gnn_graph_create(_ptr(rowptr), _ptr(colidx) if nnz else None, n_local, n_halo, nnz, _ptr(deg),
@@ -204,6 +242,10 @@ def aggregate_forward_noalloc(g: Graph, H: torch.Tensor, Z: torch.Tensor):
     """Z of layer_forward for H, computed without any device allocation."""
     ld_h, f = _mat(H)
     ld_z, _ = _mat(Z)
+    what = "gnn_aggregate_forward_noalloc"
+    _need(H.dtype == Z.dtype, what, "H and Z must share a dtype")
+    _need(_rows(H) >= g.n_total and _rows(Z) >= g.n_local, what, "H needs n_local + n_halo rows, Z n_local rows")
+    _need(_width(Z) >= _z_width(g, f, H.dtype), what, "Z is narrower than the aggregation output")
     _check(_lib().gnn_aggregate_forward_noalloc(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(Z), ld_z,
                                                 _dtype(H), ctypes.c_void_p(_stream())),
            "gnn_aggregate_forward_noalloc")
@@ -222,7 +264,11 @@ def halo_pull(g: Graph, table: torch.Tensor, halo_ids: torch.Tensor, H: torch.Te
     """H[n_local + i] = table[halo_ids[i]] over the columns of H's view."""
     ld_t, _ = _mat(table)
     ld_h, f = _mat(H)
-    assert halo_ids.dtype == torch.int64 and table.dtype == H.dtype
+    what = "gnn_halo_pull"
+    _need(halo_ids.dtype == torch.int64 and table.dtype == H.dtype, what, "int64 ids; table and H share a dtype")
+    _need(_numel(halo_ids) >= g.n_halo and _rows(H) >= g.n_total, what,
+          "n_halo ids and n_local + n_halo rows of H")
+    _need(_width(table) >= f, what, "table rows narrower than H's view")
     _check(_lib().gnn_halo_pull(ctypes.c_void_p(g.handle), _ptr(table), ld_t, table.shape[0], _ptr(halo_ids),
                                 _ptr(H), ld_h, f, _dtype(H), ctypes.c_void_p(_stream())), "gnn_halo_pull")
 
@@ -231,7 +277,10 @@ def halo_push(g: Graph, H: torch.Tensor, local_ids: torch.Tensor, table: torch.T
     """table[local_ids[v]] = H[v] over the columns of H's view (v < n_local)."""
     ld_t, _ = _mat(table)
     ld_h, f = _mat(H)
-    assert local_ids.dtype == torch.int64 and table.dtype == H.dtype
+    what = "gnn_halo_push"
+    _need(local_ids.dtype == torch.int64 and table.dtype == H.dtype, what, "int64 ids; table and H share a dtype")
+    _need(_numel(local_ids) >= g.n_local and _rows(H) >= g.n_local, what, "n_local ids and n_local rows of H")
+    _need(_width(table) >= f, what, "table rows narrower than H's view")
     _check(_lib().gnn_halo_push(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(local_ids), _ptr(table), ld_t,
                                 table.shape[0], _dtype(H), ctypes.c_void_p(_stream())), "gnn_halo_push")
 
@@ -241,14 +290,26 @@ def codec_row_bytes(f: int, bits: int) -> int:
     return (f * bits + 127) // 128 * 16
 
 
+def _codec_args(what: str, codes: torch.Tensor, scale_zero: torch.Tensor, ids: torch.Tensor, f: int, bits: int):
+    _need(ids.dtype == torch.int64 and codes.dtype == torch.uint8 and scale_zero.dtype == torch.float32, what,
+          "int64 ids, uint8 codes, float32 scale / zero point")
+    _need(codes.dim() == 2 and codes.stride(1) == 1 and scale_zero.is_contiguous(), what,
+          "codes with contiguous rows, contiguous scale / zero point")
+    _need(scale_zero.dim() == 2 and scale_zero.shape[1] == 2 and scale_zero.shape[0] >= codes.shape[0], what,
+          "scale_zero must be (n_table x 2)")
+    if bits in (1, 2, 4, 8):  # other widths are the library's to reject
+        _need(codes.shape[1] >= codec_row_bytes(f, bits), what, "code rows shorter than one packed row")
+
+
 def halo_push_quantized(g: Graph, H: torch.Tensor, local_ids: torch.Tensor, codes: torch.Tensor,
                         scale_zero: torch.Tensor, bits: int, seed: int):
     """Quantise the local rows of H's view (b-bit stochastic rounding, per-row scale and zero point) into
     codes[local_ids[v]] and scale_zero[local_ids[v]] (codes: uint8 n_table x ld_codes, scale_zero: float32
     n_table x 2)."""
     ld_h, f = _mat(H)
-    assert local_ids.dtype == torch.int64 and codes.dtype == torch.uint8 and scale_zero.dtype == torch.float32
-    assert codes.dim() == 2 and codes.stride(1) == 1 and scale_zero.is_contiguous()
+    what = "gnn_halo_push_quantized"
+    _codec_args(what, codes, scale_zero, local_ids, f, bits)
+    _need(_numel(local_ids) >= g.n_local and _rows(H) >= g.n_local, what, "n_local ids and n_local rows of H")
     _check(_lib().gnn_halo_push_quantized(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(local_ids), _ptr(codes),
                                           codes.stride(0), _ptr(scale_zero), codes.shape[0], int(bits),
                                           ctypes.c_uint64(seed & (2**64 - 1)), _dtype(H), ctypes.c_void_p(_stream())),
@@ -259,8 +320,9 @@ def halo_pull_quantized(g: Graph, codes: torch.Tensor, scale_zero: torch.Tensor,
                         H: torch.Tensor):
     """H[n_local + i] = dequantised codes[halo_ids[i]] over the columns of H's view."""
     ld_h, f = _mat(H)
-    assert halo_ids.dtype == torch.int64 and codes.dtype == torch.uint8 and scale_zero.dtype == torch.float32
-    assert codes.dim() == 2 and codes.stride(1) == 1 and scale_zero.is_contiguous()
+    what = "gnn_halo_pull_quantized"
+    _codec_args(what, codes, scale_zero, halo_ids, f, bits)
+    _need(_numel(halo_ids) >= g.n_halo and _rows(H) >= g.n_total, what, "n_halo ids and n_local + n_halo rows of H")
     _check(_lib().gnn_halo_pull_quantized(ctypes.c_void_p(g.handle), _ptr(codes), codes.stride(0), _ptr(scale_zero),
                                           codes.shape[0], int(bits), _ptr(halo_ids), _ptr(H), ld_h, f, _dtype(H),
                                           ctypes.c_void_p(_stream())), "gnn_halo_pull_quantized")
@@ -272,7 +334,12 @@ def layer_forward_narrow(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool,
     ld_h, f_in = _mat(H)
     ld_t, _ = _mat(T)
     ld_o, f_out = _mat(H_out)
-    assert W.dtype == torch.float32 and W.is_contiguous() and W.shape == (f_in, f_out)
+    what = "gnn_layer_forward_narrow"
+    _weights(what, W, f_in, f_out)
+    _need(H.dtype == T.dtype == H_out.dtype, what, "H, T and H_out share a dtype")
+    _need(_rows(H) >= g.n_total and _rows(T) >= g.n_total and _rows(H_out) >= g.n_local, what,
+          "H and T need n_local + n_halo rows, H_out n_local rows")
+    _need(_width(T) >= f_out, what, "T narrower than H_out")
     _check(_lib().gnn_layer_forward_narrow(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f_in, _ptr(W), f_out, int(relu),
                                            _ptr(T), ld_t, _ptr(H_out), ld_o, _dtype(H), ctypes.c_void_p(_stream())),
            "gnn_layer_forward_narrow")
@@ -286,6 +353,15 @@ def layer_backward_narrow(g: Graph, G: torch.Tensor, H_out: torch.Tensor, H: tor
     ld_h, f_in = _mat(H)
     ld_p, _ = _mat(P)
     ld_dh = _mat(dH)[0] if dH is not None else 0
+    what = "gnn_layer_backward_narrow"
+    _weights(what, W, f_in, f_out)
+    _weights(what, dW, f_in, f_out)
+    _need(all(t is None or t.dtype == G.dtype for t in (H_out, H, P, dH)), what, "activations share one dtype")
+    _need(_rows(G) >= g.n_local and _rows(H_out) >= g.n_local, what, "G and H_out need n_local rows")
+    _need(_rows(H) >= g.n_total and _rows(P) >= g.n_total and _width(P) >= f_out, what,
+          "H and P need n_local + n_halo rows, P f_out columns")
+    _need(dH is None or (_rows(dH) >= g.n_total and _width(dH) >= f_in), what,
+          "dH needs n_local + n_halo rows of f_in columns")
     _check(_lib().gnn_layer_backward_narrow(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(H),
                                             ld_h, _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(P), ld_p, _ptr(dH),
                                             ld_dh, _dtype(G), ctypes.c_void_p(_stream())), "gnn_layer_backward_narrow")
@@ -296,7 +372,12 @@ def layer_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, Z: tor
     ld_h, f_in = _mat(H)
     ld_z, _ = _mat(Z)
     ld_o, f_out = _mat(H_out)
-    assert W.dtype == torch.float32 and W.is_contiguous() and W.shape[1] == f_out
+    what = "gnn_layer_forward"
+    _weights(what, W, _k(g, f_in), f_out)
+    _need(H.dtype == Z.dtype == H_out.dtype, what, "H, Z and H_out share a dtype")
+    _need(_rows(H) >= g.n_total and _rows(Z) >= g.n_local and _rows(H_out) >= g.n_local, what,
+          "H needs n_local + n_halo rows, Z and H_out n_local rows")
+    _need(_width(Z) >= _z_width(g, f_in, H.dtype), what, "Z is narrower than the aggregation output")
     _check(_lib().gnn_layer_forward(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f_in, _ptr(W), f_out, int(relu),
                                     _ptr(Z), ld_z, _ptr(H_out), ld_o, _dtype(H), ctypes.c_void_p(_stream())),
            "gnn_layer_forward")
@@ -311,17 +392,37 @@ def layer_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tens
     ld_z, _ = _mat(Z)
     ld_dz = _mat(dZ)[0] if dZ is not None else 0
     ld_dh = _mat(dH)[0] if dH is not None else 0
-    assert dW.dtype == torch.float32 and dW.is_contiguous()
+    what = "gnn_layer_backward"
+    K, Kp = _k(g, f_in), _z_width(g, f_in, G.dtype)
+    _weights(what, W, K, f_out)
+    _weights(what, dW, K, f_out)
+    _need(all(t is None or t.dtype == G.dtype for t in (H_out, Z, dZ, dH)), what, "activations share one dtype")
+    _need(_rows(G) >= g.n_local and _rows(H_out) >= g.n_local and _rows(Z) >= g.n_local, what,
+          "G, H_out and Z need n_local rows")
+    _need(_width(Z) >= Kp, what, "Z is narrower than the aggregation output")
+    _need(dZ is None or (_rows(dZ) >= g.n_local and _width(dZ) >= Kp), what, "dZ needs n_local rows as wide as Z")
+    _need(dH is None or (_rows(dH) >= (g.n_total if want_halo_grad else g.n_local) and _width(dH) >= f_in), what,
+          "dH needs n_local rows (n_local + n_halo with the halo gradient) of f_in columns")
     _check(_lib().gnn_layer_backward(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(Z), ld_z,
                                      _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(dZ), ld_dz, _ptr(dH), ld_dh,
                                      int(want_halo_grad), _dtype(G), ctypes.c_void_p(_stream())),
            "gnn_layer_backward")
 
 
+def _softmax_args(what: str, logits, labels, G, row_loss, loss):
+    n, C = int(logits.shape[0]), int(logits.shape[1])
+    _need(labels.dtype == torch.int32 and row_loss.dtype == torch.float32 and loss.dtype == torch.float32, what,
+          "int32 labels, float32 row_loss and loss")
+    _need(G.dtype == logits.dtype and _rows(G) >= n and _width(G) >= C, what, "G shaped like the logits")
+    _need(_numel(labels) >= n and _numel(row_loss) >= n and _numel(loss) >= 1, what,
+          "a label and a row_loss entry per row, one loss")
+
+
 def softmax_ce(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_loss: torch.Tensor,
                loss: torch.Tensor):
     ld, C = _mat(logits)
     ld_g, _ = _mat(G)
+    _softmax_args("gnn_softmax_ce", logits, labels, G, row_loss, loss)
     _check(_lib().gnn_softmax_ce(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g, _ptr(row_loss),
                                  _ptr(loss), _dtype(logits), ctypes.c_void_p(_stream())), "gnn_softmax_ce")
 
@@ -331,6 +432,7 @@ def softmax_ce_partial(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tens
     """softmax_ce whose mean (and gradient) divides by n_mean >= the rows of logits."""
     ld, C = _mat(logits)
     ld_g, _ = _mat(G)
+    _softmax_args("gnn_softmax_ce_partial", logits, labels, G, row_loss, loss)
     _check(_lib().gnn_softmax_ce_partial(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g,
                                          _ptr(row_loss), _ptr(loss), int(n_mean), _dtype(logits),
                                          ctypes.c_void_p(_stream())), "gnn_softmax_ce_partial")
@@ -340,7 +442,10 @@ def halo_grad_send(g: Graph, dH: torch.Tensor, halo_ids: torch.Tensor, gtable: t
     """gtable[halo_ids[i]] += dH[n_local + i] over the columns of dH's view (gtable: float32)."""
     ld_h, f = _mat(dH)
     ld_t, _ = _mat(gtable)
-    assert halo_ids.dtype == torch.int64 and gtable.dtype == torch.float32
+    what = "gnn_halo_grad_send"
+    _need(halo_ids.dtype == torch.int64 and gtable.dtype == torch.float32, what, "int64 ids, float32 gradient table")
+    _need(_numel(halo_ids) >= g.n_halo and _rows(dH) >= g.n_total and _width(gtable) >= f, what,
+          "n_halo ids, n_local + n_halo rows of dH, table rows as wide as dH's view")
     _check(_lib().gnn_halo_grad_send(ctypes.c_void_p(g.handle), _ptr(dH), ld_h, f, _ptr(halo_ids), _ptr(gtable),
                                      ld_t, gtable.shape[0], _dtype(dH), ctypes.c_void_p(_stream())),
            "gnn_halo_grad_send")
@@ -350,7 +455,10 @@ def halo_grad_recv(g: Graph, gtable: torch.Tensor, local_ids: torch.Tensor, dH: 
     """dH[v] += gtable[local_ids[v]] for the local rows, over the columns of dH's view."""
     ld_h, f = _mat(dH)
     ld_t, _ = _mat(gtable)
-    assert local_ids.dtype == torch.int64 and gtable.dtype == torch.float32
+    what = "gnn_halo_grad_recv"
+    _need(local_ids.dtype == torch.int64 and gtable.dtype == torch.float32, what, "int64 ids, float32 gradient table")
+    _need(_numel(local_ids) >= g.n_local and _rows(dH) >= g.n_local and _width(gtable) >= f, what,
+          "n_local ids, n_local rows of dH, table rows as wide as dH's view")
     _check(_lib().gnn_halo_grad_recv(ctypes.c_void_p(g.handle), _ptr(gtable), ld_t, gtable.shape[0],
                                      _ptr(local_ids), _ptr(dH), ld_h, f, _dtype(dH), ctypes.c_void_p(_stream())),
            "gnn_halo_grad_recv")
