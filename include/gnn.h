@@ -173,7 +173,10 @@ int64_t gnn_sage_half_offset(int64_t f, gnn_dtype dtype);
  *          GraphSAGE: self half at column 0, mean half at
  *          gnn_sage_half_offset(f_in), padding columns zero.  ld_z >= K'.
  *   H_out  device n_local x ld_out, dtype.
- * No bias (none in sigma(A^T H W)). */
+ * No bias (none in sigma(A^T H W)).  The aggregated rows may be up to 4096
+ * bytes (f_in x element size); wider returns GNN_EUNSUPPORTED.  bf16 layers
+ * whose shapes the tensor-core kernel takes run on it, the rest (and all
+ * fp32 layers) on a CUDA-core kernel with the same results up to rounding. */
 gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
                              int64_t f_out, int relu, void *Z, int64_t ld_z, void *H_out, int64_t ld_out,
                              gnn_dtype dtype, void *stream);
@@ -193,7 +196,8 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
  *          the transposed aggregation (first layer).  want_halo_grad != 0 also
  *          writes the n_halo halo rows (Sylvie Alg. 2: the HALO gradients J
  *          that are sent back to their owners).
- * dW is summed over rows in a fixed order (deterministic). */
+ * dW is summed over rows in a fixed order (deterministic).  Same width limit
+ * as gnn_layer_forward. */
 gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
                               const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out, int relu,
                               float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
@@ -217,7 +221,8 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
  *   dH = P W^T                           device (n_local + n_halo) x ld_dh, dtype,
  *                                        every row (the halo rows are Sylvie's
  *                                        J), or NULL to skip
- * The other arguments are as for gnn_layer_forward / gnn_layer_backward. */
+ * The other arguments are as for gnn_layer_forward / gnn_layer_backward; here
+ * the aggregated rows are f_out wide (at most 4096 bytes). */
 gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
                                     int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
                                     gnn_dtype dtype, void *stream);
