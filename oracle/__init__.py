@@ -242,6 +242,30 @@ def update_backward_dw_entries(G, Hout, Z, relu: bool, entries: Sequence[tuple])
     return out
 
 
+def update_backward_dw_columns(G, Hout, Z, relu: bool, cols: Sequence[int], bf16_act: bool, bf16_grad: bool,
+                               block_rows: int = 1 << 20) -> np.ndarray:
+    """Whole columns `cols` of dW = Z^T dY (K x len(cols)) from stored matrices.
+
+    G, Hout, Z are the stored arrays (uint16 bf16 bit patterns or float32; rows of
+    any leading dimension, the first K / N columns used).  Rows are taken in
+    blocks of block_rows, each block widened to float64 and its products summed
+    by the C routine; the block sums are added in row order in double, so the
+    host never holds a widened copy of the whole matrix."""
+    cols = [int(c) for c in cols]
+    n, K = Z.shape[0], Z.shape[1]
+    out = np.zeros((K, len(cols)), dtype=np.float64)
+    part = np.empty((K, len(cols)), dtype=np.float64)
+    for r0 in range(0, n, block_rows):
+        r1 = min(n, r0 + block_rows)
+        g = _f64(widen(G[r0:r1][:, cols], bf16_grad))
+        h = _f64(widen(Hout[r0:r1][:, cols], bf16_act))
+        z = _f64(widen(Z[r0:r1], bf16_act))
+        _L().oracle_update_backward_dw(_p(g), len(cols), _p(h), len(cols), _p(z), K, r1 - r0, K, len(cols),
+                                       int(relu), _p(part))
+        out += part
+    return out
+
+
 def transpose(part):
     """(rowptrT int32[nT+1], colidxT int32[nnz], permT int32[nnz]) of the block."""
     rp, ci = _csr(part)
@@ -352,24 +376,26 @@ def layer_forward(part, H: np.ndarray, W: np.ndarray, agg: str, relu: bool, bf16
 
 
 def layer_backward(part, T, G: np.ndarray, Hout: np.ndarray, Z: np.ndarray, W: np.ndarray, agg: str, relu: bool,
-                   want_dh: bool = True, bf16: bool = False):
+                   want_dh: bool = True, grad_bf16: bool = False):
     """(dW, dZ, dH) with dH over all n_local + n_halo rows (None when not wanted).
 
-    bf16=True rounds the stored dZ and dH to bf16, as the bf16 path stores them."""
+    grad_bf16=True rounds the stored dZ and dH to bf16, as a path that stores
+    activation gradients in bf16 does; with False they stay unrounded (the
+    fp32 gradient storage of the bf16 workloads)."""
     dW, dZ = update_backward(G, Hout, Z, W, relu, want_dz=want_dh)
     dH = None
     if want_dh:
-        if bf16:
+        if grad_bf16:
             dZ = round_bf16(dZ)
         f = Z.shape[1] if agg == "gcn" else Z.shape[1] // 2
         dH = aggregate_backward(part, T, dZ, f, agg)
-        if bf16:
+        if grad_bf16:
             dH = round_bf16(dH)
     return dW, dZ, dH
 
 
 def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_local: np.ndarray, agg: str,
-          bf16: bool = False):
+          bf16: bool = False, grad_bf16: bool = False):
     """One full-graph epoch of an L-layer model on one partition.
 
     tables[l] (float64, n_table x f_l) hold the stale representations of layer l
@@ -377,7 +403,14 @@ def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_l
     rows from tables[l]; the local rows of layer 0 are the partition's own
     features (tables[0][local_ids]); the local rows of layer l > 0 are the
     previous layer's output, which is pushed into tables[l] (push of a copy).
-    ReLU on every layer but the last.  Returns a dict of every intermediate.
+    ReLU on every layer but the last.
+
+    Precision of what is stored between steps: bf16=True rounds the
+    activations (Z, H') to bf16; grad_bf16=True also rounds the activation
+    gradients (G, dZ, dH).  Everything else is double.
+
+    Returns a dict of every intermediate; G[l] is the gradient with respect to
+    layer l's output that layer l's backward consumed.
     """
     L = len(Ws)
     nL = part.n_local
@@ -399,14 +432,17 @@ def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_l
             new_tables[l + 1][part.local_ids, :Hout.shape[1]] = Hout
         h_local = Hout
     loss, G = softmax_ce(Houts[-1], labels_local)
-    if bf16:
+    if grad_bf16:
         G = round_bf16(G)
     dWs = [None] * L
     dHs = [None] * L
+    Gs = [None] * L
     for l in reversed(range(L)):
-        dW, _, dH = layer_backward(part, T, G, Houts[l], Zs[l], Ws[l], agg, relu=l < L - 1, want_dh=l > 0, bf16=bf16)
+        Gs[l] = G
+        dW, _, dH = layer_backward(part, T, G, Houts[l], Zs[l], Ws[l], agg, relu=l < L - 1, want_dh=l > 0,
+                                   grad_bf16=grad_bf16)
         dWs[l] = dW
         dHs[l] = dH
         if l > 0:
             G = dH[:nL]
-    return dict(H=Hs, Z=Zs, Hout=Houts, loss=loss, dW=dWs, dH=dHs, tables=new_tables, T=T)
+    return dict(H=Hs, Z=Zs, Hout=Houts, loss=loss, dW=dWs, dH=dHs, G=Gs, tables=new_tables, T=T)

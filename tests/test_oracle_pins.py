@@ -97,6 +97,29 @@ def test_update_forward_backward_match_dense():
         assert _rel(ent, np.array([dW[k, j] for k, j in sel])) < 1e-14
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+def test_dw_columns_streamed_over_row_blocks_match_dense(bf16):
+    # the full-size dW check streams rows in blocks; on a small case it equals
+    # the dense product (ragged last block, strided stored rows, bf16 bits)
+    rng = np.random.default_rng(17)
+    n, K, N = 1037, 12, 9
+    Zf = rng.standard_normal((n, K + 4)).astype(np.float32)
+    Gf = rng.standard_normal((n, N + 3)).astype(np.float32)
+    Hf = rng.standard_normal((n, N + 3)).astype(np.float32)
+    if bf16:
+        torch = pytest.importorskip("torch")
+        bits = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        Zs, Gs, Hs = bits(Zf), bits(Gf), bits(Hf)
+    else:
+        Zs, Gs, Hs = Zf, Gf, Hf
+    Zw, Gw, Hw = (oracle.widen(a, bf16) for a in (Zs, Gs, Hs))
+    cols = [0, 4, N - 1]
+    for relu in (False, True):
+        got = oracle.update_backward_dw_columns(Gs, Hs, Zs[:, :K], relu, cols, bf16, bf16, block_rows=100)
+        dY = Gw[:, cols] * (Hw[:, cols] > 0) if relu else Gw[:, cols]
+        assert _rel(got, Zw[:, :K].T @ dY) < 1e-13
+
+
 def test_relu_derivative_at_zero_is_zero():
     # ReLU'(0) = 0: a pre-activation of exactly zero passes no gradient.
     Z = np.array([[1.0, -1.0]])
