@@ -215,9 +215,15 @@ def update(Z: np.ndarray, W: np.ndarray, relu: bool) -> np.ndarray:
 
 
 def update_backward(G: np.ndarray, Hout: np.ndarray, Z: np.ndarray, W: np.ndarray, relu: bool,
-                    want_dz: bool = True):
-    """Returns (dW, dZ): dY = G * 1[Hout > 0] (relu) or G; dW = Z^T dY; dZ = dY W^T."""
+                    want_dz: bool = True, dy_bf16: bool = False):
+    """Returns (dW, dZ): dY = G * 1[Hout > 0] (relu) or G; dW = Z^T dY; dZ = dY W^T.
+
+    dy_bf16=True rounds dY to bf16 before the products: with bf16 activations
+    every operand of the update's products is bf16 (Z, W and dY alike)."""
     G, Hout, Z, W = _f64(G), _f64(Hout), _f64(Z), _f64(W)
+    if dy_bf16:
+        G = round_bf16(G * (Hout > 0) if relu else G)
+        relu = False
     n, N = G.shape
     K = W.shape[0]
     dW = np.empty((K, N), dtype=np.float64)
@@ -247,10 +253,12 @@ def update_backward_dw_columns(G, Hout, Z, relu: bool, cols: Sequence[int], bf16
     """Whole columns `cols` of dW = Z^T dY (K x len(cols)) from stored matrices.
 
     G, Hout, Z are the stored arrays (uint16 bf16 bit patterns or float32; rows of
-    any leading dimension, the first K / N columns used).  Rows are taken in
-    blocks of block_rows, each block widened to float64 and its products summed
-    by the C routine; the block sums are added in row order in double, so the
-    host never holds a widened copy of the whole matrix."""
+    any leading dimension, the first K / N columns used).  With bf16 activations
+    dY is rounded to bf16 (an operand of the bf16 products, as in
+    update_backward).  Rows are taken in blocks of block_rows, each block
+    widened to float64 and its products summed by the C routine; the block sums
+    are added in row order in double, so the host never holds a widened copy of
+    the whole matrix."""
     cols = [int(c) for c in cols]
     n, K = Z.shape[0], Z.shape[1]
     out = np.zeros((K, len(cols)), dtype=np.float64)
@@ -260,8 +268,12 @@ def update_backward_dw_columns(G, Hout, Z, relu: bool, cols: Sequence[int], bf16
         g = _f64(widen(G[r0:r1][:, cols], bf16_grad))
         h = _f64(widen(Hout[r0:r1][:, cols], bf16_act))
         z = _f64(widen(Z[r0:r1], bf16_act))
+        rl = relu
+        if bf16_act:
+            g = _f64(round_bf16(g * (h > 0) if relu else g))
+            rl = False
         _L().oracle_update_backward_dw(_p(g), len(cols), _p(h), len(cols), _p(z), K, r1 - r0, K, len(cols),
-                                       int(relu), _p(part))
+                                       int(rl), _p(part))
         out += part
     return out
 
@@ -376,13 +388,14 @@ def layer_forward(part, H: np.ndarray, W: np.ndarray, agg: str, relu: bool, bf16
 
 
 def layer_backward(part, T, G: np.ndarray, Hout: np.ndarray, Z: np.ndarray, W: np.ndarray, agg: str, relu: bool,
-                   want_dh: bool = True, grad_bf16: bool = False):
+                   want_dh: bool = True, bf16: bool = False, grad_bf16: bool = False):
     """(dW, dZ, dH) with dH over all n_local + n_halo rows (None when not wanted).
 
-    grad_bf16=True rounds the stored dZ and dH to bf16, as a path that stores
-    activation gradients in bf16 does; with False they stay unrounded (the
-    fp32 gradient storage of the bf16 workloads)."""
-    dW, dZ = update_backward(G, Hout, Z, W, relu, want_dz=want_dh)
+    bf16=True: the activations are bf16, so dY enters the update's products as
+    bf16 (like Z and W).  grad_bf16=True rounds the stored dZ and dH to bf16, as
+    a path that stores activation gradients in bf16 does; with False they stay
+    unrounded (the fp32 gradient storage of the bf16 workloads)."""
+    dW, dZ = update_backward(G, Hout, Z, W, relu, want_dz=want_dh, dy_bf16=bf16)
     dH = None
     if want_dh:
         if grad_bf16:
@@ -405,9 +418,10 @@ def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_l
     previous layer's output, which is pushed into tables[l] (push of a copy).
     ReLU on every layer but the last.
 
-    Precision of what is stored between steps: bf16=True rounds the
-    activations (Z, H') to bf16; grad_bf16=True also rounds the activation
-    gradients (G, dZ, dH).  Everything else is double.
+    Precision: bf16=True rounds the activations (Z, H') to bf16, and the
+    backward's products take dY in bf16 (their operands are bf16 like Z and W);
+    grad_bf16=True also rounds the stored activation gradients (G, dZ, dH).
+    Everything else is double.
 
     Returns a dict of every intermediate; G[l] is the gradient with respect to
     layer l's output that layer l's backward consumed.
@@ -440,7 +454,7 @@ def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_l
     for l in reversed(range(L)):
         Gs[l] = G
         dW, _, dH = layer_backward(part, T, G, Houts[l], Zs[l], Ws[l], agg, relu=l < L - 1, want_dh=l > 0,
-                                   grad_bf16=grad_bf16)
+                                   bf16=bf16, grad_bf16=grad_bf16)
         dWs[l] = dW
         dHs[l] = dH
         if l > 0:
