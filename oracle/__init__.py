@@ -86,6 +86,11 @@ def _L():
         L.oracle_codec_quantize.restype = None
         L.oracle_codec_dequantize.argtypes = [vp, i64, vp, i64, i64, i32, vp, i64]
         L.oracle_codec_dequantize.restype = None
+        L.oracle_gat_attend.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, ctypes.c_double, vp, vp, i64]
+        L.oracle_gat_attend.restype = None
+        L.oracle_gat_attend_backward.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i64, ctypes.c_double, vp, vp, i64,
+                                                 vp, i64, vp, vp]
+        L.oracle_gat_attend_backward.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -326,6 +331,82 @@ def softmax_ce(logits: np.ndarray, labels: np.ndarray):
     loss = _L().oracle_softmax_ce(_p(x), C, n, C, _p(lab), _p(G), C)
     return float(loss), G
 
+
+
+# --------------------------------------------------------------------------
+# graph attention (GAT; named by the Sylvie and DIGEST pages, formula from the
+# textbook single-head layer)
+# --------------------------------------------------------------------------
+
+GAT_SLOPE = 0.2  # LeakyReLU slope of the attention scores
+
+
+def gat_attend(part, T: np.ndarray, s_src: np.ndarray, s_dst: np.ndarray):
+    """(alpha per entry, Y = sum_u alpha_vu T[u] for the local rows)."""
+    rp, ci = _csr(part)
+    T = _f64(T)
+    f = T.shape[1]
+    alpha = np.empty(max(part.nnz, 1), dtype=np.float64)
+    Y = np.empty((part.n_local, f), dtype=np.float64)
+    _L().oracle_gat_attend(_p(rp), _p(ci), part.n_local, _p(_f64(s_src)), _p(_f64(s_dst)), _p(T), f, f, GAT_SLOPE,
+                           _p(alpha), _p(Y), f)
+    return alpha[:part.nnz], Y
+
+
+def gat_attend_backward(part, T, s_src, s_dst, alpha, dY):
+    """(dT over every row, ds_src over every row, ds_dst over the local rows)."""
+    rp, ci = _csr(part)
+    T, dY = _f64(T), _f64(dY)
+    f = T.shape[1]
+    nT = part.n_local + part.n_halo
+    dT = np.empty((nT, f), dtype=np.float64)
+    ds_src = np.empty(nT, dtype=np.float64)
+    ds_dst = np.empty(max(part.n_local, 1), dtype=np.float64)
+    a = _f64(alpha) if part.nnz else np.zeros(1)
+    _L().oracle_gat_attend_backward(_p(rp), _p(ci), part.n_local, nT, _p(_f64(s_src)), _p(_f64(s_dst)), _p(T), f, f,
+                                    GAT_SLOPE, _p(a), _p(dY), f, _p(dT), f, _p(ds_src), _p(ds_dst))
+    return dT, ds_src, ds_dst[:part.n_local]
+
+
+def gat_layer_forward(part, H: np.ndarray, W: np.ndarray, a_src: np.ndarray, a_dst: np.ndarray, relu: bool,
+                      bf16: bool = False):
+    """One GAT layer: T = H W (every row), scores s_src = T a_src (every row),
+    s_dst = T a_dst (local rows), attention and Y; H' = relu(Y) or Y.  bf16=True
+    stores T and H' in bf16 (the scores and alpha stay unrounded).
+    Returns dict(T, s_src, s_dst, alpha, Hout)."""
+    T = update(H, W, relu=False)
+    if bf16:
+        T = round_bf16(T)
+    s_src = T @ _f64(a_src)
+    s_dst = T[:part.n_local] @ _f64(a_dst)
+    alpha, Y = gat_attend(part, T, s_src, s_dst)
+    Hout = np.maximum(Y, 0.0) if relu else Y
+    if bf16:
+        Hout = round_bf16(Hout)
+    return dict(T=T, s_src=s_src, s_dst=s_dst, alpha=alpha, Hout=Hout)
+
+
+def gat_layer_backward(part, fwd: dict, H: np.ndarray, G: np.ndarray, W: np.ndarray, a_src: np.ndarray,
+                       a_dst: np.ndarray, relu: bool, bf16: bool = False, grad_bf16: bool = False):
+    """Chain rule of gat_layer_forward: dY = G * 1[H' > 0] (relu) or G; the
+    attention's backward gives dT, ds_src, ds_dst; dT += ds_src a_src^T (every
+    row) + ds_dst a_dst^T (local rows); da_src = T^T ds_src, da_dst = T_local^T
+    ds_dst; dW = H^T dT, dH = dT W^T (every row: the halo rows are J).  With
+    bf16 activations dT enters the products dW, dH as bf16 (their operands are
+    bf16); grad_bf16 rounds the stored dH.  Returns dict(dW, da_src, da_dst, dT, dH)."""
+    nL = part.n_local
+    G = _f64(G)
+    dY = G * (fwd["Hout"] > 0) if relu else G
+    dT, ds_src, ds_dst = gat_attend_backward(part, fwd["T"], fwd["s_src"], fwd["s_dst"], fwd["alpha"], dY)
+    dT = dT + ds_src[:, None] * _f64(a_src)[None, :]
+    dT[:nL] += ds_dst[:, None] * _f64(a_dst)[None, :]
+    da_src = fwd["T"].T @ ds_src
+    da_dst = fwd["T"][:nL].T @ ds_dst
+    dTp = round_bf16(dT) if bf16 else dT
+    dW, dH = update_backward(dTp, dTp, _f64(H), _f64(W), relu=False, want_dz=True)
+    if grad_bf16:
+        dH = round_bf16(dH)
+    return dict(dW=dW, da_src=da_src, da_dst=da_dst, dT=dT, dH=dH)
 
 
 # --------------------------------------------------------------------------

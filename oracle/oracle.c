@@ -221,6 +221,92 @@ void oracle_update_backward_dw(const double *G, int64_t ld_g, const double *Hout
 }
 
 /* ------------------------------------------------------------------------ */
+/* graph attention (GAT): the Sylvie page names GAT among the models it       */
+/* trains and the DIGEST page benchmarks it; neither prints its formula, so   */
+/* this is the textbook single-head layer (Velickovic et al., ICLR 2018)      */
+/* ------------------------------------------------------------------------ */
+
+/* For every row v and entry u of row v (the self loop is an entry of A + I):
+ *   z_vu = s_dst[v] + s_src[u],  e_vu = z_vu if z_vu > 0 else slope * z_vu,
+ *   alpha_vu = exp(e_vu) / sum over the row's entries u' of exp(e_vu'),
+ *   Y[v] = sum_u alpha_vu T[u].
+ * alpha is written per entry (CSR order), Y for the n_local rows. */
+void oracle_gat_attend(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, const double *s_src,
+                       const double *s_dst, const double *T, int64_t ld_t, int64_t f, double slope, double *alpha,
+                       double *Y, int64_t ld_y) {
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t v = 0; v < n_local; ++v) {
+        double *y = Y + (size_t)v * (size_t)ld_y;
+        for (int64_t j = 0; j < f; ++j) y[j] = 0.0;
+        const int32_t b = rowptr[v], e = rowptr[v + 1];
+        if (e == b) continue;
+        double mx = -HUGE_VAL;
+        for (int32_t k = b; k < e; ++k) {
+            double z = s_dst[v] + s_src[colidx[k]];
+            double a = z > 0.0 ? z : slope * z;
+            alpha[k] = a;
+            if (a > mx) mx = a;
+        }
+        double sum = 0.0;
+        for (int32_t k = b; k < e; ++k) {
+            alpha[k] = exp(alpha[k] - mx);
+            sum += alpha[k];
+        }
+        for (int32_t k = b; k < e; ++k) {
+            alpha[k] /= sum;
+            const double *t = T + (size_t)colidx[k] * (size_t)ld_t;
+            for (int64_t j = 0; j < f; ++j) y[j] += alpha[k] * t[j];
+        }
+    }
+}
+
+/* Backward of oracle_gat_attend by the chain rule, given dY (n_local rows):
+ *   dT[u]     = sum over entries (v, u) of alpha_vu dY[v]
+ *   dalpha_vu = dY[v] . T[u]
+ *   de_vu     = alpha_vu (dalpha_vu - sum over the row's u' of alpha_vu' dalpha_vu')
+ *   dz_vu     = de_vu (z_vu > 0 ? 1 : slope)
+ *   ds_dst[v] = sum_u dz_vu,   ds_src[u] = sum over entries (v, u) of dz_vu
+ * dT (n_total rows) and ds_src (n_total), ds_dst (n_local) are overwritten.
+ * Rows are taken one after another (the scatter into dT and ds_src is a plain
+ * loop, no parallelism). */
+void oracle_gat_attend_backward(const int32_t *rowptr, const int32_t *colidx, int64_t n_local, int64_t n_total,
+                                const double *s_src, const double *s_dst, const double *T, int64_t ld_t, int64_t f,
+                                double slope, const double *alpha, const double *dY, int64_t ld_dy, double *dT,
+                                int64_t ld_dt, double *ds_src, double *ds_dst) {
+    for (int64_t u = 0; u < n_total; ++u) {
+        double *d = dT + (size_t)u * (size_t)ld_dt;
+        for (int64_t j = 0; j < f; ++j) d[j] = 0.0;
+        ds_src[u] = 0.0;
+    }
+    for (int64_t v = 0; v < n_local; ++v) {
+        const double *dy = dY + (size_t)v * (size_t)ld_dy;
+        const int32_t b = rowptr[v], e = rowptr[v + 1];
+        double dot_sum = 0.0;
+        for (int32_t k = b; k < e; ++k) {
+            const double *t = T + (size_t)colidx[k] * (size_t)ld_t;
+            double da = 0.0;
+            for (int64_t j = 0; j < f; ++j) da += dy[j] * t[j];
+            dot_sum += alpha[k] * da;
+        }
+        double sd = 0.0;
+        for (int32_t k = b; k < e; ++k) {
+            const int64_t u = colidx[k];
+            const double *t = T + (size_t)u * (size_t)ld_t;
+            double da = 0.0;
+            for (int64_t j = 0; j < f; ++j) da += dy[j] * t[j];
+            const double de = alpha[k] * (da - dot_sum);
+            const double z = s_dst[v] + s_src[u];
+            const double dz = de * (z > 0.0 ? 1.0 : slope);
+            sd += dz;
+            ds_src[u] += dz;
+            double *d = dT + (size_t)u * (size_t)ld_dt;
+            for (int64_t j = 0; j < f; ++j) d[j] += alpha[k] * dy[j];
+        }
+        ds_dst[v] = sd;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* transpose of the block (CAGNET: A and A^T are kept apart explicitly)      */
 /* ------------------------------------------------------------------------ */
 
