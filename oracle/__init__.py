@@ -409,6 +409,42 @@ def gat_layer_backward(part, fwd: dict, H: np.ndarray, G: np.ndarray, W: np.ndar
     return dict(dW=dW, da_src=da_src, da_dst=da_dst, dT=dT, dH=dH)
 
 
+def gat_epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], a_srcs: Sequence[np.ndarray],
+              a_dsts: Sequence[np.ndarray], labels_local: np.ndarray, bf16: bool = False, grad_bf16: bool = False):
+    """One epoch of an L-layer GAT on one partition, composed like epoch():
+    layer l pulls its halo rows from tables[l] (its local rows: the features,
+    then the previous layer's output), ReLU on all layers but the last, mean
+    softmax cross-entropy over the local rows, then the backward layer by layer
+    (G of layer l - 1 = the local rows of layer l's dH).  Returns a dict with
+    the forward intermediates (fwd), Hout, loss, dW, da_src, da_dst, dH."""
+    L = len(Ws)
+    nL = part.n_local
+    h_local = tables[0][part.local_ids]
+    Hs, fwds = [], []
+    for l in range(L):
+        f = Ws[l].shape[0]
+        H = np.zeros((part.n_local + part.n_halo, f), dtype=np.float64)
+        H[:nL] = h_local[:, :f]
+        if part.n_halo:
+            H[nL:] = tables[l][part.halo_ids, :f]
+        fw = gat_layer_forward(part, H, Ws[l], a_srcs[l], a_dsts[l], relu=l < L - 1, bf16=bf16)
+        Hs.append(H)
+        fwds.append(fw)
+        h_local = fw["Hout"]
+    loss, G = softmax_ce(fwds[-1]["Hout"], labels_local)
+    if grad_bf16:
+        G = round_bf16(G)
+    out = dict(fwd=fwds, H=Hs, Hout=[fw["Hout"] for fw in fwds], loss=loss, dW=[None] * L, da_src=[None] * L,
+               da_dst=[None] * L, dH=[None] * L)
+    for l in reversed(range(L)):
+        bw = gat_layer_backward(part, fwds[l], Hs[l], G, Ws[l], a_srcs[l], a_dsts[l], relu=l < L - 1, bf16=bf16,
+                                grad_bf16=grad_bf16)
+        out["dW"][l], out["da_src"][l], out["da_dst"][l] = bw["dW"], bw["da_src"], bw["da_dst"]
+        out["dH"][l] = bw["dH"]
+        G = bw["dH"][:nL]
+    return out
+
+
 # --------------------------------------------------------------------------
 # Sylvie low-bit halo codec (Sylvie page, Quantizer / Dequantizer)
 # --------------------------------------------------------------------------

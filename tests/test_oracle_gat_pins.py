@@ -115,3 +115,51 @@ def test_gat_gradients_match_finite_differences():
             ap[i], am[i] = xp, xm
             num[idx] = (loss(*ap) - loss(*am)) / (2 * eps)
         assert _rel(bw[name], num) < 1e-6, name
+
+
+def test_gat_epoch_gradients_match_finite_differences_of_its_loss():
+    # a 3-layer GAT on a partition with stale halo tables: dW, da_src, da_dst of
+    # every layer and the halo rows of every dH are the derivatives of the loss
+    N, nL = 26, 16
+    A = random_sym_adjacency(N, 0.2, 8)
+    part, _ = partition_from_dense(A, np.arange(nL))
+    rng = np.random.default_rng(8)
+    widths = [4, 5, 4, 3]
+    Ws = [rng.standard_normal((widths[l], widths[l + 1])) * 0.7 for l in range(3)]
+    a_s = [rng.standard_normal(widths[l + 1]) * 0.5 for l in range(3)]
+    a_d = [rng.standard_normal(widths[l + 1]) * 0.5 for l in range(3)]
+    tables = [rng.standard_normal((N, f)) for f in widths[:-1]]
+    y = rng.integers(0, widths[-1], nL).astype(np.int32)
+    ref = oracle.gat_epoch(part, tables, Ws, a_s, a_d, y)
+    for l in range(2):
+        pre = oracle.gat_attend(part, ref["fwd"][l]["T"], ref["fwd"][l]["s_src"], ref["fwd"][l]["s_dst"])[1]
+        assert np.min(np.abs(pre)) > 2e-5
+
+    def loss(Wx, asx, adx, tx):
+        return oracle.gat_epoch(part, tx, Wx, asx, adx, y)["loss"]
+
+    eps = 1e-6
+    for name, params, key in (("W", Ws, "dW"), ("a_src", a_s, "da_src"), ("a_dst", a_d, "da_dst")):
+        for l in range(3):
+            num = np.zeros_like(params[l])
+            for idx in np.ndindex(*params[l].shape):
+                pp = [p.copy() for p in params]
+                pm = [p.copy() for p in params]
+                pp[l][idx] += eps
+                pm[l][idx] -= eps
+                args_p = {"W": Ws, "a_src": a_s, "a_dst": a_d}
+                args_m = dict(args_p)
+                args_p[name], args_m[name] = pp, pm
+                num[idx] = (loss(args_p["W"], args_p["a_src"], args_p["a_dst"], tables)
+                            - loss(args_m["W"], args_m["a_src"], args_m["a_dst"], tables)) / (2 * eps)
+            assert _rel(ref[key][l], num) < 1e-6, (name, l)
+    for l in (1, 2):
+        num = np.zeros((part.n_halo, widths[l]))
+        for i, u in enumerate(part.halo_ids):
+            for c in range(widths[l]):
+                tp = [t.copy() for t in tables]
+                tm = [t.copy() for t in tables]
+                tp[l][u, c] += eps
+                tm[l][u, c] -= eps
+                num[i, c] = (loss(Ws, a_s, a_d, tp) - loss(Ws, a_s, a_d, tm)) / (2 * eps)
+        assert _rel(ref["dH"][l][nL:], num) < 1e-6, l
