@@ -410,10 +410,12 @@ def gat_layer_backward(part, fwd: dict, H: np.ndarray, G: np.ndarray, W: np.ndar
 
 
 def gat_epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], a_srcs: Sequence[np.ndarray],
-              a_dsts: Sequence[np.ndarray], labels_local: np.ndarray, bf16: bool = False, grad_bf16: bool = False):
+              a_dsts: Sequence[np.ndarray], labels_local: np.ndarray, bf16: bool = False, grad_bf16: bool = False,
+              hidden_relu: bool = True):
     """One epoch of an L-layer GAT on one partition, composed like epoch():
     layer l pulls its halo rows from tables[l] (its local rows: the features,
-    then the previous layer's output), ReLU on all layers but the last, mean
+    then the previous layer's output), ReLU on all layers but the last (none
+    with hidden_relu=False), mean
     softmax cross-entropy over the local rows, then the backward layer by layer
     (G of layer l - 1 = the local rows of layer l's dH).  Returns a dict with
     the forward intermediates (fwd), Hout, loss, dW, da_src, da_dst, dH."""
@@ -427,7 +429,7 @@ def gat_epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], a_sr
         H[:nL] = h_local[:, :f]
         if part.n_halo:
             H[nL:] = tables[l][part.halo_ids, :f]
-        fw = gat_layer_forward(part, H, Ws[l], a_srcs[l], a_dsts[l], relu=l < L - 1, bf16=bf16)
+        fw = gat_layer_forward(part, H, Ws[l], a_srcs[l], a_dsts[l], relu=hidden_relu and l < L - 1, bf16=bf16)
         Hs.append(H)
         fwds.append(fw)
         h_local = fw["Hout"]
@@ -437,8 +439,8 @@ def gat_epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], a_sr
     out = dict(fwd=fwds, H=Hs, Hout=[fw["Hout"] for fw in fwds], loss=loss, dW=[None] * L, da_src=[None] * L,
                da_dst=[None] * L, dH=[None] * L)
     for l in reversed(range(L)):
-        bw = gat_layer_backward(part, fwds[l], Hs[l], G, Ws[l], a_srcs[l], a_dsts[l], relu=l < L - 1, bf16=bf16,
-                                grad_bf16=grad_bf16)
+        bw = gat_layer_backward(part, fwds[l], Hs[l], G, Ws[l], a_srcs[l], a_dsts[l], relu=hidden_relu and l < L - 1,
+                                bf16=bf16, grad_bf16=grad_bf16)
         out["dW"][l], out["da_src"][l], out["da_dst"][l] = bw["dW"], bw["da_src"], bw["da_dst"]
         out["dH"][l] = bw["dH"]
         G = bw["dH"][:nL]
