@@ -123,12 +123,14 @@ def narrow_layers(w, enabled: bool = False):
     return [enabled and w.agg != "sage" and w.widths[l + 1] < w.widths[l] for l in range(w.layers)]
 
 
-def aggregation_bytes(part, w, elem: int, narrow: bool = False):
+def aggregation_bytes(part, w, elem: int, narrow: bool = False, grad_elem: int = None):
     """Compulsory bytes of each aggregation launch of one step, in launch order
     (forward layers 0..L-1, then backward layers L-1..1): row pointers, column
     ids, the normalisation vector, every input row once and every output row once.
-    A narrow layer aggregates at its output width (T = H W forward, dY backward),
-    and its backward aggregation also runs on the first layer."""
+    The backward launches move gradient rows (grad_elem bytes per value, default
+    elem).  A narrow layer aggregates at its output width (T = H W forward, dY
+    backward), and its backward aggregation also runs on the first layer."""
+    gel = elem if grad_elem is None else grad_elem
     nL, nT, nnz = part.n_local, part.n_total, part.nnz
     sage = w.agg == "sage"
     nar = narrow_layers(w, narrow)
@@ -142,7 +144,7 @@ def aggregation_bytes(part, w, elem: int, narrow: bool = False):
             continue
         f = w.widths[l + 1] if nar[l] else w.widths[l]
         in_cols = 2 * f if sage else f
-        bwd.append(4 * (nT + 1) + 4 * nnz + 4 * (nL if sage else nT) + nL * in_cols * elem + nT * f * elem)
+        bwd.append(4 * (nT + 1) + 4 * nnz + 4 * (nL if sage else nT) + nL * in_cols * gel + nT * f * gel)
     return fwd, bwd
 
 
@@ -161,19 +163,22 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per aggregation launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def ncu_traffic(workload: str, grad: str):
+    """DRAM bytes of one step's aggregation launches from the committed ncu
+    summary, if it was taken on the current kernel source with the same gradient
+    storage; else None."""
     p = os.path.join(ROOT, "profiles", f"aggregate_{workload}.txt")
     if not os.path.exists(p):
         return None
-    src, traffic = None, None
+    src, traffic, gd = None, None, None
     for line in open(p):
         if line.startswith("kernel_source_sha1:"):
             src = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_step_aggregations:"):
             traffic = float(line.split(":", 1)[1].strip())
-    if src != kernel_source_hash() or traffic is None:
+        if line.startswith("grad_dtype:"):
+            gd = line.split(":", 1)[1].strip()
+    if src != kernel_source_hash() or traffic is None or gd != grad:
         return None
     return traffic
 
@@ -430,6 +435,45 @@ def measure_other_schedule(m, stream, steps: int) -> float:
         m.overlap, m.side = was, side
 
 
+def measure_other_precision(m, stream, steps: int, ef: int):
+    """The step with the activation gradients stored in the other dtype (bf16 <-> fp32; bf16 activations)."""
+    import torch
+
+    was = m.grad_dtype
+    other = torch.bfloat16 if was == torch.float32 else torch.float32
+    m.set_grad_dtype(other)
+    try:
+        m.step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        m.check_errors()
+        ms = e0.elapsed_time(e1) / steps
+    finally:
+        m.set_grad_dtype(was)
+    return {"grad_dtype": "bf16" if other == torch.bfloat16 else "f32", "ms_per_step": ms, "value": ef / (ms / 1e3),
+            "steps": steps}
+
+
+def measure_h2d(x_pin, dst, stream, reps: int = 3) -> float:
+    """GB/s of the e2e leg's feature copy alone (pinned host -> device)."""
+    import torch
+
+    dst.copy_(x_pin, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        dst.copy_(x_pin, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return x_pin.numel() * x_pin.element_size() * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -444,7 +488,9 @@ def run_ours(args, rank, world, local_rank):
     part = w.make(SEED + rank)
     t_gen = time.time() - t_gen
     t_create = time.time()
-    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda", overlap=not args.sequential, narrow=args.narrow)
+    gdt = torch.bfloat16 if (bf and args.grad_dtype == "bf16") else torch.float32
+    m = PartitionModel(part, w.widths, w.agg, tdt, "cuda", overlap=not args.sequential, narrow=args.narrow,
+                       grad_dtype=gdt)
     torch.cuda.synchronize()
     t_create = time.time() - t_create
     for l in range(w.layers):
@@ -501,12 +547,12 @@ def run_ours(args, rank, world, local_rank):
 
     # dominant kernel: the aggregation (forward + backward launches)
     hbm, bf16_tf, peak_kind = measured_peaks()
-    fwd_b, bwd_b = aggregation_bytes(part, w, 2 if bf else 4, args.narrow)
+    fwd_b, bwd_b = aggregation_bytes(part, w, 2 if bf else 4, args.narrow, 2 if gdt == torch.bfloat16 else 4)
     alg_bytes = (sum(fwd_b) + sum(bwd_b)) * args.steps
     agg_ms = prof["agg_fwd"][0] + prof["agg_bwd"][0]
     agg_launches = prof["agg_fwd"][1] + prof["agg_bwd"][1]
     achieved = alg_bytes / (agg_ms / 1e3) / 1e9 if agg_ms > 0 else 0.0
-    traffic = ncu_traffic(w.name)
+    traffic = ncu_traffic(w.name, "bf16" if gdt == torch.bfloat16 else "f32")
     breakdown = {k: round(v[0] / args.steps, 3) for k, v in prof.items()}
     breakdown["other"] = round(ms_local - sum(v[0] for v in prof.values()) / args.steps, 3)
 
@@ -540,6 +586,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, True)
     codec = measure_codec(m, part, w, tdt, stream)
     other_ms = measure_other_schedule(m, stream, max(3, min(args.steps, 5)))
+    other_prec = measure_other_precision(m, stream, max(3, min(args.steps, 5)), ef) if bf and not args.narrow else None
+    h2d_gbs = measure_h2d(x_pin, h0, stream)
     h2d = int(x_pin.numel() * x_pin.element_size() + y_pin.numel() * 4)
     d2h = int(4 + sum(d.numel() * 4 for d in m.dW))
 
@@ -572,6 +620,10 @@ def run_ours(args, rank, world, local_rank):
                    else "L2 flushed before every timed step (512 MiB written); steps timed one by one"),
             "seed": SEED,
             "layer_order": "multiplication first on narrowing GCN layers" if args.narrow else "aggregation first",
+            "grad_dtype": "bf16" if gdt == torch.bfloat16 else "f32",
+            "precision": ("bf16 activations (features, tables, Z, layer outputs), "
+                          + ("bf16" if gdt == torch.bfloat16 else "fp32") + " activation gradients (G, dZ, dH), "
+                          "fp32 accumulation, fp32 dW") if bf else "fp32 throughout",
         },
         "roofline": {
             "bound": "hbm",
@@ -595,7 +647,9 @@ def run_ours(args, rank, world, local_rank):
                           "beside the layers, so the groups can sum to more than the step ('other' < 0)",
         "cpu_baseline": cpu,
         "e2e": {"value": total_ef / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms, "steps": e2e_steps,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_gbs_feature_copy_alone": round(h2d_gbs, 1)},
+        "other_precision": other_prec,
         "gpu_launches": int(launches),
         "halo_codec": codec,
         "schedule": "sequential" if args.sequential else "overlapped (pulls and pushes on a second stream)",
@@ -650,9 +704,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--narrow", action="store_true",
                     help="GCN layers whose output is narrower than their input multiply first: A (H W)")
+    ap.add_argument("--grad-dtype", choices=["f32", "bf16"], default="f32",
+                    help="storage of the activation gradients of bf16 workloads (default fp32)")
     ap.add_argument("--sequential", action="store_true",
                     help="pulls and pushes in line on the compute stream instead of on a second stream")
     args = ap.parse_args(argv)
+    if args.narrow and args.grad_dtype != "bf16" and workload_by_name(args.workload).dtype == "bf16":
+        args.grad_dtype = "bf16"  # the multiplication-first layers keep their gradients in the activations' dtype
     if args.warmup < 3 and args.impl == "ours" and not args.workload.endswith("-tiny"):
         args.warmup = 3
     rank, world, local_rank = rank_env()

@@ -57,14 +57,17 @@ typedef enum {
     GNN_ENOMEM = 2,       /* device allocation failed */
     GNN_ECUDA = 3,        /* a CUDA runtime call failed */
     GNN_EUNSUPPORTED = 4, /* valid but unsupported shape / dtype */
-    GNN_EINDEX = 5        /* bad index data found on the device */
+    GNN_EINDEX = 5,       /* bad index data found on the device */
+    GNN_ETIMEOUT = 6      /* a kernel's bounded wait ran out: it gave up, and
+                             the outputs of that call are incomplete */
 } gnn_status;
 
 typedef enum { GNN_F32 = 0, GNN_BF16 = 1 } gnn_dtype;
 
 typedef enum {
     GNN_AGG_GCN_SYM = 0,  /* Z[v] = sum_u dinv[v] dinv[u] H[u]  (A_hat = D^-1/2 (A+I) D^-1/2) */
-    GNN_AGG_SAGE_MEAN = 1 /* Z[v] = [ H[v] | mean of H[u] over u in N(v), u != v ] */
+    GNN_AGG_SAGE_MEAN = 1, /* Z[v] = [ H[v] | mean of H[u] over u in N(v), u != v ] */
+    GNN_AGG_GAT = 2        /* graph attention: gnn_gat_forward / gnn_gat_backward */
 } gnn_agg;
 
 /* Create the partition's graph (CAGNET GNN section: A with self loops and its
@@ -78,7 +81,12 @@ typedef enum {
  *           then a local vertex's degree is its row length and a halo
  *           vertex's degree is 1 + the number of times its column occurs.
  *           Degree 0 gives a normalisation factor of 0.  (GCN only; ignored
- *           for GraphSAGE, whose mean counts the entries u != v of row v.)
+ *           for GraphSAGE, whose mean counts the entries u != v of row v, and
+ *           for attention graphs, whose weights are computed per call.)
+ *   agg     the layer kind the graph serves: GCN and GraphSAGE graphs take
+ *           gnn_layer_forward / backward, GNN_AGG_GAT graphs gnn_gat_forward /
+ *           backward (they keep 4 bytes per entry more: where each transpose
+ *           entry's attention sits in the block).
  * The graph copies the CSR, validates it on the device, computes the
  * normalisation, builds the transpose (entries of a transpose row ordered by
  * ascending source row) and the load-balance schedules.  For the aggregation
@@ -184,24 +192,34 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
 /* Backward layer, by the chain rule of the forward above:
  *   dY = relu ? G * 1[H_out > 0] : G      (ReLU'(0) = 0)
  *   dW = Z^T dY                           device float[K x f_out], overwritten
- *   dZ = dY W^T                           device n_local x ld_dz, dtype (work
- *                                         buffer, same layout as Z); needed
- *                                         only when dH != NULL
+ *   dZ = dY W^T                           device n_local x ld_dz, grad_dtype
+ *                                         (work buffer, same layout as Z);
+ *                                         needed only when dH != NULL
  *   dH = A_hat_block^T dZ                 (GCN)
  *   dH[u] = [u local] dZ_self[u] + sum over v with u in N(v), u != v of
  *           dZ_mean[v] / |N(v) \ {v}|     (GraphSAGE)
- *   G      device n_local x ld_g, dtype
+ *   G      device n_local x ld_g, grad_dtype
  *   H_out  device n_local x ld_out, dtype (read only when relu)
- *   dH     device (n_local or n_local + n_halo) x ld_dh, dtype, or NULL to skip
- *          the transposed aggregation (first layer).  want_halo_grad != 0 also
- *          writes the n_halo halo rows (Sylvie Alg. 2: the HALO gradients J
- *          that are sent back to their owners).
+ *   Z      device n_local x ld_z, dtype (as written by gnn_layer_forward)
+ *   dH     device (n_local or n_local + n_halo) x ld_dh, grad_dtype, or NULL to
+ *          skip the transposed aggregation (first layer).  want_halo_grad != 0
+ *          also writes the n_halo halo rows (Sylvie Alg. 2: the HALO gradients
+ *          J that are sent back to their owners).
+ * Precision: `dtype` is that of the activations (H_out, Z), `grad_dtype` that
+ * of the activation gradients (G, dZ, dH).  Accepted pairs: (F32, F32),
+ * (BF16, BF16) and (BF16, F32) - bf16 activations with fp32 gradients; another
+ * pair returns GNN_EINVAL.  With bf16 activations every operand of the
+ * update's products is bf16: Z, W (rounded as in the forward) and dY, which in
+ * the (BF16, F32) pair is rounded to bf16 from the fp32 G; the products
+ * accumulate in fp32 and dZ and dH are stored in fp32, so the transposed
+ * aggregation gathers fp32 rows.  On the tensor cores this pair stages dY in
+ * the graph's workspace (n_local x f_out bf16).
  * dW is summed over rows in a fixed order (deterministic).  Same width limit
- * as gnn_layer_forward. */
+ * as gnn_layer_forward, in bytes of grad_dtype for the aggregation. */
 gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
                               const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out, int relu,
                               float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
-                              gnn_dtype dtype, void *stream);
+                              gnn_dtype dtype, gnn_dtype grad_dtype, void *stream);
 
 /* The same GCN layer with the multiplication first, for layers whose output
  * is narrower than their input (f_out < f_in): A_hat (H W) = (A_hat H) W, so
@@ -222,7 +240,8 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
  *                                        every row (the halo rows are Sylvie's
  *                                        J), or NULL to skip
  * The other arguments are as for gnn_layer_forward / gnn_layer_backward; here
- * the aggregated rows are f_out wide (at most 4096 bytes). */
+ * the aggregated rows are f_out wide (at most 4096 bytes), and every operand,
+ * gradients included, is stored in the one `dtype`. */
 gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
                                     int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
                                     gnn_dtype dtype, void *stream);
@@ -234,12 +253,16 @@ gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, 
 /* Training-harness helper (not a layer step): mean softmax cross-entropy over
  * n rows of C logits with integer labels.
  *   logits  device n x ld, dtype;  labels device int32[n] in [0, C)
- *   G       device n x ld_g, dtype: (softmax - onehot) / n
+ *   G       device n x ld_g, grad_dtype: (softmax - onehot) / n (computed in
+ *           fp32, rounded to grad_dtype); columns past C are not written
  *   row_loss device float[n] work buffer;  loss device float[1]: the mean,
- *   summed in a fixed order.  A label outside [0, C) gives GNN_EINDEX from
- *   the call's return only when checkable; on the device it yields a NaN loss. */
+ *   summed in a fixed order.  A label outside [0, C) yields a NaN loss (the
+ *   labels live on the device and are not checked on the host).
+ * ld and ld_g are multiples of the 16-byte element counts of their dtypes
+ * for the vectorised kernel; other leading dimensions take a slower one. */
 gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream);
+                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, gnn_dtype grad_dtype,
+                          void *stream);
 
 /* As gnn_softmax_ce, but the mean (and the gradient's 1/n) divides by n_mean
  * >= n instead of n: the share of these n rows in the mean over n_mean rows
@@ -247,7 +270,7 @@ gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, 
  * whole mean, and their G together are the gradient of it). */
 gnn_status gnn_softmax_ce_partial(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels,
                                   void *G, int64_t ld_g, float *row_loss, float *loss, int64_t n_mean,
-                                  gnn_dtype dtype, void *stream);
+                                  gnn_dtype dtype, gnn_dtype grad_dtype, void *stream);
 
 /* Halo-gradient return (Sylvie page, backward propagation and Alg. 2: the
  * feature gradients J of a partition's HALO vertices go back to the owning
@@ -269,9 +292,84 @@ gnn_status gnn_halo_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, 
                               const int64_t *local_ids, void *dH, int64_t ld_dh, int64_t f, gnn_dtype dtype,
                               void *stream);
 
-/* Synchronise the device, then return and clear the graph's device error word
- * (GNN_OK or GNN_EINDEX); GNN_ECUDA if the synchronisation itself failed. */
+/* Graph attention layer (GAT) on a graph created with GNN_AGG_GAT.  The
+ * Sylvie page names GAT among the models it trains and the DIGEST page
+ * benchmarks it; neither prints the layer, so this is the textbook
+ * single-head form (no normalisation by degrees):
+ *   T        = H W over every row, local and halo      device (n_local + n_halo) x ld_t, dtype
+ *   s_src[u] = T[u] . a_src (every row),  s_dst[v] = T[v] . a_dst (local rows)
+ *              scores: device float[2 n_local + n_halo] = s_src then s_dst
+ *   alpha_vu = softmax over the entries u of row v of LeakyReLU_0.2(s_dst[v] + s_src[u])
+ *              alpha: device float[nnz], in the library's entry order, with the
+ *              sign bit of each row's last entry set (kept for the backward)
+ *   H_out[v] = relu ? max(sum_u alpha_vu T[u], 0) : sum_u alpha_vu T[u]
+ *              device n_local x ld_out, dtype
+ * W device float[f_in x f_out] (rounded to bf16 for the bf16 path);
+ * a_src, a_dst device float[f_out].  The aggregated rows T are at most 4096
+ * bytes wide.  GNN_EINVAL for a graph of another kind. */
+gnn_status gnn_gat_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
+                           const float *a_src, const float *a_dst, int64_t f_out, int relu, void *T, int64_t ld_t,
+                           float *scores, float *alpha, void *H_out, int64_t ld_out, gnn_dtype dtype, void *stream);
+
+/* Backward of gnn_gat_forward, by the chain rule:
+ *   dY        = relu ? G * 1[H_out > 0] : G
+ *   de_vu     = alpha_vu (dY[v] . T[u] - sum_u' alpha_vu' dY[v] . T[u'])
+ *   dz_vu     = de_vu (s_dst[v] + s_src[u] > 0 ? 1 : 0.2)
+ *   ds_dst[v] = sum_u dz_vu,   ds_src[u] = sum over entries (v, u) of dz_vu
+ *   dT[u]     = sum over entries (v, u) of alpha_vu dY[v] + ds_src[u] a_src
+ *               + [u local] ds_dst[u] a_dst          device (n_local + n_halo) x ld_dt, grad_dtype (written)
+ *   da_src    = sum_u ds_src[u] T[u],  da_dst = sum_v ds_dst[v] T[v]   device float[f_out]
+ *   dW        = H^T dT                                device float[f_in x f_out]
+ *   dH        = dT W^T over every row (the halo rows are Sylvie's J)
+ *               device (n_local + n_halo) x ld_dh, grad_dtype, or NULL to skip
+ * G device n_local x ld_g, grad_dtype; H_out, H, T, scores and alpha as the
+ * forward used or wrote them.  Precision pairs as for gnn_layer_backward; with
+ * bf16 activations dT enters the products as bf16.  Every sum is formed in a
+ * fixed order (reproducible bits).  The workspace grows by about 8 bytes per
+ * entry plus the staging of dY (and of dT in bf16). */
+gnn_status gnn_gat_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                            const void *H, int64_t ld_h, int64_t f_in, const float *W, const float *a_src,
+                            const float *a_dst, int64_t f_out, int relu, const void *T, int64_t ld_t,
+                            const float *scores, const float *alpha, float *dW, float *da_src, float *da_dst,
+                            void *dT, int64_t ld_dt, void *dH, int64_t ld_dh, gnn_dtype dtype, gnn_dtype grad_dtype,
+                            void *stream);
+
+/* Rows of the halo exchange between processes (Sylvie page, Graph Engine and
+ * Alg. 1 / Alg. 2: each partition sends the rows of its vertices that other
+ * partitions hold as HALO vertices, and in the backward pass receives the
+ * gradients J of those rows back).  No graph is involved: these are the
+ * packing and unpacking steps around a collective (all-to-all) that moves the
+ * rows between partitions.
+ * Gather: dst[i, 0:f] = src[ids[i], 0:f] for i < n (bit-exact copy).
+ *   src  device n_src x ld_src, dtype;  ids device int64[n];  dst device n x ld_dst.
+ * Scatter-add: dst[ids[i], 0:f] += src[i, 0:f] for i < n, summed in fp32 and
+ *   stored as dtype.  The ids of one call must be distinct (rows added by one
+ *   call must not collide; several calls on one stream add in call order, so
+ *   sums are reproducible).  src device n x ld_src; dst device n_dst x ld_dst.
+ * An id outside the rows of its matrix leaves that row alone and, when err
+ * (device int, nullable) is given, sets bit 0 of *err.  Host-checkable
+ * argument errors return GNN_EINVAL. */
+gnn_status gnn_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const int64_t *ids, int64_t n, void *dst,
+                           int64_t ld_dst, int64_t f, gnn_dtype dtype, int *err, void *stream);
+gnn_status gnn_scatter_add_rows(const void *src, int64_t ld_src, const int64_t *ids, int64_t n, void *dst,
+                                int64_t ld_dst, int64_t n_dst, int64_t f, gnn_dtype dtype, int *err, void *stream);
+
+/* Synchronise the device, then return and clear the graph's device error word:
+ * GNN_OK, GNN_ETIMEOUT (a kernel of one of the graph's calls gave up on a
+ * bounded wait - every wait on the device gives up after about 2 s, records
+ * this and returns instead of spinning), or GNN_EINDEX (bad index data);
+ * GNN_ECUDA if the synchronisation itself failed. */
 gnn_status gnn_get_error(gnn_graph *g);
+
+/* Failure-detection test hook (not a step of the method): arms a one-shot
+ * fault in the next aggregation launched by this process, on any graph.  The
+ * first batch of that launch's first producer / consumer warp pair is never
+ * issued, so its consumer's bounded wait runs out after wait_ns nanoseconds
+ * (> 0): the kernel raises its abort flag, the other warps of the block stop,
+ * every gather already issued is waited for, and the launch returns; the
+ * call's graph then reports GNN_ETIMEOUT through gnn_get_error.  Nothing faults
+ * and the context stays usable.  wait_ns <= 0 disarms the hook. */
+gnn_status gnn_debug_expire_next_wait(int64_t wait_ns);
 
 /* Sizes of a graph (host outputs, any may be NULL). */
 gnn_status gnn_graph_sizes(const gnn_graph *g, int64_t *n_local, int64_t *n_halo, int64_t *nnz);

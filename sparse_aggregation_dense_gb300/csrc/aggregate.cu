@@ -11,22 +11,24 @@
 // The column factors live in per-entry weights built with the graph, so the
 // kernel streams (column id, weight) pairs and gathers feature rows.
 //
-// Design (a gather bound by memory latency and DRAM traffic):
-//  - work items: row groups (runs of consecutive light rows, <= kHeavyNnz
-//    entries each, whose entries form one range) and kChunkNnz-entry chunks of
-//    heavy rows; chunks are scheduled first so hub rows spread over all SMs; a
-//    chunk writes an fp32 partial and a fix-up adds a heavy row's partials in
-//    chunk order (deterministic, no atomics);
-//  - a warp streams an item's entries in batches that may span rows; the 32
-//    lanes split a feature row into VW-byte pieces (VPT boxes of 32 * VW bytes)
-//    and walk the batch entry by entry, writing each row out where it ends;
-//  - the gathers are TMA gathers of four rows (tile::gather4) into a per-warp
-//    shared-memory ring of NS slots (a slot: BE entries), completed on one
-//    mbarrier per slot; the warp consumes one slot while the next NS - 1 are
-//    in flight, and the next 64 column ids sit in registers, fetched ahead;
+// Design (a gather bound by DRAM traffic and by instruction issue):
+//  - work items: row groups (runs of consecutive non-empty light rows, <=
+//    kHeavyNnz entries each, whose entries form one range) and kChunkNnz-entry
+//    chunks of heavy rows; chunks are scheduled first so hub rows spread over
+//    all SMs; a chunk writes an fp32 partial and a fix-up adds a heavy row's
+//    partials in chunk order (deterministic, no atomics); the fix-up also
+//    writes the empty rows;
+//  - each item's entries stream through a producer / consumer warp pair in
+//    batches that may span rows: the producer issues TMA gathers of four rows
+//    (tile::gather4) into the pair's shared-memory ring, the consumer only
+//    waits, loads from shared memory, multiplies-adds and writes rows out; the
+//    end of a row is the sign bit of its last entry's weight (set at graph
+//    creation), so the consumer never walks row pointers;
 //  - L2 residency: column ids carry a hotness tier (access-count rank); rows
 //    of the hottest tiers that fit a share of L2 are loaded with an evict_last
 //    policy, the rest and the streamed ids / weights / outputs with evict_first.
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "gnn_internal.cuh"
@@ -169,15 +171,19 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
-// Shared memory of one warp: NS slots of BE gathered rows (R bytes each), the
-// entries' weights (each stored twice, as a packed-FMA operand) and one
-// mbarrier per slot.  A slot is laid out box-major:
-// box v (bytes [v * LPG * 16, (v + 1) * LPG * 16) of every row) holds the BE
-// rows one after another, as the TMA gathers deliver them.
+// Shared memory of one producer / consumer pair: NS slots, each holding BE
+// gathered rows (R bytes each), then the slots' weights (each stored twice, as
+// a packed-FMA operand), their row-end masks, and a "full" and an "empty"
+// mbarrier per slot.  A slot is laid out box-major: box v (bytes
+// [v * 32 * VW, (v + 1) * 32 * VW) of every row) holds the BE rows one after
+// another, as the TMA gathers deliver them.
 template <int R, int BE, int NS>
-struct BulkRing {
-    static constexpr int kRowBytes = NS * BE * R;
-    static constexpr int kBytes = kRowBytes + NS * BE * 8 + NS * 8;  // rows, weight pairs, mbarriers
+struct PairRing {
+    static constexpr int kSlotBytes = BE * R;
+    static constexpr int kWeightOff = NS * kSlotBytes;                 // NS x BE weight pairs
+    static constexpr int kMaskOff = kWeightOff + NS * BE * 8;          // NS row-end masks
+    static constexpr int kBarOff = (kMaskOff + NS * 4 + 7) / 8 * 8;    // NS full, then NS empty mbarriers
+    static constexpr int kBytes = (kBarOff + 2 * NS * 8 + 127) / 128 * 128;  // the next pair's rows stay 128-aligned
 };
 
 // One work item: a row group (consecutive light rows, one entry range) or one
@@ -362,29 +368,48 @@ __device__ __forceinline__ bool next_work_item(int64_t &it, Item &x, int64_t W, 
     }
 }
 
-// lane j: column id (tier bits kept) and weight of entry base + j of item x
-__device__ __forceinline__ void fetch_window(const Item &x, bool valid, int32_t base,
-                                             const uint32_t *__restrict__ colidx, const float *__restrict__ wts,
-                                             int lane, uint64_t pol, uint32_t &c, float &w) {
-    c = 0;
-    w = 0.f;
-    if (valid && base + lane < x.e - x.b) {
-        c = ld_stream_u32(colidx + x.b + base + lane, pol);
-        w = __uint_as_float(ld_stream_u32(wts + x.b + base + lane, pol));
+// bounded wait of one warp: every lane polls the barrier; the warp gives up
+// together when any lane's wait ran out (after ~2 s) or, with a flag, when the
+// CTA's abort flag is raised
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t limit_ns) {
+    bool ok = bar_try(bar, parity);
+    if (!__all_sync(0xffffffffu, ok)) {
+        uint64_t t0;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+        for (;;) {
+            ok = bar_try(bar, parity);
+            if (__all_sync(0xffffffffu, ok)) break;
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            const bool give_up = (abort && *abort) || t - t0 > limit_ns;
+            if (__any_sync(0xffffffffu, give_up)) return false;
+        }
     }
+    return true;
 }
 
-// Persistent warps: warp w of W handles items w, w + W, ... as one stream of
-// batches (a batch: up to BE consecutive entries of one item, which may span
-// several rows of a row group).  Lane j of a batch holds entry j's column id
-// and weight; every fourth lane gathers its four entries' rows with one TMA
-// gather per box into the warp's slot (a short last group repeats its last
-// row, weighted 0).  The consume side, NS - 1 batches behind, walks the
-// batch's entries in order: it accumulates runs of entries of one row and
-// writes a row out (or, for a chunk of a heavy row, its fp32 partial) where
-// the row ends.  Each lane owns VW bytes of each of the VPT boxes of a row.
-template <typename T, int VW, int VPT, int BE, int NS, int WPC>
-__global__ void __launch_bounds__(WPC * 32)
+__device__ __forceinline__ void bar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                 : "memory");
+}
+
+// Producer / consumer warp pairs.  Pair q of P handles work items q, q + P, ...
+// (row groups and heavy-row chunks) as one stream of batches of up to BE
+// consecutive entries of one item.
+//  - The producer warp reads an item's column ids and weights 32 entries at a
+//    time (lane j: entry j), takes the row ends from the weights' sign bits and
+//    the L2 policy of each group of four rows from their hotness tiers, then
+//    per batch: waits for the slot to be free, stores the weights and the
+//    row-end mask, and issues one TMA gather of four rows per group and box.
+//  - The consumer warp waits for the batch, accumulates its entries (each lane
+//    owns VW bytes of each of the VPT boxes of a row; packed fp32x2 FMA on
+//    64-bit accumulator pairs), writes a row out at each marked row end (a
+//    chunk of a heavy row writes its fp32 partial at the chunk's end instead),
+//    and frees the slot.
+// The consumer never reads row pointers or column ids: a group's rows are
+// consecutive and non-empty, so its k-th row end is row r0 + k.
+template <typename T, int VW, int VPT, int BE, int NS, int PPC, int MINB>
+__global__ void __launch_bounds__(PPC * 64, MINB)
     aggregate_kernel(const AggParams p, const __grid_constant__ CUtensorMap xmap, const int32_t *__restrict__ chunk_row,
                      const int32_t *__restrict__ chunk_begin, const int32_t *__restrict__ chunk_end, int64_t n_chunks,
                      const int32_t *__restrict__ group_r0, const int32_t *__restrict__ group_r1, int64_t n_groups,
@@ -393,118 +418,115 @@ __global__ void __launch_bounds__(WPC * 32)
     constexpr int BOX = 32 * VW;              // bytes of one gathered box of a row
     constexpr int R = VPT * BOX;
     static_assert(VW == 4 || VW == 8 || VW == 16, "lane piece of 4, 8 or 16 bytes");
-    static_assert(BE <= 32 && BE % 4 == 0 && 32 % BE == 0, "whole groups of four entries inside one id window");
+    static_assert(BE == 4 || BE == 8 || BE == 16, "batches of whole groups of four inside one 32-entry window");
     static_assert(BOX % 128 == 0, "TMA destinations stay 128-byte aligned");
-    using Ring = BulkRing<R, BE, NS>;
+    using Ring = PairRing<R, BE, NS>;
+    constexpr uint32_t kBatchMask = (1u << BE) - 1u;
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ int abort_flag;
     // TMA destinations must be 128-byte aligned: round the dynamic base up
     // (the launch adds 128 bytes for this)
-    uint8_t *smem_bulk = smem_raw + ((128u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 127u)) & 127u);
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    uint8_t *rows = smem_bulk + wib * Ring::kRowBytes;
-    unsigned long long *wring =
-        reinterpret_cast<unsigned long long *>(smem_bulk + WPC * Ring::kRowBytes) + wib * NS * BE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_bulk + WPC * Ring::kRowBytes + WPC * NS * BE * 8) + wib * NS;
+    uint8_t *smem = smem_raw + ((128u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 127u)) & 127u);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool producer = warp >= PPC;
+    const int pair = producer ? warp - PPC : warp;
+    uint8_t *rows = smem + pair * Ring::kBytes;
+    unsigned long long *wring = reinterpret_cast<unsigned long long *>(rows + Ring::kWeightOff);
+    uint32_t *emask = reinterpret_cast<uint32_t *>(rows + Ring::kMaskOff);
+    uint64_t *full = reinterpret_cast<uint64_t *>(rows + Ring::kBarOff);
+    uint64_t *empty = full + NS;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (!producer && lane == 0)
+        for (int s = 0; s < NS; ++s) {
+            bar_init(&full[s]);
+            bar_init(&empty[s]);
+        }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
 
-    const int64_t W = (int64_t)gridDim.x * WPC;
-    const int64_t w0 = (int64_t)blockIdx.x * WPC + wib;
+    const int64_t P = (int64_t)gridDim.x * PPC;
+    const int64_t q0 = (int64_t)blockIdx.x * PPC + pair;
     const int64_t n_items = n_chunks + n_groups;
-    const uint64_t pol_keep = policy_evict_last();
-    const uint64_t pol_stream = policy_evict_first();
-    const T *__restrict__ X = static_cast<const T *>(p.X);
-    const int64_t f = p.f, ldx = p.ldx;
-    const uint32_t *__restrict__ colidx = p.colidx;
-    const float *__restrict__ wts = p.wts;
-    const uint32_t colmask = p.colmask;
-    const int hot_tier = p.hot_tier;
     const int32_t *__restrict__ rowptr = p.rowptr;
     const int64_t n_rows = p.n_rows;
 
-    if (lane == 0)
-        for (int s = 0; s < NS; ++s) bar_init(&bars[s]);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncwarp();
-
-    // ---- issue side ----
-    // The column ids and weights of the next 64 entries of the current item
-    // sit in registers (lane j holds entry wb + j in (ic0, iw0) and wb + 32 + j
-    // in (ic1, iw1)); the next item with its first 32 ids is fetched one item
-    // ahead.  Issuing a batch therefore never waits on an index load.
-    Item ci = Item{0, 0, 0, 0, false, true}, ni = Item{0, 0, 0, 0, false, true};
-    int64_t it_i = w0 - W;
-    bool more = next_work_item(it_i, ci, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1,
-                               rowptr, n_rows);
-    int64_t it_n = it_i;
-    bool nmore = more && next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0,
-                                        group_r1, rowptr, n_rows);
-    int32_t off_i = 0, wb = 0;
-    uint32_t ic0, ic1, nc0;
-    float iw0, iw1, nw0;
-    fetch_window(ci, more, 0, colidx, wts, lane, pol_stream, ic0, iw0);
-    fetch_window(ci, more, 32, colidx, wts, lane, pol_stream, ic1, iw1);
-    fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);
-    uint32_t s_i = 0;
-    bool ok = true;
-
-#define GNN_ISSUE_BATCH()                                                                                   \
-    do {                                                                                                    \
-        if (!more) break;                                                                                   \
-        const int slot = (int)(s_i % NS);                                                                   \
-        const int32_t n_ci = ci.e - ci.b;                                                                   \
-        const int32_t left = n_ci - off_i;                                                                  \
-        const int cnt = left < BE ? left : BE;                                                              \
-        /* lanes past the batch repeat its last entry: a valid row, weight 0 */                           \
-        const int src = (off_i - wb + (lane < cnt ? lane : cnt - 1)) & 31;                                  \
-        const uint32_t raw = __shfl_sync(0xffffffffu, ic0, src);                                            \
-        const float wv = __shfl_sync(0xffffffffu, iw0, src);                                                \
-        if (lane < BE) {                                                                                    \
-            const uint32_t wb32 = __float_as_uint(lane < cnt ? wv : 0.f);                                   \
-            wring[slot * BE + lane] = ((unsigned long long)wb32 << 32) | wb32;                              \
-        }                                                                                                   \
-        const int32_t col = (int32_t)(raw & colmask);                                                       \
-        const int tier = colmask == kColMask ? (int)(raw >> kTierShift) : 0;                                \
-        const uint32_t hot = __ballot_sync(0xffffffffu, lane < cnt && tier <= hot_tier);                    \
-        const int32_t c1 = __shfl_down_sync(0xffffffffu, col, 1);                                           \
-        const int32_t c2 = __shfl_down_sync(0xffffffffu, col, 2);                                           \
-        const int32_t c3 = __shfl_down_sync(0xffffffffu, col, 3);                                           \
-        const int ngr = (cnt + 3) >> 2;                                                                     \
-        if (lane == 0) bar_expect(&bars[slot], (uint32_t)(ngr * VPT * 4 * BOX));                            \
-        __syncwarp();                                                                                       \
-        if ((lane & 3) == 0 && lane < 4 * ngr) {                                                            \
-            /* keep the group in L2 when most of its rows are hot */                                        \
-            const uint64_t pol = __popc((hot >> lane) & 0xfu) >= 2 ? pol_keep : pol_stream;                 \
-            uint8_t *dst = rows + slot * BE * R + lane * BOX;                                               \
-            _Pragma("unroll") for (int v = 0; v < VPT; ++v)                                                \
-                tma_gather4(dst + v * BE * BOX, &xmap, v * (BOX / (int)sizeof(T)), col, c1, c2, c3,         \
-                            &bars[slot], pol);                                                              \
-        }                                                                                                   \
-        ++s_i;                                                                                              \
-        off_i += BE;                                                                                        \
-        if (off_i >= n_ci) {                                                                                \
-            more = nmore;                                                                                   \
-            if (more) {                                                                                     \
-                ci = ni;                                                                                    \
-                off_i = 0;                                                                                  \
-                wb = 0;                                                                                     \
-                ic0 = nc0;                                                                                  \
-                iw0 = nw0;                                                                                  \
-                fetch_window(ci, true, 32, colidx, wts, lane, pol_stream, ic1, iw1);                        \
-                nmore = next_work_item(it_n, ni, W, n_items, n_chunks, chunk_row, chunk_begin, chunk_end,   \
-                                       group_r0, group_r1, rowptr, n_rows);                                 \
-                fetch_window(ni, nmore, 0, colidx, wts, lane, pol_stream, nc0, nw0);                        \
-            }                                                                                               \
-        } else if (off_i >= wb + 32) {                                                                      \
-            wb += 32;                                                                                       \
-            ic0 = ic1;                                                                                      \
-            iw0 = iw1;                                                                                      \
-            fetch_window(ci, true, wb + 32, colidx, wts, lane, pol_stream, ic1, iw1);                      \
-        }                                                                                                   \
-    } while (0)
-
+    if (producer) {
+        const uint64_t pol_keep = policy_evict_last();
+        const uint64_t pol_stream = policy_evict_first();
+        const uint32_t *__restrict__ colidx = p.colidx;
+        const float *__restrict__ wts = p.wts;
+        const uint32_t colmask = p.colmask;
+        const bool tagged = colmask == kColMask;
+        const int hot_tier = p.hot_tier;
+        uint32_t s_i = 0;
+        bool ok = true;
+        Item x;
+        int64_t it = q0 - P;
 #pragma unroll 1
-    for (int s = 0; s < NS; ++s) GNN_ISSUE_BATCH();
+        while (ok && next_work_item(it, x, P, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1,
+                                    rowptr, n_rows)) {
+            const int32_t n = x.e - x.b;
+#pragma unroll 1
+            for (int32_t wb = 0; wb < n && ok; wb += 32) {
+                const int nb = n - wb < 32 ? n - wb : 32;  // entries of this window
+                const bool valid = lane < nb;
+                uint32_t raw = 0, wbits = 0;
+                if (valid) {
+                    raw = ld_stream_u32(colidx + x.b + wb + lane, pol_stream);
+                    wbits = ld_stream_u32(wts + x.b + wb + lane, pol_stream);
+                }
+                const uint32_t ends = __ballot_sync(0xffffffffu, wbits >> 31);  // last entries of rows
+                const uint32_t wa = wbits & 0x7fffffffu;
+                const int tier = tagged ? (int)(raw >> kTierShift) : 0;
+                const uint32_t hot = __ballot_sync(0xffffffffu, valid && tier <= hot_tier);
+                // lanes past the window's entries repeat its last entry: a valid row (its weight is 0)
+                const int32_t col = (int32_t)(__shfl_sync(0xffffffffu, raw, valid ? lane : nb - 1) & colmask);
+                const int32_t c1 = __shfl_down_sync(0xffffffffu, col, 1);
+                const int32_t c2 = __shfl_down_sync(0xffffffffu, col, 2);
+                const int32_t c3 = __shfl_down_sync(0xffffffffu, col, 3);
+#pragma unroll 1
+                for (int k0 = 0; k0 < nb; k0 += BE) {
+                    const int slot = (int)(s_i % NS);
+                    if (!warp_wait(&empty[slot], ((s_i / NS) & 1u) ^ 1u, &abort_flag, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const int cnt = nb - k0 < BE ? nb - k0 : BE;
+                    if (lane >= k0 && lane < k0 + BE)
+                        wring[slot * BE + (lane - k0)] = ((unsigned long long)wa << 32) | wa;
+                    if (lane == 0) emask[slot] = (ends >> k0) & kBatchMask;
+                    const int ngr = (cnt + 3) >> 2;
+                    __syncwarp();
+                    // the arrive releases the weights and the mask; the gathers complete the phase
+                    if (lane == 0) bar_expect(&full[slot], (uint32_t)(ngr * VPT * 4 * BOX));
+                    __syncwarp();
+                    const bool starved = p.starve && q0 == 0 && s_i == 0;  // failure test: never issued
+                    if ((lane & 3) == 0 && lane >= k0 && lane < k0 + 4 * ngr && !starved) {
+                        // keep the group in L2 when most of its rows are hot
+                        const uint64_t pol = __popc((hot >> lane) & 0xfu) >= 2 ? pol_keep : pol_stream;
+                        uint8_t *dst = rows + slot * Ring::kSlotBytes + (lane - k0) * BOX;
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v)
+                            tma_gather4(dst + v * BE * BOX, &xmap, v * (BOX / (int)sizeof(T)), col, c1, c2, c3,
+                                        &full[slot], pol);
+                    }
+                    ++s_i;
+                }
+            }
+        }
+        if (!ok) {
+            // the consumer gave up: let the gathers still in flight land (bounded)
+            // before the CTA's shared memory is released
+            for (uint32_t k = s_i > (uint32_t)NS ? s_i - NS : 0u; k < s_i; ++k)
+                if (!(p.starve && q0 == 0 && k == 0)) warp_wait(&full[k % NS], (k / NS) & 1u, nullptr, p.wait_ns);
+        }
+        return;
+    }
 
-    // ---- consume side ----
+    // ---- consumer ----
+    const T *__restrict__ X = static_cast<const T *>(p.X);
+    const int64_t f = p.f, ldx = p.ldx;
+    const uint64_t pol_out = policy_evict_first();
     const int64_t f_store = (f * (int64_t)sizeof(T) + 15) / 16 * 16 / (int64_t)sizeof(T);  // f, padded to 16 bytes
     constexpr int NP = Lane<T, VW>::kPairs;
     unsigned long long acc[VPT][NP];
@@ -512,155 +534,131 @@ __global__ void __launch_bounds__(WPC * 32)
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
-    uint32_t s_c = 0;
-#pragma unroll 1
-    for (int64_t it_c = w0; it_c < n_items && ok; it_c += W) {
-        const Item x =
-            load_item(it_c, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1, rowptr, n_rows);
-        if (x.skip) continue;
-        // rows [wbase, wbase + 32) of a group: lane i holds row wbase + i's end
-        // entry and its scale
-        int32_t r = x.r0, wbase = x.r0, rwin = x.e;
-        float swin = 1.f;
-        auto load_rows = [&](int32_t base) {
-            wbase = base;
-            rwin = x.e;
-            swin = 1.f;
-            if (!x.chunk && base + lane < x.r1) {
-                rwin = rowptr[base + lane + 1];
-                if (p.rowscale) swin = __ldg(p.rowscale + base + lane);
-            }
-        };
-        load_rows(x.r0);
-        int32_t rend = x.chunk ? x.e : __shfl_sync(0xffffffffu, rwin, 0);
-        // write row r (or the chunk's partial) and clear the accumulator
-        auto finish_row = [&]() {
-            if (r - wbase >= 32) load_rows(r);
-            if (x.chunk) {
-                float *dst = partial + it_c * pld;
+    // per-row scales of a group, prefetched 32 rows at a time into the lanes
+    // (lane i holds the scale of row sbase + i; the next 32 wait in snext)
+    int32_t sbase = 0;
+    float swin = 1.f, snext = 1.f;
+    auto load_scales = [&](int32_t base, int32_t r1, float &dst) {
+        dst = 1.f;
+        if (p.rowscale && base + lane < r1) dst = __ldg(p.rowscale + base + lane);
+    };
+    // write row r of the output and clear the accumulator
+    auto finish_row = [&](int32_t r, int32_t r1) {
+        if (r - sbase >= 32) {  // rows run into the next window of 32
+            sbase += 32;
+            swin = snext;
+            load_scales(sbase + 32, r1, snext);
+        }
+        const float scale = __shfl_sync(0xffffffffu, swin, r - sbase);
+        T *out = static_cast<T *>(p.out) + (int64_t)r * p.ldo;
+        const T *selfrow = nullptr;
+        if (p.self_mode == SELF_COPY) selfrow = X + (int64_t)r * ldx;
+        if (p.self_mode == SELF_ADD && r < p.n_self) selfrow = static_cast<const T *>(p.self) + (int64_t)r * p.ld_self;
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
-                    if (c0 < pld) {
-                        float a[EPL];
-                        pairs_to_vals<T, VW>(acc[v], a);
+        for (int v = 0; v < VPT; ++v) {
+            const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
+            if (c0 < f_store) {
+                const int f_left = (int)(f - c0 < EPL ? f - c0 : EPL);
+                float o[EPL];
+                pairs_to_vals<T, VW>(acc[v], o);
 #pragma unroll
-                        for (int k = 0; k < EPL; ++k) dst[c0 + k] = a[k];
-                    }
-                }
-            } else {
-                const float scale = __shfl_sync(0xffffffffu, swin, r - wbase);
-                T *out = static_cast<T *>(p.out) + (int64_t)r * p.ldo;
-                const T *selfrow = nullptr;
-                if (p.self_mode == SELF_COPY) selfrow = X + (int64_t)r * ldx;
-                if (p.self_mode == SELF_ADD && r < p.n_self)
-                    selfrow = static_cast<const T *>(p.self) + (int64_t)r * p.ld_self;
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
-                    if (c0 >= f_store) continue;
-                    const int f_left = (int)(f - c0 < EPL ? f - c0 : EPL);
-                    float o[EPL];
-                    pairs_to_vals<T, VW>(acc[v], o);
-#pragma unroll
-                    for (int k = 0; k < EPL; ++k) o[k] *= scale;
-                    if (selfrow) {
-                        uint32_t q[VW / 4];
-                        float sv[EPL];
-                        ldg_words<VW>(selfrow + c0, q);
-                        words_to_vals<T, VW>(q, sv);
-                        if (p.self_mode == SELF_ADD) {
-#pragma unroll
-                            for (int k = 0; k < EPL; ++k) o[k] += sv[k];
-                        } else {
-                            vals_to_words<T, VW>(sv, f_left, q);
-                            stg_words<VW>(out + c0, q, pol_stream);
-                        }
-                    }
-                    if (p.relu) {
-#pragma unroll
-                        for (int k = 0; k < EPL; ++k) o[k] = o[k] > 0.f ? o[k] : 0.f;
-                    }
+                for (int k = 0; k < EPL; ++k) o[k] *= scale;
+                if (selfrow) {
                     uint32_t q[VW / 4];
-                    vals_to_words<T, VW>(o, f_left, q);
-                    stg_words<VW>(out + p.out_off + c0, q, pol_stream);
+                    float sv[EPL];
+                    ldg_words<VW>(selfrow + c0, q);
+                    words_to_vals<T, VW>(q, sv);
+                    if (p.self_mode == SELF_ADD) {
+#pragma unroll
+                        for (int k = 0; k < EPL; ++k) o[k] += sv[k];
+                    } else {
+                        vals_to_words<T, VW>(sv, f_left, q);
+                        stg_words<VW>(out + p.self_off + c0, q, pol_out);
+                    }
                 }
+                if (p.relu) {
+#pragma unroll
+                    for (int k = 0; k < EPL; ++k) o[k] = o[k] > 0.f ? o[k] : 0.f;
+                }
+                uint32_t q[VW / 4];
+                vals_to_words<T, VW>(o, f_left, q);
+                stg_words<VW>(out + p.out_off + c0, q, pol_out);
             }
 #pragma unroll
-            for (int v = 0; v < VPT; ++v)
-#pragma unroll
-                for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
-        };
-        int32_t pos = x.b;
+            for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
+        }
+    };
+    uint32_t s_c = 0;
+    bool ok = true;
 #pragma unroll 1
-        for (int32_t off = 0; off < x.e - x.b; off += BE) {
+    for (int64_t it = q0; it < n_items && ok; it += P) {
+        const Item x = load_item(it, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1, rowptr, n_rows);
+        if (x.skip || x.e <= x.b) continue;
+        int32_t r = x.r0;
+        const int32_t n = x.e - x.b;
+        if (!x.chunk) {
+            sbase = x.r0;
+            load_scales(x.r0, x.r1, swin);
+            load_scales(x.r0 + 32, x.r1, snext);
+        }
+#pragma unroll 1
+        for (int32_t off = 0; off < n; off += BE) {
             const int slot = (int)(s_c % NS);
-            if (!bar_wait(&bars[slot], (s_c / NS) & 1u)) {
+            if (!warp_wait(&full[slot], (s_c / NS) & 1u, &abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
             }
-            const int32_t left = x.e - x.b - off;
-            const int cnt = left < BE ? left : BE;
-            const uint8_t *sr = rows + slot * BE * R + lane * VW;  // this lane's piece of the slot's first row
+            const int cnt = n - off < BE ? n - off : BE;
+            const uint8_t *sr = rows + slot * Ring::kSlotBytes + lane * VW;  // this lane's piece of the first row
             const unsigned long long *ws = wring + slot * BE;
-            if (cnt == BE && rend - pos >= BE) {
-                // the whole batch lies in the current row
+            const uint32_t em = x.chunk ? 0u : emask[slot];
+            if (em == 0u) {
+                if (cnt == BE) {
 #pragma unroll
-                for (int k = 0; k < BE; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
-                pos += BE;
+                    for (int k = 0; k < BE; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
+                } else {
+#pragma unroll 1
+                    for (int k = 0; k < cnt; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
+                }
             } else {
-                int j = 0;
-#pragma unroll 1
-                while (j < cnt) {
-                    // rows that end here (empty rows too) are written out first
-#pragma unroll 1
-                    while (pos == rend) {
-                        finish_row();
-                        ++r;
-                        if (r - wbase >= 32) load_rows(r);
-                        rend = __shfl_sync(0xffffffffu, rwin, r - wbase);
+#pragma unroll
+                for (int k = 0; k < BE; ++k) {
+                    if (k < cnt) {
+                        accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
+                        if (em & (1u << k)) finish_row(r++, x.r1);
                     }
-                    const int run = rend - pos < cnt - j ? rend - pos : cnt - j;
-                    const uint8_t *rp = sr + j * BOX;
-                    const unsigned long long *wp = ws + j;
-                    if constexpr (VPT <= 2) {
-                        // short rows: the run two entries at a time, then the odd one
-                        int k = run;
-#pragma unroll 1
-                        for (; k >= 2; k -= 2, rp += 2 * BOX, wp += 2) {
-                            accumulate_entry<T, VW, VPT, BE>(acc, rp, wp[0]);
-                            accumulate_entry<T, VW, VPT, BE>(acc, rp + BOX, wp[1]);
-                        }
-                        if (k) accumulate_entry<T, VW, VPT, BE>(acc, rp, wp[0]);
-                    } else {
-#pragma unroll 1
-                        for (int k = 0; k < run; ++k) accumulate_entry<T, VW, VPT, BE>(acc, rp + k * BOX, wp[k]);
-                    }
-                    j += run;
-                    pos += run;
                 }
             }
-            ++s_c;
-            __syncwarp();
-            // the slot's rows were read through the generic proxy; the next
-            // TMA gather into it is an async-proxy write
+            // the slot was read through the generic proxy; the next gathers into it
+            // are async-proxy writes
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            GNN_ISSUE_BATCH();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&empty[slot]);
+            ++s_c;
         }
         if (!ok) break;
-        // the last row, then any empty rows after it
-#pragma unroll 1
-        while (r < x.r1) {
-            finish_row();
-            ++r;
+        if (x.chunk) {
+            float *dst = partial + it * pld;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int64_t c0 = (int64_t)(v * 32 + lane) * EPL;
+                if (c0 < pld) {
+                    float a[EPL];
+                    pairs_to_vals<T, VW>(acc[v], a);
+#pragma unroll
+                    for (int k = 0; k < EPL; ++k) dst[c0 + k] = a[k];
+                }
+#pragma unroll
+                for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
+            }
         }
     }
-#undef GNN_ISSUE_BATCH
     if (!ok) {
-        // a copy never completed: report, then let every copy still in flight
-        // land (bounded) before the warp's shared memory is released
-        if (lane == 0 && p.err) atomicOr(p.err, 4);
-        for (uint32_t s = s_c; s < s_i; ++s) bar_wait(&bars[s % NS], (s / NS) & 1u);
+        // a batch never arrived: report and make the producer stop
+        if (lane == 0) {
+            abort_flag = 1;
+            if (p.err) atomicOr(p.err, kErrWaitAgg);
+        }
     }
 }
 
@@ -707,7 +705,7 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
                 if (col + 1 >= f) sv.y = 0.f;
                 if (col + 2 >= f) sv.z = 0.f;
                 if (col + 3 >= f) sv.w = 0.f;
-                store4(out + col, sv);
+                store4(out + p.self_off + col, sv);
             }
         }
         if (p.relu) {
@@ -724,27 +722,27 @@ __global__ void __launch_bounds__(256) aggregate_fixup_kernel(const AggParams p,
     }
 }
 
-template <typename T, int VW, int VPT, int BE, int NS, int WPC>
+template <typename T, int VW, int VPT, int BE, int NS, int PPC, int MINB>
 gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
     const int64_t items = sc.n_chunks + sc.n_groups;
     if (items > 0) {
         constexpr int R = 32 * VW * VPT;
-        const int smem = WPC * BulkRing<R, BE, NS>::kBytes + 128;
+        const int smem = PPC * PairRing<R, BE, NS>::kBytes + 128;
         // the gathered matrix, one row high boxes of 32 * VW bytes (zero past column f)
         CUtensorMap xmap;
         memset(&xmap, 0, sizeof(xmap));
         if (p.n_x > 0 && !make_map_rows(&xmap, sizeof(T) == 2, p.X, (uint64_t)p.f, (uint64_t)p.n_x,
                                         (uint64_t)p.ldx * sizeof(T), (uint32_t)(32 * VW / (int)sizeof(T))))
             return GNN_ECUDA;
-        auto kern = aggregate_kernel<T, VW, VPT, BE, NS, WPC>;
+        auto kern = aggregate_kernel<T, VW, VPT, BE, NS, PPC, MINB>;
         GNN_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        // persistent warps: as many blocks as fit on the GPU at once
+        // persistent pairs: as many blocks as fit on the GPU at once
         int per_sm = 0;
-        GNN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WPC * 32, smem));
+        GNN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PPC * 64, smem));
         if (per_sm < 1) per_sm = 1;
         int64_t blocks = (int64_t)num_sms() * per_sm;
-        if (blocks > ceil_div(items, WPC)) blocks = ceil_div(items, WPC);
-        { kern<<<(unsigned)blocks, WPC * 32, smem, s>>>(p, xmap, sc.chunk_row, sc.chunk_begin, sc.chunk_end,
+        if (blocks > ceil_div(items, PPC)) blocks = ceil_div(items, PPC);
+        { kern<<<(unsigned)blocks, PPC * 64, smem, s>>>(p, xmap, sc.chunk_row, sc.chunk_begin, sc.chunk_end,
                                                         sc.n_chunks, sc.group_r0, sc.group_r1, sc.n_groups, partial,
                                                         pld); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
@@ -760,19 +758,18 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
 
 template <typename T>
 gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
-    // steps in flight per warp D: D * 512 * VPT bytes of gathered rows per warp;
-    // shared memory (8 warps per block) then sets the blocks per SM (MINB)
+    // a slot holds 2-16 KB of gathered rows (whole groups of four); four pairs
+    // per block; the pairs a SM holds are set by shared memory and registers
     const int64_t bytes = p.f * (int64_t)sizeof(T);
-    // a warp keeps NS batches of BE rows in flight (8-16 KB of shared memory)
-    if (bytes <= 128) return launch_cfg<T, 4, 1, 32, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 256) return launch_cfg<T, 8, 1, 16, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 512) return launch_cfg<T, 16, 1, 8, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1024) return launch_cfg<T, 16, 2, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 16, 3, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 16, 4, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 16, 5, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 16, 6, 4, 2, 4>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 16, 8, 4, 2, 2>(p, sc, partial, pld, s);
+    if (bytes <= 128) return launch_cfg<T, 4, 1, 16, 4, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 256) return launch_cfg<T, 8, 1, 16, 3, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 512) return launch_cfg<T, 16, 1, 8, 3, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1024) return launch_cfg<T, 16, 2, 4, 3, 4, 4>(p, sc, partial, pld, s);
+    if (bytes <= 1536) return launch_cfg<T, 16, 3, 4, 3, 4, 3>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 16, 4, 4, 2, 4, 2>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 16, 5, 4, 2, 4, 2>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 16, 6, 4, 2, 4, 2>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 16, 8, 4, 2, 2, 2>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 
@@ -782,11 +779,60 @@ size_t aggregate_partial_bytes(const Schedule &sc, int64_t f) {
     return (size_t)sc.n_chunks * (size_t)round_up(f, 8) * sizeof(float);
 }
 
-gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s) {
-    if (p.n_rows == 0) return GNN_OK;
-    const int64_t pld = round_up(p.f, 8);
-    if (dt == GNN_BF16) return launch_typed<__nv_bfloat16>(p, sc, partial, pld, s);
-    return launch_typed<float>(p, sc, partial, pld, s);
+namespace {
+std::atomic<int64_t> g_expire_ns{0};  // armed by gnn_debug_expire_next_wait
+
+// Rows wider than this many bytes are aggregated in column slices of this
+// width, one pass per slice (0: one pass).  GNN_AGG_SLICE_BYTES overrides it
+// (a multiple of 128).
+int64_t agg_slice_bytes() {
+    static int64_t v = -1;
+    if (v < 0) {
+        const char *e = getenv("GNN_AGG_SLICE_BYTES");
+        int64_t x = e ? atoll(e) : kAggSliceBytes;
+        v = (x > 0 && x % 128 == 0) ? x : 0;
+    }
+    return v;
+}
+}  // namespace
+
+gnn_status launch_aggregate(const AggParams &p_in, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s) {
+    if (p_in.n_rows == 0) return GNN_OK;
+    AggParams p = p_in;
+    p.wait_ns = 2000000000ull;
+    p.starve = 0;
+    if (sc.n_chunks + sc.n_groups > 0) {
+        const int64_t ns = g_expire_ns.exchange(0);
+        if (ns > 0) {
+            p.wait_ns = (uint64_t)ns;
+            p.starve = 1;
+        }
+    }
+    const int64_t es = dt == GNN_BF16 ? 2 : 4;
+    const int64_t slice = agg_slice_bytes();
+    if (slice <= 0 || p.f * es <= slice) {
+        const int64_t pld = round_up(p.f, 8);
+        if (dt == GNN_BF16) return launch_typed<__nv_bfloat16>(p, sc, partial, pld, s);
+        return launch_typed<float>(p, sc, partial, pld, s);
+    }
+    // column slices, one pass each: a pass gathers rows of `slice` bytes, so the
+    // L2 holds more of the hot rows of the pass
+    const int64_t fs = slice / es;
+    for (int64_t c0 = 0; c0 < p.f; c0 += fs) {
+        AggParams q = p;
+        q.f = p.f - c0 < fs ? p.f - c0 : fs;
+        q.X = static_cast<const char *>(p.X) + c0 * es;
+        q.out_off = p.out_off + c0;
+        q.self_off = p.self_off + c0;
+        if (p.self) q.self = static_cast<const char *>(p.self) + c0 * es;
+        q.hot_tier = hot_tier_for(sc, round_up(q.f * es, 32));
+        if (c0 > 0) q.starve = 0;
+        const int64_t pld = round_up(q.f, 8);
+        const gnn_status st = dt == GNN_BF16 ? launch_typed<__nv_bfloat16>(q, sc, partial, pld, s)
+                                             : launch_typed<float>(q, sc, partial, pld, s);
+        if (st != GNN_OK) return st;
+    }
+    return GNN_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -838,10 +884,15 @@ bool rows_ok(const void *p, int64_t rows, int64_t ld, int64_t f, gnn_dtype t) {
 
 }  // namespace gnn
 
+extern "C" gnn_status gnn_debug_expire_next_wait(int64_t wait_ns) {
+    gnn::g_expire_ns.store(wait_ns > 0 ? wait_ns : 0);
+    return GNN_OK;
+}
+
 extern "C" gnn_status gnn_aggregate_forward_noalloc(const gnn_graph *g, const void *H, int64_t ld_h, int64_t f,
                                                     void *Z, int64_t ld_z, gnn_dtype dtype, void *stream) {
     using namespace gnn;
-    if (!g || (dtype != GNN_F32 && dtype != GNN_BF16) || f <= 0) return GNN_EINVAL;
+    if (!g || (dtype != GNN_F32 && dtype != GNN_BF16) || f <= 0 || g->agg == GNN_AGG_GAT) return GNN_EINVAL;
     const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
     const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
     const int64_t half = gnn_sage_half_offset(f, dtype);

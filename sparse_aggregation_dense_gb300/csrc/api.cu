@@ -1,5 +1,6 @@
 // api.cu - the C ABI (include/gnn.h): argument checks, graph lifetime and the
 // order of the kernels of each call.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <new>
@@ -156,6 +157,7 @@ const char *gnn_status_string(gnn_status s) {
         case GNN_ECUDA: return "CUDA runtime error";
         case GNN_EUNSUPPORTED: return "unsupported shape or type";
         case GNN_EINDEX: return "bad index data on the device";
+        case GNN_ETIMEOUT: return "a bounded wait on the device ran out";
     }
     return "unknown status";
 }
@@ -181,6 +183,7 @@ static void destroy_graph(gnn_graph *g) {
     cudaFree(g->colw);
     cudaFree(g->wfwd);
     cudaFree(g->wbwd);
+    cudaFree(g->t2b);
     cudaFree(g->err);
     cudaFree(g->ws);
     cudaFree(g->claim);
@@ -195,7 +198,7 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     *out = nullptr;
     if (n_local < 0 || n_halo < 0 || nnz < 0 || !rowptr) return GNN_EINVAL;
     if (nnz > 0 && !colidx) return GNN_EINVAL;
-    if (agg != GNN_AGG_GCN_SYM && agg != GNN_AGG_SAGE_MEAN) return GNN_EINVAL;
+    if (agg != GNN_AGG_GCN_SYM && agg != GNN_AGG_SAGE_MEAN && agg != GNN_AGG_GAT) return GNN_EINVAL;
     if (n_local + n_halo >= ((int64_t)1 << 31) || nnz >= ((int64_t)1 << 31)) return GNN_EUNSUPPORTED;
     cudaStream_t s = as_stream(stream);
     gnn_graph *g = new (std::nothrow) gnn_graph();
@@ -234,8 +237,10 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     TRY_CUDA(cudaMemcpyAsync(&bad, g->err, sizeof(int), cudaMemcpyDeviceToHost, s));
     TRY_CUDA(cudaStreamSynchronize(s));
     if (bad) return fail(GNN_EINDEX);
-    // normalisation
-    if (agg == GNN_AGG_GCN_SYM) {
+    const bool gat = agg == GNN_AGG_GAT;
+    // normalisation (GraphSAGE: inverse neighbour counts; attention: computed per call)
+    if (gat) {
+    } else if (agg == GNN_AGG_GCN_SYM) {
         TRY_CUDA(cudaMalloc((void **)&g->colw, (size_t)(nT > 0 ? nT : 1) * sizeof(float)));
         TRY(launch_gcn_dinv(g->rowptr, g->colidx, n_local, n_halo, nnz, deg, g->colw, s));
     } else {
@@ -253,10 +258,12 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     // per-entry weights: the column factor of each entry (forward over the
     // block, backward over the transpose), 0 on the diagonal for the mean
     const bool sage = agg == GNN_AGG_SAGE_MEAN;
-    TRY_CUDA(cudaMalloc((void **)&g->wfwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
-    TRY_CUDA(cudaMalloc((void **)&g->wbwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
-    TRY(launch_entry_weights(g->rowptr, g->colidx, n_local, sage ? nullptr : g->colw, sage, g->wfwd, s));
-    TRY(launch_entry_weights(g->rowptrT, g->colidxT, nT, g->colw, sage, g->wbwd, s));
+    if (!gat) {
+        TRY_CUDA(cudaMalloc((void **)&g->wfwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
+        TRY_CUDA(cudaMalloc((void **)&g->wbwd, (size_t)(nnz > 0 ? nnz : 1) * sizeof(float)));
+        TRY(launch_entry_weights(g->rowptr, g->colidx, n_local, sage ? nullptr : g->colw, sage, g->wfwd, s));
+        TRY(launch_entry_weights(g->rowptrT, g->colidxT, nT, g->colw, sage, g->wbwd, s));
+    }
     // hotness tiers: forward columns by how often they are gathered (their
     // transpose row length), backward columns (local rows) by their row length
     TRY(tag_tiers(g->colidx, nnz, g->rowptrT, nT, &g->fwd, s));
@@ -265,7 +272,40 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
     // gather mostly share one L2 policy; the block's own copy is reordered in
     // place, the transpose gets a second copy (colidxT stays the stable
     // transpose that gnn_graph_copy_transpose hands out)
-    if (nnz > 0 && (g->fwd.tagged || g->bwd.tagged)) {
+    // graph attention: the weights are the attention, computed per call; what
+    // the graph keeps is where each transpose entry's attention sits in the
+    // block (the permutations of the two sorts below, composed with permT)
+    int32_t *fperm = nullptr, *tperm = nullptr, *iota = nullptr;
+    if (gat && nnz > 0) {
+        TRY_CUDA(cudaMalloc((void **)&g->t2b, (size_t)nnz * sizeof(int32_t)));
+        TRY_CUDA(cudaMallocAsync((void **)&iota, (size_t)nnz * sizeof(int32_t), s));
+        TRY(launch_iota(iota, nnz, s));
+        if (g->fwd.tagged) TRY_CUDA(cudaMallocAsync((void **)&fperm, (size_t)nnz * sizeof(int32_t), s));
+        if (g->bwd.tagged) TRY_CUDA(cudaMallocAsync((void **)&tperm, (size_t)nnz * sizeof(int32_t), s));
+    }
+    if (gat && nnz > 0 && (g->fwd.tagged || g->bwd.tagged)) {
+        // the sorts carry entry indices (moved bit for bit as the weight payload)
+        int32_t *tc = nullptr;
+        TRY_CUDA(cudaMallocAsync((void **)&tc, (size_t)nnz * sizeof(int32_t), s));
+        if (g->fwd.tagged) {
+            TRY_CUDA(cudaMemcpyAsync(tc, g->colidx, (size_t)nnz * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+            TRY(sort_rows_by_tier(g->rowptr, n_local, tc, reinterpret_cast<const float *>(iota), g->colidx,
+                                  reinterpret_cast<float *>(fperm), s));
+        }
+        if (g->bwd.tagged) {
+            TRY_CUDA(cudaMalloc((void **)&g->colidxTa, (size_t)nnz * sizeof(int32_t)));
+            TRY(sort_rows_by_tier(g->rowptrT, nT, g->colidxT, reinterpret_cast<const float *>(iota), g->colidxTa,
+                                  reinterpret_cast<float *>(tperm), s));
+        }
+        TRY_CUDA(cudaFreeAsync(tc, s));
+    }
+    if (gat && nnz > 0) {
+        TRY(launch_gat_entry_map(fperm, tperm, g->permT, nnz, g->t2b, iota, s));
+        TRY_CUDA(cudaFreeAsync(iota, s));
+        if (fperm) TRY_CUDA(cudaFreeAsync(fperm, s));
+        if (tperm) TRY_CUDA(cudaFreeAsync(tperm, s));
+    }
+    if (!gat && nnz > 0 && (g->fwd.tagged || g->bwd.tagged)) {
         int32_t *tc = nullptr;
         float *tw = nullptr;
         TRY_CUDA(cudaMallocAsync((void **)&tc, (size_t)nnz * sizeof(int32_t), s));
@@ -282,6 +322,11 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
         }
         TRY_CUDA(cudaFreeAsync(tc, s));
         TRY_CUDA(cudaFreeAsync(tw, s));
+    }
+    // row ends, on the entries in their final order (attention: set per call)
+    if (!gat) {
+        TRY(launch_mark_row_ends(g->rowptr, n_local, g->wfwd, s));
+        TRY(launch_mark_row_ends(g->rowptrT, nT, g->wbwd, s));
     }
     TRY_CUDA(cudaStreamSynchronize(s));
     TRY_CUDA(cudaGetLastError());
@@ -327,6 +372,7 @@ gnn_status gnn_get_error(gnn_graph *g) {
     int v = 0;
     GNN_CUDA_TRY(cudaMemcpy(&v, g->err, sizeof(int), cudaMemcpyDeviceToHost));
     GNN_CUDA_TRY(cudaMemset(g->err, 0, sizeof(int)));
+    if (v & (kErrWaitTc | kErrWaitAgg)) return GNN_ETIMEOUT;
     return v ? GNN_EINDEX : GNN_OK;
 }
 
@@ -395,6 +441,7 @@ gnn_status gnn_halo_pull_quantized(gnn_graph *g, const uint8_t *codes, int64_t l
 gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W, int64_t f_out,
                              int relu, void *Z, int64_t ld_z, void *H_out, int64_t ld_out, gnn_dtype dtype,
                              void *stream) {
+    if (g && g->agg == GNN_AGG_GAT) return GNN_EINVAL;  // attention layers: gnn_gat_forward / backward
     if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W) return GNN_EINVAL;
     const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
     const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
@@ -450,45 +497,60 @@ gnn_status gnn_layer_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
 gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
                               const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out, int relu,
                               float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
-                              gnn_dtype dtype, void *stream) {
-    if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W || !dW) return GNN_EINVAL;
+                              gnn_dtype dtype, gnn_dtype grad_dtype, void *stream) {
+    if (g && g->agg == GNN_AGG_GAT) return GNN_EINVAL;  // attention layers: gnn_gat_forward / backward
+    if (!g || !dtype_ok(dtype) || !dtype_ok(grad_dtype) || f_in <= 0 || f_out <= 0 || !W || !dW) return GNN_EINVAL;
+    if (dtype == GNN_F32 && grad_dtype != GNN_F32) return GNN_EINVAL;  // fp32 activations keep fp32 gradients
+    const bool mixed = dtype != grad_dtype;                              // bf16 activations, fp32 gradients
     const bool sage = g->agg == GNN_AGG_SAGE_MEAN;
     const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    // Z's layout is that of the activations; dZ shares it column for column
     const int64_t half = gnn_sage_half_offset(f_in, dtype);
     const int64_t K = sage ? 2 * f_in : f_in;
     const int64_t Kp = sage ? 2 * half : f_in;
     const int64_t out_rows = want_halo_grad ? nT : nL;
-    if (!operand_ok(G, nL, ld_g, f_out, dtype) || !operand_ok(Z, nL, ld_z, Kp, dtype)) return GNN_EINVAL;
+    if (!operand_ok(G, nL, ld_g, f_out, grad_dtype) || !operand_ok(Z, nL, ld_z, Kp, dtype)) return GNN_EINVAL;
     if (relu && !operand_ok(H_out, nL, ld_out, f_out, dtype)) return GNN_EINVAL;
-    if (dH && (!operand_ok(dH, out_rows, ld_dh, f_in, dtype) || !operand_ok(dZ, nL, ld_dz, Kp, dtype)))
+    if (dH && (!operand_ok(dH, out_rows, ld_dh, f_in, grad_dtype) || !operand_ok(dZ, nL, ld_dz, Kp, grad_dtype)))
         return GNN_EINVAL;
-    if (f_in * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    if (f_in * elem_size(grad_dtype) > 4096 || f_in * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
     cudaStream_t s = as_stream(stream);
     const int64_t ldw = round_up(f_out, 4);
     const bool use_tc = dtype == GNN_BF16 && update_bwd_tc_supported(Kp, f_out) && !force_simt_update();
+    // the tensor cores take dY in bf16: the fp32 gradient is masked and rounded into a staging buffer
+    const int64_t ldy = round_up(f_out, 8);
+    const size_t y_bytes = (use_tc && mixed) ? align_up((size_t)nL * ldy * 2) : 0;
     const size_t wp_bytes = align_up((size_t)Kp * ldw * sizeof(float));
     const size_t dwp_bytes = sage ? align_up((size_t)Kp * f_out * sizeof(float)) : 0;
     const size_t wg_bytes = align_up(use_tc ? update_bwd_tc_ws_bytes(nL, Kp, f_out)
                                             : update_bwd_ws_bytes(nL, Kp, f_out, dtype));
     const size_t part_bytes = dH ? align_up(aggregate_partial_bytes(g->bwd, f_in)) : 0;
-    gnn_status st = ensure_workspace(g, wp_bytes + dwp_bytes + wg_bytes + part_bytes, s);
+    gnn_status st = ensure_workspace(g, wp_bytes + dwp_bytes + wg_bytes + part_bytes + y_bytes, s);
     if (st != GNN_OK) return st;
     char *base = static_cast<char *>(g->ws);
     float *Wp = reinterpret_cast<float *>(base);
     float *dWp = sage ? reinterpret_cast<float *>(base + wp_bytes) : dW;
     float *wg = reinterpret_cast<float *>(base + wp_bytes + dwp_bytes);
     float *partial = reinterpret_cast<float *>(base + wp_bytes + dwp_bytes + wg_bytes);
+    void *Ystage = base + wp_bytes + dwp_bytes + wg_bytes + part_bytes;
     { pack_w_kernel<<<(unsigned)ceil_div(Kp * ldw, 256), 256, 0, s>>>(W, K, f_out, f_in, half, sage, Kp, Wp, ldw,
                                                                       dtype == GNN_BF16); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     {
         ProfScope prof(g, GNN_PROF_UPD_BWD, s);
-        if (use_tc)
+        if (use_tc && mixed) {
+            st = launch_grad_to_bf16(static_cast<const float *>(G), ld_g, relu ? H_out : nullptr, ld_out, nL, f_out,
+                                     Ystage, ldy, s);
+            if (st == GNN_OK)
+                st = launch_update_bwd_tc(Ystage, ldy, nullptr, 0, 0, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp,
+                                          dH ? dZ : nullptr, ld_dz, true, wg, g->err, s);
+        } else if (use_tc) {
             st = launch_update_bwd_tc(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp,
-                                      dH ? dZ : nullptr, ld_dz, wg, g->err, s);
-        else
+                                      dH ? dZ : nullptr, ld_dz, false, wg, g->err, s);
+        } else {
             st = launch_update_bwd(G, ld_g, H_out, ld_out, relu, Z, ld_z, nL, Kp, Wp, ldw, f_out, dWp,
-                                   dH ? dZ : nullptr, ld_dz, dtype, wg, wg_bytes, s);
+                                   dH ? dZ : nullptr, ld_dz, dtype, grad_dtype, wg, wg_bytes, s);
+        }
     }
     if (st != GNN_OK) return st;
     if (sage) {
@@ -504,7 +566,7 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     p.rowscale = sage ? nullptr : g->colw;
     p.n_rows = out_rows;
     p.colmask = g->bwd.tagged ? kColMask : 0xffffffffu;
-    p.hot_tier = hot_tier_for(g->bwd, round_up(f_in * elem_size(dtype), 32));
+    p.hot_tier = hot_tier_for(g->bwd, round_up(f_in * elem_size(grad_dtype), 32));
     p.f = f_in;
     p.out = dH;
     p.ldo = ld_dh;
@@ -513,7 +575,7 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     p.n_x = nL;
     if (sage) {
         p.self_mode = SELF_ADD;
-        p.X = static_cast<const char *>(dZ) + half * elem_size(dtype);
+        p.X = static_cast<const char *>(dZ) + half * elem_size(grad_dtype);
         p.self = dZ;
         p.ld_self = ld_dz;
         p.n_self = nL;
@@ -522,12 +584,13 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
         p.X = dZ;
     }
     ProfScope prof(g, GNN_PROF_AGG_BWD, s);
-    return launch_aggregate(p, g->bwd, dtype, partial, s);
+    return launch_aggregate(p, g->bwd, grad_dtype, partial, s);
 }
 
 gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
                                     int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
                                     gnn_dtype dtype, void *stream) {
+    if (g && g->agg == GNN_AGG_GAT) return GNN_EINVAL;  // attention layers: gnn_gat_forward / backward
     if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W) return GNN_EINVAL;
     if (g->agg != GNN_AGG_GCN_SYM) return GNN_EUNSUPPORTED;
     const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
@@ -583,6 +646,7 @@ gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, 
                                      const void *H, int64_t ld_h, const float *W, int64_t f_in, int64_t f_out,
                                      int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
                                      gnn_dtype dtype, void *stream) {
+    if (g && g->agg == GNN_AGG_GAT) return GNN_EINVAL;  // attention layers: gnn_gat_forward / backward
     if (!g || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W || !dW) return GNN_EINVAL;
     if (g->agg != GNN_AGG_GCN_SYM) return GNN_EUNSUPPORTED;
     const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
@@ -653,25 +717,29 @@ gnn_status gnn_layer_backward_narrow(gnn_graph *g, const void *G, int64_t ld_g, 
     // dW = H^T P and dH = P W^T over every row
     ProfScope prof(g, GNN_PROF_UPD_BWD, s);
     if (use_tc)
-        return launch_update_bwd_tc(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, wg,
-                                    g->err, s);
-    return launch_update_bwd(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, dtype, wg,
-                             wg_bytes, s);
+        return launch_update_bwd_tc(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, false,
+                                    wg, g->err, s);
+    return launch_update_bwd(P, ld_p, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, dtype, dtype,
+                             wg, wg_bytes, s);
 }
 
 gnn_status gnn_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, void *stream) {
-    if (!dtype_ok(dtype) || n < 0 || C <= 0 || !loss) return GNN_EINVAL;
+                          int64_t ld_g, float *row_loss, float *loss, gnn_dtype dtype, gnn_dtype grad_dtype,
+                          void *stream) {
+    if (!dtype_ok(dtype) || !dtype_ok(grad_dtype) || n < 0 || C <= 0 || !loss) return GNN_EINVAL;
     if (n > 0 && (!logits || !labels || !G || !row_loss || ld < C || ld_g < C)) return GNN_EINVAL;
-    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n, dtype, as_stream(stream));
+    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n, dtype, grad_dtype,
+                             as_stream(stream));
 }
 
 gnn_status gnn_softmax_ce_partial(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels,
                                   void *G, int64_t ld_g, float *row_loss, float *loss, int64_t n_mean,
-                                  gnn_dtype dtype, void *stream) {
-    if (!dtype_ok(dtype) || n < 0 || C <= 0 || !loss || n_mean < n || n_mean <= 0) return GNN_EINVAL;
+                                  gnn_dtype dtype, gnn_dtype grad_dtype, void *stream) {
+    if (!dtype_ok(dtype) || !dtype_ok(grad_dtype) || n < 0 || C <= 0 || !loss || n_mean < n || n_mean <= 0)
+        return GNN_EINVAL;
     if (n > 0 && (!logits || !labels || !G || !row_loss || ld < C || ld_g < C)) return GNN_EINVAL;
-    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n_mean, dtype, as_stream(stream));
+    return launch_softmax_ce(logits, ld, n, C, labels, G, ld_g, row_loss, loss, n_mean, dtype, grad_dtype,
+                             as_stream(stream));
 }
 
 gnn_status gnn_halo_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
@@ -695,6 +763,185 @@ gnn_status gnn_halo_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, 
         !operand_ok(gtable, n_table > 0 ? 1 : 0, ld_gt, f, GNN_F32))
         return GNN_EINVAL;
     return launch_grad_recv(g, gtable, ld_gt, n_table, local_ids, dH, ld_dh, f, dtype, as_stream(stream));
+}
+
+gnn_status gnn_gat_forward(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
+                           const float *a_src, const float *a_dst, int64_t f_out, int relu, void *T, int64_t ld_t,
+                           float *scores, float *alpha, void *H_out, int64_t ld_out, gnn_dtype dtype, void *stream) {
+    if (!g || g->agg != GNN_AGG_GAT || !dtype_ok(dtype) || f_in <= 0 || f_out <= 0 || !W || !a_src || !a_dst)
+        return GNN_EINVAL;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    if (!operand_ok(H, nT, ld_h, f_in, dtype) || !operand_ok(T, nT, ld_t, f_out, dtype) ||
+        !operand_ok(H_out, nL, ld_out, f_out, dtype) || (nT > 0 && !scores) || (g->nnz > 0 && !alpha))
+        return GNN_EINVAL;
+    if (f_out * elem_size(dtype) > 4096) return GNN_EUNSUPPORTED;
+    if (nL == 0) return GNN_OK;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const bool use_tc = dtype == GNN_BF16 && update_fwd_tc_supported(f_in, f_out) && !force_simt_update();
+    const size_t wp_bytes = align_up((size_t)f_in * ldw * sizeof(float));
+    const size_t wt_bytes = use_tc ? align_up(update_tc_wt_bytes(f_in, f_out)) : 0;
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->fwd, f_out));
+    gnn_status st = ensure_workspace(g, wp_bytes + wt_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    float *Wp = static_cast<float *>(g->ws);
+    void *wt = static_cast<char *>(g->ws) + wp_bytes;
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(g->ws) + wp_bytes + wt_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(f_in * ldw, 256), 256, 0, s>>>(W, f_in, f_out, f_in, f_in, 0, f_in, Wp, ldw,
+                                                                        dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    {
+        // T = H W over every row, local and halo
+        ProfScope prof(g, GNN_PROF_UPD_FWD, s);
+        st = use_tc ? launch_update_fwd_tc(H, ld_h, nT, f_in, Wp, ldw, f_out, 0, T, ld_t, wt, g->err, s)
+                    : launch_update_fwd(H, ld_h, nT, f_in, Wp, ldw, f_out, 0, T, ld_t, dtype, s);
+    }
+    if (st != GNN_OK) return st;
+    float *s_src = scores, *s_dst = scores + nT;
+    st = launch_gat_scores(T, ld_t, nT, nL, f_out, a_src, a_dst, s_src, s_dst, dtype, s);
+    if (st != GNN_OK) return st;
+    st = launch_gat_softmax(g, s_src, s_dst, alpha, s);
+    if (st != GNN_OK) return st;
+    AggParams p{};
+    p.err = g->err;
+    p.rowptr = g->rowptr;
+    p.colidx = reinterpret_cast<const uint32_t *>(g->colidx);
+    p.wts = alpha;
+    p.rowscale = nullptr;
+    p.n_rows = nL;
+    p.colmask = g->fwd.tagged ? kColMask : 0xffffffffu;
+    p.hot_tier = hot_tier_for(g->fwd, round_up(f_out * elem_size(dtype), 32));
+    p.X = T;
+    p.ldx = ld_t;
+    p.n_x = nT;
+    p.f = f_out;
+    p.self_mode = SELF_NONE;
+    p.out = H_out;
+    p.ldo = ld_out;
+    p.relu = relu;
+    ProfScope prof(g, GNN_PROF_AGG_FWD, s);
+    return launch_aggregate(p, g->fwd, dtype, partial, s);
+}
+
+gnn_status gnn_gat_backward(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                            const void *H, int64_t ld_h, int64_t f_in, const float *W, const float *a_src,
+                            const float *a_dst, int64_t f_out, int relu, const void *T, int64_t ld_t,
+                            const float *scores, const float *alpha, float *dW, float *da_src, float *da_dst,
+                            void *dT, int64_t ld_dt, void *dH, int64_t ld_dh, gnn_dtype dtype, gnn_dtype grad_dtype,
+                            void *stream) {
+    if (!g || g->agg != GNN_AGG_GAT || !dtype_ok(dtype) || !dtype_ok(grad_dtype) || f_in <= 0 || f_out <= 0 || !W ||
+        !a_src || !a_dst || !dW || !da_src || !da_dst)
+        return GNN_EINVAL;
+    if (dtype == GNN_F32 && grad_dtype != GNN_F32) return GNN_EINVAL;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    if (!operand_ok(G, nL, ld_g, f_out, grad_dtype) || !operand_ok(H, nT, ld_h, f_in, dtype) ||
+        !operand_ok(T, nT, ld_t, f_out, dtype) || !operand_ok(dT, nT, ld_dt, f_out, grad_dtype) ||
+        (relu && !operand_ok(H_out, nL, ld_out, f_out, dtype)) || (dH && !operand_ok(dH, nT, ld_dh, f_in, grad_dtype)) ||
+        (nT > 0 && !scores) || (g->nnz > 0 && !alpha))
+        return GNN_EINVAL;
+    if (f_out * elem_size(grad_dtype) > 4096) return GNN_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const bool mixed = dtype != grad_dtype;
+    const int64_t ldw = round_up(f_out, 4);
+    const int64_t ldy = round_up(f_out, elems_per_16b(grad_dtype));
+    const int64_t ldb = round_up(f_out, 8);
+    const bool use_tc = dtype == GNN_BF16 && update_bwd_tc_supported(f_in, f_out) && !force_simt_update();
+    const size_t wp_bytes = align_up((size_t)f_in * ldw * sizeof(float));
+    const size_t y_bytes = align_up((size_t)(nL > 0 ? nL : 1) * ldy * elem_size(grad_dtype));
+    const size_t e_bytes = align_up((size_t)(g->nnz > 0 ? g->nnz : 1) * sizeof(float));  // dz, then alphaT
+    const size_t v_bytes = align_up((size_t)(nT + nL + 1) * sizeof(float));                // ds_src, ds_dst
+    const size_t c_bytes = align_up(std::max(gat_colsum_ws_floats(nT, f_out), (size_t)1) * sizeof(float));
+    const size_t b_bytes = (use_tc && mixed) ? align_up((size_t)(nT > 0 ? nT : 1) * ldb * 2) : 0;
+    const size_t wg_bytes = align_up(use_tc ? update_bwd_tc_ws_bytes(nT, f_in, f_out)
+                                            : update_bwd_ws_bytes(nT, f_in, f_out, dtype));
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->bwd, f_out));
+    gnn_status st = ensure_workspace(g, wp_bytes + y_bytes + 2 * e_bytes + v_bytes + c_bytes + b_bytes + wg_bytes +
+                                            part_bytes, s);
+    if (st != GNN_OK) return st;
+    char *base = static_cast<char *>(g->ws);
+    float *Wp = reinterpret_cast<float *>(base);
+    char *q = base + wp_bytes;
+    void *Y = q;
+    q += y_bytes;
+    float *dz = reinterpret_cast<float *>(q);
+    q += e_bytes;
+    float *alphaT = reinterpret_cast<float *>(q);
+    q += e_bytes;
+    float *ds_src = reinterpret_cast<float *>(q), *ds_dst = ds_src + nT;
+    q += v_bytes;
+    float *cws = reinterpret_cast<float *>(q);
+    q += c_bytes;
+    void *dTb = q;
+    q += b_bytes;
+    float *wg = reinterpret_cast<float *>(q);
+    q += wg_bytes;
+    float *partial = reinterpret_cast<float *>(q);
+    const float *s_src = scores, *s_dst = scores + nT;
+    { pack_w_kernel<<<(unsigned)ceil_div(f_in * ldw, 256), 256, 0, s>>>(W, f_in, f_out, f_in, f_in, 0, f_in, Wp, ldw,
+                                                                        dtype == GNN_BF16); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    // dY, the attention's backward per entry (dz) and per row (ds_dst), then over the transpose (ds_src, alphaT)
+    st = launch_gat_mask(G, ld_g, relu ? H_out : nullptr, ld_out, nL, f_out, Y, ldy, dtype, grad_dtype, s);
+    if (st == GNN_OK)
+        st = launch_gat_edge_backward(g, s_src, s_dst, alpha, Y, ldy, T, ld_t, f_out, dz, ds_dst, dtype, grad_dtype, s);
+    if (st == GNN_OK) st = launch_gat_transpose(g, dz, alpha, ds_src, alphaT, s);
+    if (st != GNN_OK) return st;
+    {
+        // dT = sum over the transpose of alpha dY, then the rank-1 terms of the scores
+        AggParams p{};
+        p.err = g->err;
+        p.rowptr = g->rowptrT;
+        p.colidx = reinterpret_cast<const uint32_t *>(g->colidxTa ? g->colidxTa : g->colidxT);
+        p.wts = alphaT;
+        p.rowscale = nullptr;
+        p.n_rows = nT;
+        p.colmask = g->bwd.tagged ? kColMask : 0xffffffffu;
+        p.hot_tier = hot_tier_for(g->bwd, round_up(f_out * elem_size(grad_dtype), 32));
+        p.X = Y;
+        p.ldx = ldy;
+        p.n_x = nL;
+        p.f = f_out;
+        p.self_mode = SELF_NONE;
+        p.out = dT;
+        p.ldo = ld_dt;
+        ProfScope prof(g, GNN_PROF_AGG_BWD, s);
+        st = launch_aggregate(p, g->bwd, grad_dtype, partial, s);
+    }
+    if (st == GNN_OK) st = launch_gat_rank1(dT, ld_dt, nT, nL, f_out, ds_src, ds_dst, a_src, a_dst, grad_dtype, s);
+    if (st == GNN_OK) st = launch_gat_colsum(T, ld_t, nT, f_out, ds_src, da_src, cws, dtype, s);
+    if (st == GNN_OK) st = launch_gat_colsum(T, ld_t, nL, f_out, ds_dst, da_dst, cws, dtype, s);
+    if (st != GNN_OK) return st;
+    // dW = H^T dT and dH = dT W^T over every row (bf16 activations: dT is a bf16 operand)
+    ProfScope prof(g, GNN_PROF_UPD_BWD, s);
+    if (use_tc && mixed) {
+        st = launch_grad_to_bf16(static_cast<const float *>(dT), ld_dt, nullptr, 0, nT, f_out, dTb, ldb, s);
+        if (st != GNN_OK) return st;
+        return launch_update_bwd_tc(dTb, ldb, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, true,
+                                    wg, g->err, s);
+    }
+    if (use_tc)
+        return launch_update_bwd_tc(dT, ld_dt, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, false,
+                                    wg, g->err, s);
+    return launch_update_bwd(dT, ld_dt, nullptr, 0, 0, H, ld_h, nT, f_in, Wp, ldw, f_out, dW, dH, ld_dh, dtype,
+                             grad_dtype, wg, wg_bytes, s);
+}
+
+gnn_status gnn_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const int64_t *ids, int64_t n, void *dst,
+                           int64_t ld_dst, int64_t f, gnn_dtype dtype, int *err, void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || n_src < 0 || f <= 0) return GNN_EINVAL;
+    if (n == 0) return GNN_OK;
+    if (!ids || !operand_ok(src, n_src > 0 ? 1 : 0, ld_src, f, dtype) || !operand_ok(dst, n, ld_dst, f, dtype))
+        return GNN_EINVAL;
+    return launch_gather_rows(src, ld_src, n_src, ids, n, dst, ld_dst, f, dtype, err, as_stream(stream));
+}
+
+gnn_status gnn_scatter_add_rows(const void *src, int64_t ld_src, const int64_t *ids, int64_t n, void *dst,
+                                int64_t ld_dst, int64_t n_dst, int64_t f, gnn_dtype dtype, int *err, void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || n_dst < 0 || f <= 0) return GNN_EINVAL;
+    if (n == 0) return GNN_OK;
+    if (!ids || !operand_ok(src, n, ld_src, f, dtype) || !operand_ok(dst, n_dst > 0 ? 1 : 0, ld_dst, f, dtype))
+        return GNN_EINVAL;
+    return launch_scatter_add_rows(src, ld_src, ids, n, dst, ld_dst, n_dst, f, dtype, err, as_stream(stream));
 }
 
 }  // extern "C"

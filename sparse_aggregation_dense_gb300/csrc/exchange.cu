@@ -97,7 +97,89 @@ __global__ void __launch_bounds__(256) grad_recv_kernel(const float *__restrict_
     }
 }
 
+// dst[i, 0:f] = src[ids[i], 0:f], bit-exact: one warp per row, 16-byte pieces
+// (rows start on 16-byte boundaries) and element copies for the tail
+template <typename T>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const T *__restrict__ src, int64_t ld_src, int64_t n_src,
+                                                          const int64_t *__restrict__ ids, int64_t n,
+                                                          T *__restrict__ dst, int64_t ld_dst, int64_t f, int *err) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        const int64_t id = ids[i];
+        if (id < 0 || id >= n_src) {
+            if (lane == 0 && err) atomicOr(err, kErrIndex);
+            continue;
+        }
+        const T *a = src + id * ld_src;
+        T *b = dst + i * ld_dst;
+        const int64_t nv = f / EPV;
+        for (int64_t v = lane; v < nv; v += 32)
+            reinterpret_cast<uint4 *>(b)[v] = __ldg(reinterpret_cast<const uint4 *>(a) + v);
+        for (int64_t c = nv * EPV + lane; c < f; c += 32) b[c] = a[c];
+    }
+}
+
+// dst[ids[i], 0:f] += src[i, 0:f] (fp32 sum, stored as T); the ids of one launch
+// are distinct, so rows never collide
+template <typename T>
+__global__ void __launch_bounds__(256) scatter_add_rows_kernel(const T *__restrict__ src, int64_t ld_src,
+                                                               const int64_t *__restrict__ ids, int64_t n,
+                                                               T *__restrict__ dst, int64_t ld_dst, int64_t n_dst,
+                                                               int64_t f, int *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        const int64_t id = ids[i];
+        if (id < 0 || id >= n_dst) {
+            if (lane == 0 && err) atomicOr(err, kErrIndex);
+            continue;
+        }
+        const T *a = src + i * ld_src;
+        T *b = dst + id * ld_dst;
+        for (int64_t c = (int64_t)lane * 4; c < f; c += 128) {
+            if (c + 4 <= f) {
+                const float4 x = load4v(b + c), y = load4v(a + c);
+                store4v(b + c, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
+            } else {
+                for (int64_t k = c; k < f; ++k) set_elem(b + k, elem(b + k) + elem(a + k));
+            }
+        }
+    }
+}
+
 }  // namespace
+
+gnn_status launch_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const int64_t *ids, int64_t n,
+                              void *dst, int64_t ld_dst, int64_t f, gnn_dtype dt, int *err, cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n * 32, 256), (int64_t)num_sms() * 16);
+    if (dt == GNN_BF16)
+        { gather_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), ld_src,
+                                                                   n_src, ids, n, static_cast<__nv_bfloat16 *>(dst),
+                                                                   ld_dst, f, err); GNN_LAUNCHED(1); }
+    else
+        { gather_rows_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(src), ld_src, n_src, ids, n,
+                                                           static_cast<float *>(dst), ld_dst, f, err); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
+gnn_status launch_scatter_add_rows(const void *src, int64_t ld_src, const int64_t *ids, int64_t n, void *dst,
+                                   int64_t ld_dst, int64_t n_dst, int64_t f, gnn_dtype dt, int *err, cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n * 32, 256), (int64_t)num_sms() * 16);
+    if (dt == GNN_BF16)
+        { scatter_add_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(src), ld_src, ids, n, static_cast<__nv_bfloat16 *>(dst), ld_dst, n_dst,
+            f, err); GNN_LAUNCHED(1); }
+    else
+        { scatter_add_rows_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(src), ld_src, ids, n,
+                                                                static_cast<float *>(dst), ld_dst, n_dst, f, err); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
 
 gnn_status launch_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
                             float *gtable, int64_t ld_gt, int64_t n_table, gnn_dtype dt, cudaStream_t s) {

@@ -14,6 +14,11 @@ namespace gnn {
 
 constexpr int kWarp = 32;
 
+// bits of a graph's device error word
+constexpr int kErrIndex = 1;    // bad index data (a row was skipped)
+constexpr int kErrWaitTc = 2;   // a tensor-core kernel's bounded wait ran out
+constexpr int kErrWaitAgg = 4;  // an aggregation's bounded wait ran out
+
 // A row of the block (or of its transpose) with more than kHeavyNnz entries is
 // split into chunks of kChunkNnz entries, each summed by its own warp into an
 // fp32 partial; a fix-up pass adds the partials of a row in chunk order.
@@ -21,6 +26,8 @@ constexpr int kHeavyNnz = 512;
 constexpr int kChunkNnz = 512;
 constexpr int kGroupNnz = 512;   // entry window of a row group
 constexpr int kGroupRows = 256;  // rows of a row group at most
+// rows wider than this are aggregated in column slices of this many bytes (0: never)
+constexpr int64_t kAggSliceBytes = 0;
 
 // Column ids of the graph's CSR copies carry a 5-bit "hotness tier" in bits
 // 27..31 (when the column count is below 2^27): tier t holds the columns of
@@ -31,21 +38,24 @@ constexpr int kTierShift = 27;
 constexpr uint32_t kColMask = (1u << kTierShift) - 1u;
 constexpr int kTiers = 32;
 
-// Heavy-row schedule of one CSR (block rows or transpose rows).
+// Schedule of one CSR (block rows or transpose rows) for the aggregation.
+// Work items: chunks of heavy rows and groups of light rows.  The fix-up rows
+// are the heavy rows (partials added in chunk order) and the empty rows (no
+// chunk: only their zero or self term is written).
 struct Schedule {
     bool tagged = false;           // column ids carry tiers
     int64_t tier_rows[kTiers] = {};  // columns per tier
     int64_t n_rows = 0;        // rows of the CSR
-    int64_t n_heavy = 0;       // rows split into chunks
+    int64_t n_heavy = 0;       // fix-up rows: rows split into chunks, and empty rows
     int64_t n_chunks = 0;      // total chunks
     int32_t *heavy_rows = nullptr;   // [n_heavy] row ids, ascending
     int32_t *heavy_choff = nullptr;  // [n_heavy + 1] first chunk of each heavy row
     int32_t *chunk_row = nullptr;    // [n_chunks]
     int32_t *chunk_begin = nullptr;  // [n_chunks] entry range of the chunk
     int32_t *chunk_end = nullptr;    // [n_chunks]
-    // row groups: runs of consecutive light rows whose first entries fall in
-    // one kGroupNnz-entry window (at most kGroupRows rows); the aggregation
-    // streams a group's entries as one range
+    // row groups: runs of consecutive light rows (1 to kHeavyNnz entries)
+    // whose first entries fall in one kGroupNnz-entry window (at most
+    // kGroupRows rows); the aggregation streams a group's entries as one range
     int64_t n_groups = 0;
     int32_t *group_r0 = nullptr;     // [n_groups] first row of the group
     int32_t *group_r1 = nullptr;     // [n_groups] one past its last row
@@ -66,6 +76,10 @@ struct gnn_graph {
     // the transpose's tagged column ids in the aggregation's order (each row
     // hottest tier first); null when untagged, and colidxT is used instead
     int32_t *colidxTa = nullptr;
+    // graph attention graphs: for each entry of the transpose in the
+    // aggregation's order, the block entry (in the block's aggregation order)
+    // it came from
+    int32_t *t2b = nullptr;
     // per-entry weights of the block (forward) and of its transpose (backward),
     // in the aggregation's order
     float *wfwd = nullptr, *wbwd = nullptr;
@@ -130,6 +144,32 @@ gnn_status sort_rows_by_tier(const int32_t *rowptr, int64_t n_rows, const int32_
                              int32_t *col_out, float *w_out, cudaStream_t s);
 void free_schedule(Schedule *sc);
 
+// ---- graph attention (GAT) steps -------------------------------------------
+gnn_status launch_iota(int32_t *out, int64_t n, cudaStream_t s);
+// t2b[k] = block position (sorted order) of transpose entry k (sorted order):
+// fperm[e_sorted] = e_original (null: not sorted), tperm[k_sorted] = k_stable
+// (null: not sorted), permT[k_stable] = e_original; scratch: int32[nnz]
+gnn_status launch_gat_entry_map(const int32_t *fperm, const int32_t *tperm, const int32_t *permT, int64_t nnz,
+                                int32_t *t2b, int32_t *scratch, cudaStream_t s);
+gnn_status launch_gat_scores(const void *T, int64_t ld, int64_t n_total, int64_t n_local, int64_t f,
+                             const float *a_src, const float *a_dst, float *s_src, float *s_dst, gnn_dtype dt,
+                             cudaStream_t s);
+gnn_status launch_gat_softmax(const gnn_graph *g, const float *s_src, const float *s_dst, float *alpha,
+                              cudaStream_t s);
+gnn_status launch_gat_mask(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int64_t n, int64_t f,
+                           void *Y, int64_t ld_y, gnn_dtype dt, gnn_dtype gdt, cudaStream_t s);
+gnn_status launch_gat_edge_backward(const gnn_graph *g, const float *s_src, const float *s_dst, const float *alpha,
+                                    const void *dY, int64_t ld_y, const void *T, int64_t ld_t, int64_t f, float *dz,
+                                    float *ds_dst, gnn_dtype dt, gnn_dtype gdt, cudaStream_t s);
+gnn_status launch_gat_transpose(const gnn_graph *g, const float *dz, const float *alpha, float *ds_src,
+                                float *alphaT, cudaStream_t s);
+gnn_status launch_gat_rank1(void *dT, int64_t ld, int64_t n_total, int64_t n_local, int64_t f, const float *ds_src,
+                            const float *ds_dst, const float *a_src, const float *a_dst, gnn_dtype gdt,
+                            cudaStream_t s);
+size_t gat_colsum_ws_floats(int64_t n_rows, int64_t f);
+gnn_status launch_gat_colsum(const void *T, int64_t ld, int64_t n_rows, int64_t f, const float *w, float *out,
+                             float *ws, gnn_dtype dt, cudaStream_t s);
+
 // ---- kernels launched by the API ------------------------------------------
 gnn_status launch_validate_csr(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, int64_t n_cols,
                                int64_t nnz, int *err, cudaStream_t s);
@@ -141,6 +181,9 @@ gnn_status launch_sage_invcnt(const int32_t *rowptr, const int32_t *colidx, int6
 // skip_self and col_e equals the entry's row
 gnn_status launch_entry_weights(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, const float *colw,
                                 bool skip_self, float *w, cudaStream_t s);
+// set the sign bit of the weight of each row's last entry (in the aggregation's
+// entry order): the aggregation reads it as the row's end; weights are >= 0
+gnn_status launch_mark_row_ends(const int32_t *rowptr, int64_t n_rows, float *w, cudaStream_t s);
 
 gnn_status launch_pull(const void *table, int64_t ld_t, int64_t n_table, const int64_t *ids, int64_t n_ids,
                        void *H, int64_t ld_h, int64_t row0, int64_t f, int es, int *err, cudaStream_t s);
@@ -155,6 +198,11 @@ gnn_status launch_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t
 gnn_status launch_grad_recv(gnn_graph *g, const float *gtable, int64_t ld_gt, int64_t n_table,
                             const int64_t *local_ids, void *dH, int64_t ld_dh, int64_t f, gnn_dtype dt,
                             cudaStream_t s);
+// rows for the exchange between processes: an indexed gather and an ordered scatter-add
+gnn_status launch_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const int64_t *ids, int64_t n,
+                              void *dst, int64_t ld_dst, int64_t f, gnn_dtype dt, int *err, cudaStream_t s);
+gnn_status launch_scatter_add_rows(const void *src, int64_t ld_src, const int64_t *ids, int64_t n, void *dst,
+                                   int64_t ld_dst, int64_t n_dst, int64_t f, gnn_dtype dt, int *err, cudaStream_t s);
 // low-bit halo codec (quantise on push, dequantise on pull)
 gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                              uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
@@ -190,11 +238,16 @@ struct AggParams {
     void *out;
     int64_t ldo;
     int64_t out_off;         // column of out where the aggregate is written
+    int64_t self_off;        // column of out where SELF_COPY writes the copied row (0)
     const void *self;        // SELF_ADD source (row stride ld_self)
     int64_t ld_self;
     int64_t n_self;
     int relu;                // 1: the aggregated values are written as max(x, 0)
     int *err;                // device error word
+    // set by launch_aggregate: the bound of every wait, and the failure-test
+    // switch (first batch of the first pair not issued)
+    uint64_t wait_ns;
+    int starve;
 };
 gnn_status launch_aggregate(const AggParams &p, const Schedule &sc, gnn_dtype dt, float *partial, cudaStream_t s);
 size_t aggregate_partial_bytes(const Schedule &sc, int64_t f);
@@ -221,20 +274,30 @@ int num_sms();
 // partials of each CTA (ws: update_bwd_tc_ws_bytes), then dWp = their sum.
 bool update_bwd_tc_supported(int64_t Kp, int64_t N);
 size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp, int64_t N);
+// dz_f32: dZ is stored in fp32 (G, H_out and Z are bf16 either way).
 gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                                 int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
-                                float *dWp, void *dZ, int64_t ld_dz, void *ws, int *err, cudaStream_t s);
+                                float *dWp, void *dZ, int64_t ld_dz, bool dz_f32, void *ws, int *err, cudaStream_t s);
+// dY = bf16(relu ? G * 1[H_out > 0] : G) for an fp32 G and a bf16 H_out (H_out may
+// be null without ReLU): the tensor-core operand of the (bf16, fp32) backward.
+// Y: n x ld_y bf16, ld_y a multiple of 8; columns [N, ld_y) are written as 0.
+gnn_status launch_grad_to_bf16(const float *G, int64_t ld_g, const void *Hout, int64_t ld_h, int64_t n, int64_t N,
+                               void *Y, int64_t ld_y, cudaStream_t s);
+// 2-D fp32 tensor map with 128-byte swizzle (box_inner x box_outer elements)
+bool make_map_f32_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                     uint32_t box_inner, uint32_t box_outer);
 // GNN_UPDATE_SIMT=1 in the environment selects the CUDA-core update for bf16 too
 bool force_simt_update();
 // Dense update, backward: dZ = dY Wp^T (n x Kp) when dZ != NULL; dWp partials then dW.
+// dt: the activations (Z, Hout); gdt: the gradients (G, dZ); (F32, BF16) is not taken.
 gnn_status launch_update_bwd(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                              int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
-                             float *dWp, void *dZ, int64_t ld_dz, gnn_dtype dt, float *ws, size_t ws_bytes,
-                             cudaStream_t s);
+                             float *dWp, void *dZ, int64_t ld_dz, gnn_dtype dt, gnn_dtype gdt, float *ws,
+                             size_t ws_bytes, cudaStream_t s);
 size_t update_bwd_ws_bytes(int64_t n, int64_t Kp, int64_t N, gnn_dtype dt);
 
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt,
+                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt, gnn_dtype gdt,
                              cudaStream_t s);
 
 }  // namespace gnn

@@ -14,9 +14,9 @@ __device__ __forceinline__ float ld_elem(const __nv_bfloat16 *p) { return __bflo
 __device__ __forceinline__ void st_elem(float *p, float v) { *p = v; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
-template <typename T>
+template <typename T, typename TG>
 __global__ void softmax_ce_rows(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C,
-                                const int32_t *__restrict__ labels, T *__restrict__ G, int64_t ld_g,
+                                const int32_t *__restrict__ labels, TG *__restrict__ G, int64_t ld_g,
                                 float *__restrict__ row_loss, float inv_n) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -65,15 +65,34 @@ __device__ __forceinline__ uint4 pack_vec(const float (&v)[8]) {
     return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
 }
 
+// the EPV gradient values of one logits vector, stored as TG with streaming
+// stores (16 bytes each; 8 bytes for four bf16 values)
+template <int EPV>
+__device__ __forceinline__ void store_vals(float *dst, const float (&o)[EPV]) {
+#pragma unroll
+    for (int k = 0; k < EPV; k += 4)
+        __stcs(reinterpret_cast<uint4 *>(dst + k),
+               make_uint4(__float_as_uint(o[k]), __float_as_uint(o[k + 1]), __float_as_uint(o[k + 2]),
+                          __float_as_uint(o[k + 3])));
+}
+template <int EPV>
+__device__ __forceinline__ void store_vals(__nv_bfloat16 *dst, const float (&o)[EPV]) {
+    if constexpr (EPV == 8) {
+        __stcs(reinterpret_cast<uint4 *>(dst), pack_vec(o));
+    } else {
+        __stcs(reinterpret_cast<uint2 *>(dst), make_uint2(pack_bf2(o[0], o[1]), pack_bf2(o[2], o[3])));
+    }
+}
+
 // Rows of up to 32 * VPL 16-byte vectors of classes, rows 16-byte aligned:
 // a warp takes RPW consecutive rows and loads all of them first (lane q holds
 // vectors q, q + 32, ... of each row), so RPW rows' loads are in flight at
 // once; then each row is reduced from registers and its gradient written back
 // with 16-byte stores (element stores only for the vector that straddles C,
 // so G's padding is left alone).
-template <typename T, int VPL, int RPW>
+template <typename T, typename TG, int VPL, int RPW>
 __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__ X, int64_t ld, int64_t n, int64_t C64,
-                                                           const int32_t *__restrict__ labels, T *__restrict__ G,
+                                                           const int32_t *__restrict__ labels, TG *__restrict__ G,
                                                            int64_t ld_g, float *__restrict__ row_loss, float inv_n) {
     constexpr int EPV = 16 / (int)sizeof(T);
     const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW;
@@ -131,7 +150,7 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
             xy += __shfl_xor_sync(0xffffffffu, xy, o);
         }
         const float inv_se = 1.0f / se;
-        T *gr = G + i * ld_g;
+        TG *gr = G + i * ld_g;
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
             const int c0 = (lane + 32 * q) * EPV;
@@ -141,7 +160,7 @@ __global__ void __launch_bounds__(256) softmax_ce_rows_vec(const T *__restrict__
 #pragma unroll
             for (int k = 0; k < EPV; ++k) o[k] = (v[r][q][k] * inv_se - (k == yk ? 1.f : 0.f)) * inv_n;
             if (c0 + EPV <= C) {
-                __stcs(reinterpret_cast<uint4 *>(gr + c0), pack_vec(o));
+                store_vals<EPV>(gr + c0, o);
             } else {
                 for (int k = 0; k < EPV && c0 + k < C; ++k) st_elem(gr + c0 + k, o[k]);
             }
@@ -192,41 +211,50 @@ __global__ void __launch_bounds__(kLossThreads) loss_mean_of_chunks(const float 
 
 constexpr int kRowsPerWarp = 4;
 
+namespace {
+
+template <typename T, typename TG>
+gnn_status softmax_rows_typed(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
+                              int64_t ld_g, float *row_loss, float inv_n, cudaStream_t s) {
+    constexpr int epv = 16 / (int)sizeof(T);                // logits per 16-byte vector
+    constexpr int gbytes = epv * (int)sizeof(TG);            // bytes of their gradient
+    const T *X = static_cast<const T *>(logits);
+    TG *Gt = static_cast<TG *>(G);
+    const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(G) % (gbytes < 16 ? gbytes : 16)) == 0 && ld % epv == 0 &&
+                         (ld_g * (int64_t)sizeof(TG)) % 16 == 0;
+    const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
+    const unsigned vblocks = (unsigned)ceil_div(ceil_div(n, kRowsPerWarp) * 32, 256);
+    if (aligned && C <= 32 * epv) {
+        { softmax_ce_rows_vec<T, TG, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(X, ld, n, C, labels, Gt, ld_g,
+                                                                             row_loss, inv_n); GNN_LAUNCHED(1); }
+    } else if (aligned && C <= 64 * epv) {
+        { softmax_ce_rows_vec<T, TG, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(X, ld, n, C, labels, Gt, ld_g,
+                                                                             row_loss, inv_n); GNN_LAUNCHED(1); }
+    } else {
+        { softmax_ce_rows<T, TG><<<blocks, 256, 0, s>>>(X, ld, n, C, labels, Gt, ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
+    }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
+}  // namespace
+
 gnn_status launch_softmax_ce(const void *logits, int64_t ld, int64_t n, int64_t C, const int32_t *labels, void *G,
-                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt,
+                             int64_t ld_g, float *row_loss, float *loss, int64_t n_mean, gnn_dtype dt, gnn_dtype gdt,
                              cudaStream_t s) {
     const float inv_n = n_mean > 0 ? 1.0f / (float)n_mean : 0.f;
-    const int es = dt == GNN_BF16 ? 2 : 4;
-    const int epv = 16 / es;
-    const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(G)) & 15u) == 0 &&
-                         ld % epv == 0 && ld_g % epv == 0;
     if (n > 0) {
-        const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
-        const unsigned vblocks = (unsigned)ceil_div(ceil_div(n, kRowsPerWarp) * 32, 256);
-        if (aligned && C <= 32 * epv) {
-            if (dt == GNN_BF16)
-                { softmax_ce_rows_vec<__nv_bfloat16, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
-                    static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
-                    ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-            else
-                { softmax_ce_rows_vec<float, 1, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
-                                                                      labels, static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-        } else if (aligned && C <= 64 * epv) {
-            if (dt == GNN_BF16)
-                { softmax_ce_rows_vec<__nv_bfloat16, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(
-                    static_cast<const __nv_bfloat16 *>(logits), ld, n, C, labels, static_cast<__nv_bfloat16 *>(G),
-                    ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-            else
-                { softmax_ce_rows_vec<float, 2, kRowsPerWarp><<<vblocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C,
-                                                                      labels, static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-        } else if (dt == GNN_BF16) {
-            { softmax_ce_rows<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(logits), ld, n,
-                                                                   C, labels, static_cast<__nv_bfloat16 *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-        } else {
-            { softmax_ce_rows<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(logits), ld, n, C, labels,
-                                                          static_cast<float *>(G), ld_g, row_loss, inv_n); GNN_LAUNCHED(1); }
-        }
-        GNN_CUDA_TRY(cudaGetLastError());
+        gnn_status st;
+        if (dt == GNN_BF16 && gdt == GNN_BF16)
+            st = softmax_rows_typed<__nv_bfloat16, __nv_bfloat16>(logits, ld, n, C, labels, G, ld_g, row_loss, inv_n, s);
+        else if (dt == GNN_BF16)
+            st = softmax_rows_typed<__nv_bfloat16, float>(logits, ld, n, C, labels, G, ld_g, row_loss, inv_n, s);
+        else if (gdt == GNN_BF16)
+            st = softmax_rows_typed<float, __nv_bfloat16>(logits, ld, n, C, labels, G, ld_g, row_loss, inv_n, s);
+        else
+            st = softmax_rows_typed<float, float>(logits, ld, n, C, labels, G, ld_g, row_loss, inv_n, s);
+        if (st != GNN_OK) return st;
     }
     const int64_t n_chunks = ceil_div(n, kLossChunk);
     if (n_chunks > 0) {

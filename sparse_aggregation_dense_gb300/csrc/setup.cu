@@ -240,6 +240,21 @@ __global__ void entry_weights_kernel(const int32_t *__restrict__ rowptr, const i
     }
 }
 
+// the sign bit of the weight of every row's last entry marks the row's end
+__global__ void mark_row_ends_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, float *__restrict__ w) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= n_rows) return;
+    const int32_t e = rowptr[r + 1];
+    if (e > rowptr[r]) w[e - 1] = __uint_as_float(__float_as_uint(w[e - 1]) | 0x80000000u);
+}
+
+gnn_status launch_mark_row_ends(const int32_t *rowptr, int64_t n_rows, float *w, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    { mark_row_ends_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, s>>>(rowptr, n_rows, w); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
 gnn_status launch_entry_weights(const int32_t *rowptr, const int32_t *colidx, int64_t n_rows, const float *colw,
                                 bool skip_self, float *w, cudaStream_t s) {
     if (n_rows == 0) return GNN_OK;
@@ -394,13 +409,19 @@ gnn_status csr_transpose(const int32_t *rowptr, const int32_t *colidx, int64_t n
 // ---------------------------------------------------------------------------
 // heavy-row schedule
 // ---------------------------------------------------------------------------
+// Rows the fix-up writes: heavy rows (their chunk partials summed) and empty
+// rows (no chunk: the fix-up writes their zero / self term).  Row groups hold
+// the other rows, each with at least one entry, so the end of every row of a
+// group is marked on an entry.
+__device__ __forceinline__ bool fixup_row(int32_t d) { return d > kHeavyNnz || d == 0; }
+
 __global__ void sched_count_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, int32_t *nch, int32_t *flag) {
     int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= n_rows) return;
     int32_t d = rowptr[r + 1] - rowptr[r];
     int32_t c = d > kHeavyNnz ? (d + kChunkNnz - 1) / kChunkNnz : 0;
     nch[r] = c;
-    flag[r] = c > 0;
+    flag[r] = fixup_row(d);
 }
 
 __global__ void sched_fill_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, const int32_t *__restrict__ choff,
@@ -409,7 +430,7 @@ __global__ void sched_fill_kernel(const int32_t *__restrict__ rowptr, int64_t n_
     int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= n_rows) return;
     int32_t c0 = choff[r], c1 = choff[r + 1];
-    if (c1 == c0) return;
+    if (hidx[r + 1] == hidx[r]) return;  // not a fix-up row
     int32_t h = hidx[r];
     heavy_rows[h] = (int32_t)r;
     heavy_choff[h] = c0;
@@ -423,11 +444,11 @@ __global__ void sched_fill_kernel(const int32_t *__restrict__ rowptr, int64_t n_
     }
 }
 
-// row r (light) starts a group when it is the first row, follows a heavy row,
-// starts in another kGroupNnz-entry window than row r - 1, or is a multiple of
-// kGroupRows
+// row r (light) starts a group when it is the first row, follows a fix-up row
+// (heavy or empty), starts in another kGroupNnz-entry window than row r - 1,
+// or is a multiple of kGroupRows
 __device__ __forceinline__ bool is_heavy_row(const int32_t *__restrict__ rowptr, int64_t r) {
-    return rowptr[r + 1] - rowptr[r] > kHeavyNnz;
+    return fixup_row(rowptr[r + 1] - rowptr[r]);
 }
 __global__ void group_flag_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, int32_t *flag) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

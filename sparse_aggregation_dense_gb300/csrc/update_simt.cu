@@ -23,11 +23,14 @@ __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v) { *p = __floa
 
 // C[n x N] = A[n x K] * B[K x N]; A element (i, k) and B element (k, j) come
 // from the loaders; 4 x 4 outputs per thread.
-template <typename T, int AMODE>
-__global__ void __launch_bounds__(NT) gemm_simt_kernel(const T *__restrict__ A, int64_t lda, const T *__restrict__ M,
-                                                       int64_t ldm, const float *__restrict__ Wp, int64_t ldw,
-                                                       int64_t n, int64_t K, int64_t N, int relu,
-                                                       T *__restrict__ C, int64_t ldc) {
+// A and C have type TA (the forward's Z and H_out, or the backward's G and dZ),
+// the mask operand M the activations' type TM.
+template <typename TA, typename TM, int AMODE>
+__global__ void __launch_bounds__(NT) gemm_simt_kernel(const TA *__restrict__ A, int64_t lda,
+                                                       const TM *__restrict__ M, int64_t ldm,
+                                                       const float *__restrict__ Wp, int64_t ldw, int64_t n,
+                                                       int64_t K, int64_t N, int relu, TA *__restrict__ C,
+                                                       int64_t ldc) {
     // AMODE 0: A = Z (n x K), B[k][j] = Wp[k][j]          (forward)
     // AMODE 1: A = dY = G * mask (n x K=N_out), B[k][j] = Wp[j][k]   (dZ = dY Wp^T)
     __shared__ float As[BK][BM + 4];
@@ -46,6 +49,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const T *__restrict__ A, 
             if (i < n && k < K) {
                 a = ld_elem(A + i * lda + k);
                 if (AMODE == 1 && relu && !(ld_elem(M + i * ldm + k) > 0.f)) a = 0.f;
+                // bf16 activations: dY is a bf16 operand of the products, as on the tensor cores
+                if (AMODE == 1 && sizeof(TA) == 4 && sizeof(TM) == 2) a = __bfloat162float(__float2bfloat16_rn(a));
             }
             As[kk][mm] = a;
             int kb = idx / BN, jb = idx % BN;
@@ -86,8 +91,9 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const T *__restrict__ A, 
 }
 
 // dWp partial of one row slab: P[s][k][j] = sum_{i in slab s} Z[i][k] * dY[i][j]
-template <typename T>
-__global__ void __launch_bounds__(NT) wgrad_simt_kernel(const T *__restrict__ Z, int64_t ldz, const T *__restrict__ G,
+// Z and H_out have the activations' type T, G the gradients' type TG
+template <typename T, typename TG>
+__global__ void __launch_bounds__(NT) wgrad_simt_kernel(const T *__restrict__ Z, int64_t ldz, const TG *__restrict__ G,
                                                         int64_t ldg, const T *__restrict__ Hout, int64_t ldh, int relu,
                                                         int64_t n, int64_t Kp, int64_t N, int64_t rows_per_slab,
                                                         float *__restrict__ P) {
@@ -112,6 +118,8 @@ __global__ void __launch_bounds__(NT) wgrad_simt_kernel(const T *__restrict__ Z,
                 if (j0 + cc < N) {
                     y = ld_elem(G + i * ldg + j0 + cc);
                     if (relu && !(ld_elem(Hout + i * ldh + j0 + cc) > 0.f)) y = 0.f;
+                    // bf16 activations: dY is a bf16 operand of the products, as on the tensor cores
+                    if (sizeof(TG) == 4 && sizeof(T) == 2) y = __bfloat162float(__float2bfloat16_rn(y));
                 }
             }
             Zs[ii][cc] = z;
@@ -178,29 +186,29 @@ template <typename T>
 gnn_status update_fwd_t(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
                         int relu, void *out, int64_t ld_o, cudaStream_t s) {
     dim3 grid((unsigned)ceil_div(n, BM), (unsigned)ceil_div(N, BN));
-    { gemm_simt_kernel<T, 0><<<grid, NT, 0, s>>>(static_cast<const T *>(Z), ld_z, nullptr, 0, Wp, ld_w, n, Kp, N, relu,
-                                               static_cast<T *>(out), ld_o); GNN_LAUNCHED(1); }
+    { gemm_simt_kernel<T, T, 0><<<grid, NT, 0, s>>>(static_cast<const T *>(Z), ld_z, nullptr, 0, Wp, ld_w, n, Kp, N,
+                                                  relu, static_cast<T *>(out), ld_o); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }
 
-template <typename T>
+template <typename T, typename TG>
 gnn_status update_bwd_t(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                         int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N, float *dWp,
                         void *dZ, int64_t ld_dz, float *ws, cudaStream_t s) {
-    const T *Gt = static_cast<const T *>(G);
+    const TG *Gt = static_cast<const TG *>(G);
     const T *Ht = static_cast<const T *>(Hout);
     if (dZ) {
         dim3 grid((unsigned)ceil_div(n, BM), (unsigned)ceil_div(Kp, BN));
-        { gemm_simt_kernel<T, 1><<<grid, NT, 0, s>>>(Gt, ld_g, Ht, ld_h, Wp, ld_w, n, N, Kp, relu,
-                                                   static_cast<T *>(dZ), ld_dz); GNN_LAUNCHED(1); }
+        { gemm_simt_kernel<TG, T, 1><<<grid, NT, 0, s>>>(Gt, ld_g, Ht, ld_h, Wp, ld_w, n, N, Kp, relu,
+                                                       static_cast<TG *>(dZ), ld_dz); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
     }
     const int64_t slabs = wgrad_slabs(n, Kp, N, sizeof(T) == 4);
     const int64_t rows_per_slab = ceil_div(n, slabs);
     dim3 grid((unsigned)ceil_div(N, BN), (unsigned)ceil_div(Kp, BM), (unsigned)slabs);
-    { wgrad_simt_kernel<T><<<grid, NT, 0, s>>>(static_cast<const T *>(Z), ld_z, Gt, ld_g, Ht, ld_h, relu, n, Kp, N,
-                                             rows_per_slab, ws); GNN_LAUNCHED(1); }
+    { wgrad_simt_kernel<T, TG><<<grid, NT, 0, s>>>(static_cast<const T *>(Z), ld_z, Gt, ld_g, Ht, ld_h, relu, n, Kp,
+                                                  N, rows_per_slab, ws); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     { sum_slabs_kernel<<<(unsigned)ceil_div(Kp * N, 256), 256, 0, s>>>(ws, slabs, Kp * N, dWp); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
@@ -222,17 +230,21 @@ gnn_status launch_update_fwd(const void *Z, int64_t ld_z, int64_t n, int64_t Kp,
 
 gnn_status launch_update_bwd(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                              int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
-                             float *dWp, void *dZ, int64_t ld_dz, gnn_dtype dt, float *ws, size_t ws_bytes,
-                             cudaStream_t s) {
+                             float *dWp, void *dZ, int64_t ld_dz, gnn_dtype dt, gnn_dtype gdt, float *ws,
+                             size_t ws_bytes, cudaStream_t s) {
     if (ws_bytes < update_bwd_ws_bytes(n, Kp, N, dt)) return GNN_EINVAL;
     if (n == 0) {
         GNN_CUDA_TRY(cudaMemsetAsync(dWp, 0, (size_t)Kp * (size_t)N * sizeof(float), s));
         return GNN_OK;
     }
+    if (dt == GNN_BF16 && gdt == GNN_BF16)
+        return update_bwd_t<__nv_bfloat16, __nv_bfloat16>(G, ld_g, Hout, ld_h, relu, Z, ld_z, n, Kp, Wp, ld_w, N, dWp,
+                                                          dZ, ld_dz, ws, s);
     if (dt == GNN_BF16)
-        return update_bwd_t<__nv_bfloat16>(G, ld_g, Hout, ld_h, relu, Z, ld_z, n, Kp, Wp, ld_w, N, dWp, dZ, ld_dz, ws,
-                                           s);
-    return update_bwd_t<float>(G, ld_g, Hout, ld_h, relu, Z, ld_z, n, Kp, Wp, ld_w, N, dWp, dZ, ld_dz, ws, s);
+        return update_bwd_t<__nv_bfloat16, float>(G, ld_g, Hout, ld_h, relu, Z, ld_z, n, Kp, Wp, ld_w, N, dWp, dZ,
+                                                  ld_dz, ws, s);
+    if (gdt != GNN_F32) return GNN_EINVAL;
+    return update_bwd_t<float, float>(G, ld_g, Hout, ld_h, relu, Z, ld_z, n, Kp, Wp, ld_w, N, dWp, dZ, ld_dz, ws, s);
 }
 
 }  // namespace gnn

@@ -28,7 +28,7 @@ constexpr int kDRows = 128;  // dgrad rows per tile
 constexpr int kWRows = 64;   // wgrad rows per tile
 constexpr int kBoxD = kDRows * 128;  // one 64-column bf16 box of a dgrad tile
 constexpr int kBoxW = kWRows * 128;  // one 64-column bf16 box of a wgrad tile
-constexpr int kStageOut = 32 * 128;           // one 32-row x 64-column bf16 dZ tile (TMA store source)
+constexpr int kStageOut = 32 * 128;           // one 32-row x 128-byte dZ tile (TMA store source)
 constexpr int kOutBytes = 4 * 2 * kStageOut;  // 4 epilogue warps x 2 buffers
 
 struct BarsB {
@@ -92,7 +92,7 @@ __device__ __forceinline__ void init_common(BarsB *bars, int stages, uint32_t te
 __global__ void __launch_bounds__(kThreadsB, 1)
     update_dgrad_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapH,
                            const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapO,
-                           int Kp_pad, int NC, int stages, int relu, int64_t n_tiles, int *err) {
+                           int Kp_pad, int NC, int stages, int relu, int out_f32, int64_t n_tiles, int *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int w_chunk = Kp_pad * 128;
@@ -223,43 +223,64 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             }
         }
     } else {
-        // epilogue: TMEM -> bf16 -> swizzled 32 x 64 staging tile -> TMA store
-        // (rows and columns past dZ's edge are not written)
+        // epilogue: TMEM -> a swizzled staging tile of 32 rows x 128 bytes (64 bf16
+        // or 32 fp32 columns) -> TMA store (rows and columns past dZ's edge are
+        // not written)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t *stage_out = sO + (warp - 2) * 2 * kStageOut;
+        const int cstep = out_f32 ? 32 : 64;  // columns per 128-byte staging row
         int acc = 0, ob = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
             if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, abort_flag)) break;
             tc::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride;
-            for (int cc = 0; cc < Kp_pad; cc += 64) {
+            for (int cc = 0; cc < Kp_pad; cc += cstep) {
                 // the TMA store that last read this buffer must be done with it
                 if (lane == 0) tc::bulk_wait_read<1>();
                 __syncwarp();
                 uint8_t *buf = stage_out + ob * kStageOut;
+                uint8_t *rowp = buf + lane * 128;
+                if (out_f32) {
 #pragma unroll
-                for (int sub = 0; sub < 4; ++sub) {
-                    const int c = cc + sub * 16;
-                    uint32_t r[16];
-                    if (c < Kp_pad) {
-                        tc::tmem_ld16(taddr + (uint32_t)c, r);
-                    } else {
+                    for (int sub = 0; sub < 2; ++sub) {
+                        const int c = cc + sub * 16;
+                        uint32_t r[16];
+                        if (c < Kp_pad) {
+                            tc::tmem_ld16(taddr + (uint32_t)c, r);
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = 0u;
+                            for (int i = 0; i < 16; ++i) r[i] = 0u;
+                        }
+                        // 16-byte chunks 4*sub .. 4*sub+3 of this thread's row, 128-byte swizzle
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4 *>(rowp + (((4 * sub + j) ^ (lane & 7)) * 16)) =
+                                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                     }
-                    // 16-byte chunks 2*sub and 2*sub+1 of this thread's 128-byte row, 128-byte swizzle
-                    uint4 lo = make_uint4(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                                          pack2(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                                          pack2(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                                          pack2(__uint_as_float(r[6]), __uint_as_float(r[7])));
-                    uint4 hi = make_uint4(pack2(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                                          pack2(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                                          pack2(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                                          pack2(__uint_as_float(r[14]), __uint_as_float(r[15])));
-                    uint8_t *rowp = buf + lane * 128;
-                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub) ^ (lane & 7)) * 16)) = lo;
-                    *reinterpret_cast<uint4 *>(rowp + (((2 * sub + 1) ^ (lane & 7)) * 16)) = hi;
+                } else {
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) {
+                        const int c = cc + sub * 16;
+                        uint32_t r[16];
+                        if (c < Kp_pad) {
+                            tc::tmem_ld16(taddr + (uint32_t)c, r);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) r[i] = 0u;
+                        }
+                        // 16-byte chunks 2*sub and 2*sub+1 of this thread's 128-byte row, 128-byte swizzle
+                        uint4 lo = make_uint4(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                              pack2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                              pack2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                              pack2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+                        uint4 hi = make_uint4(pack2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                              pack2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                              pack2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                              pack2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+                        *reinterpret_cast<uint4 *>(rowp + (((2 * sub) ^ (lane & 7)) * 16)) = lo;
+                        *reinterpret_cast<uint4 *>(rowp + (((2 * sub + 1) ^ (lane & 7)) * 16)) = hi;
+                    }
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && bars->abort_flag) atomicOr(err, 2);
+    if (threadIdx.x == 0 && bars->abort_flag) atomicOr(err, kErrWaitTc);
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem_base, ncols);
@@ -429,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && bars->abort_flag) atomicOr(err, 2);
+    if (threadIdx.x == 0 && bars->abort_flag) atomicOr(err, kErrWaitTc);
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem_base, ncols);
@@ -451,6 +472,37 @@ __global__ void sum_partials_kernel(const float *__restrict__ P, int64_t parts, 
     double s = 0.0;
     for (int64_t q = 0; q < parts; ++q) s += (double)P[q * KN + x];
     out[x] = (float)s;
+}
+
+// dY = bf16(relu ? G * 1[H_out > 0] : G), eight columns per thread (two 16-byte
+// loads of G, one of H_out, one 16-byte store); the group that straddles N
+// reads element by element, and columns [N, ld_y) are written as zero.
+__global__ void grad_to_bf16_kernel(const float *__restrict__ G, int64_t ld_g, const __nv_bfloat16 *__restrict__ H,
+                                    int64_t ld_h, int64_t n, int64_t N, int64_t groups, __nv_bfloat16 *__restrict__ Y,
+                                    int64_t ld_y) {
+    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= n * groups) return;
+    const int64_t r = x / groups, c0 = (x % groups) * 8;
+    const float *g = G + r * ld_g + c0;
+    float v[8];
+    if (c0 + 8 <= N) {
+        const float4 a = *reinterpret_cast<const float4 *>(g), b = *reinterpret_cast<const float4 *>(g + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = c0 + k < N ? g[k] : 0.f;
+    }
+    if (H) {
+        const uint4 h = *reinterpret_cast<const uint4 *>(H + r * ld_h + c0);  // c0 + 8 <= ld_h: ld_h is a multiple of 8
+        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (!(__uint_as_float(hw[k] << 16) > 0.f)) v[2 * k] = 0.f;
+            if (!(__uint_as_float(hw[k] & 0xffff0000u) > 0.f)) v[2 * k + 1] = 0.f;
+        }
+    }
+    *reinterpret_cast<uint4 *>(Y + r * ld_y + c0) =
+        make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
 
 struct BwdPlan {
@@ -484,6 +536,18 @@ bool plan_bwd(int64_t Kp, int64_t N, int relu, BwdPlan *p) {
 
 }  // namespace
 
+gnn_status launch_grad_to_bf16(const float *G, int64_t ld_g, const void *Hout, int64_t ld_h, int64_t n, int64_t N,
+                               void *Y, int64_t ld_y, cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    if (ld_y % 8 != 0 || ld_y < N) return GNN_EINVAL;
+    const int64_t groups = ld_y / 8;
+    { grad_to_bf16_kernel<<<(unsigned)ceil_div(n * groups, 256), 256, 0, s>>>(
+        G, ld_g, static_cast<const __nv_bfloat16 *>(Hout), ld_h, n, N, groups, static_cast<__nv_bfloat16 *>(Y),
+        ld_y); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
 bool update_bwd_tc_supported(int64_t Kp, int64_t N) {
     BwdPlan p;
     return plan_bwd(Kp, N, 1, &p);
@@ -498,7 +562,7 @@ size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp, int64_t N) {
 
 gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                                 int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
-                                float *dWp, void *dZ, int64_t ld_dz, void *ws, int *err, cudaStream_t s) {
+                                float *dWp, void *dZ, int64_t ld_dz, bool dz_f32, void *ws, int *err, cudaStream_t s) {
     BwdPlan p;
     if (!plan_bwd(Kp, N, relu, &p)) return GNN_EUNSUPPORTED;
     if (n == 0) {
@@ -538,13 +602,15 @@ gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, i
                           (uint32_t)p.Kp_pad))
         return GNN_ECUDA;
     CUtensorMap mO;
-    if (!make_map_bf16_2d(&mO, dZ, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_dz * 2, 64, 32)) return GNN_ECUDA;
+    if (dz_f32 ? !make_map_f32_2d(&mO, dZ, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_dz * 4, 32, 32)
+               : !make_map_bf16_2d(&mO, dZ, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_dz * 2, 64, 32))
+        return GNN_ECUDA;
     GNN_CUDA_TRY(cudaFuncSetAttribute(update_dgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)p.dsmem));
     const int64_t dtiles = ceil_div(n, kDRows);
     const int64_t dgrid = dtiles < num_sms() ? dtiles : num_sms();
     { update_dgrad_tc_kernel<<<(unsigned)dgrid, kThreadsB, p.dsmem, s>>>(
-        mG, mH, mW, mO, (int)p.Kp_pad, (int)p.NC, p.dstages, relu, dtiles, err); GNN_LAUNCHED(1); }
+        mG, mH, mW, mO, (int)p.Kp_pad, (int)p.NC, p.dstages, relu, dz_f32 ? 1 : 0, dtiles, err); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

@@ -21,9 +21,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgnn.so")
 
-GNN_OK, GNN_EINVAL, GNN_ENOMEM, GNN_ECUDA, GNN_EUNSUPPORTED, GNN_EINDEX = range(6)
+GNN_OK, GNN_EINVAL, GNN_ENOMEM, GNN_ECUDA, GNN_EUNSUPPORTED, GNN_EINDEX, GNN_ETIMEOUT = range(7)
 GNN_F32, GNN_BF16 = 0, 1
-GNN_AGG_GCN_SYM, GNN_AGG_SAGE_MEAN = 0, 1
+GNN_AGG_GCN_SYM, GNN_AGG_SAGE_MEAN, GNN_AGG_GAT = 0, 1, 2
 
 EXPORTS = (
     "gnn_graph_create", "gnn_graph_destroy", "gnn_halo_pull", "gnn_halo_push", "gnn_sage_half_offset",
@@ -31,7 +31,8 @@ EXPORTS = (
     "gnn_graph_copy_transpose", "gnn_status_string", "gnn_last_cuda_error", "gnn_halo_push_quantized",
     "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv",
     "gnn_layer_forward_narrow", "gnn_layer_backward_narrow", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
-    "gnn_aggregate_forward_noalloc",
+    "gnn_aggregate_forward_noalloc", "gnn_debug_expire_next_wait", "gnn_gather_rows", "gnn_scatter_add_rows",
+    "gnn_gat_forward", "gnn_gat_backward",
 )
 
 PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
@@ -66,12 +67,12 @@ def _lib():
         L.gnn_sage_half_offset.restype = i64
         L.gnn_layer_forward.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
         L.gnn_layer_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp, i64, i32,
-                                         i32, vp]
-        L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, vp]
+                                         i32, i32, vp]
+        L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, i32, vp]
         L.gnn_layer_forward_narrow.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
         L.gnn_layer_backward_narrow.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp,
                                                 i64, i32, vp]
-        L.gnn_softmax_ce_partial.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp]
+        L.gnn_softmax_ce_partial.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i64, i32, i32, vp]
         L.gnn_halo_grad_send.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
         L.gnn_halo_grad_recv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i32, vp]
         L.gnn_get_error.argtypes = [vp]
@@ -80,6 +81,12 @@ def _lib():
         L.gnn_profile_enable.argtypes = [vp, i32]
         L.gnn_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
         L.gnn_aggregate_forward_noalloc.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp]
+        L.gnn_debug_expire_next_wait.argtypes = [i64]
+        L.gnn_gat_forward.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, vp, i64, vp, vp, vp, i64, i32, vp]
+        L.gnn_gat_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, i64, vp, vp, vp, i64, i32, vp, i64, vp, vp, vp,
+                                       vp, vp, vp, i64, vp, i64, i32, i32, vp]
+        L.gnn_gather_rows.argtypes = [vp, i64, i64, vp, i64, vp, i64, i64, i32, vp, vp]
+        L.gnn_scatter_add_rows.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i32, vp, vp]
         L.gnn_launch_count.argtypes = []
         L.gnn_launch_count.restype = i64
         L.gnn_status_string.argtypes = [i32]
@@ -146,7 +153,7 @@ def _mat(t: torch.Tensor) -> Tuple[int, int]:
 
 
 def agg_code(agg: str) -> int:
-    return {"gcn": GNN_AGG_GCN_SYM, "sage": GNN_AGG_SAGE_MEAN}[agg]
+    return {"gcn": GNN_AGG_GCN_SYM, "sage": GNN_AGG_SAGE_MEAN, "gat": GNN_AGG_GAT}[agg]
 
 
 def _k(g, f_in: int) -> int:
@@ -249,6 +256,94 @@ def aggregate_forward_noalloc(g: Graph, H: torch.Tensor, Z: torch.Tensor):
     _check(_lib().gnn_aggregate_forward_noalloc(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f, _ptr(Z), ld_z,
                                                 _dtype(H), ctypes.c_void_p(_stream())),
            "gnn_aggregate_forward_noalloc")
+
+
+def debug_expire_next_wait(wait_ns: int):
+    """Failure-detection test hook: the next aggregation's first batch is never issued, so its bounded wait runs
+    out after wait_ns and the call's graph reports GNN_ETIMEOUT (nothing faults)."""
+    _check(_lib().gnn_debug_expire_next_wait(int(wait_ns)), "gnn_debug_expire_next_wait")
+
+
+def _vec(what: str, t: torch.Tensor, n: int, name: str):
+    _need(t.dtype == torch.float32 and t.is_contiguous() and t.numel() == n, what,
+          f"{name} must be a contiguous float32 vector of {n} values")
+
+
+def gat_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Tensor, relu: bool,
+                T: torch.Tensor, scores: torch.Tensor, alpha: torch.Tensor, H_out: torch.Tensor):
+    """Graph attention layer: T = H W (every row), scores, alpha (per entry), H_out = act(sum alpha T)."""
+    ld_h, f_in = _mat(H)
+    ld_t, _ = _mat(T)
+    ld_o, f_out = _mat(H_out)
+    what = "gnn_gat_forward"
+    _need(g.agg == "gat", what, "the graph was not created for attention")
+    _weights(what, W, f_in, f_out)
+    _vec(what, a_src, f_out, "a_src")
+    _vec(what, a_dst, f_out, "a_dst")
+    _vec(what, scores, g.n_total + g.n_local, "scores")
+    _vec(what, alpha, max(g.nnz, 0), "alpha")
+    _need(H.dtype == T.dtype == H_out.dtype, what, "H, T and H_out share a dtype")
+    _need(_rows(H) >= g.n_total and _rows(T) >= g.n_total and _rows(H_out) >= g.n_local and _width(T) >= f_out, what,
+          "H and T need n_local + n_halo rows, H_out n_local rows")
+    _check(_lib().gnn_gat_forward(ctypes.c_void_p(g.handle), _ptr(H), ld_h, f_in, _ptr(W), _ptr(a_src), _ptr(a_dst),
+                                  f_out, int(relu), _ptr(T), ld_t, _ptr(scores), _ptr(alpha), _ptr(H_out), ld_o,
+                                  _dtype(H), ctypes.c_void_p(_stream())), what)
+
+
+def gat_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, H: torch.Tensor, W: torch.Tensor,
+                 a_src: torch.Tensor, a_dst: torch.Tensor, relu: bool, T: torch.Tensor, scores: torch.Tensor,
+                 alpha: torch.Tensor, dW: torch.Tensor, da_src: torch.Tensor, da_dst: torch.Tensor, dT: torch.Tensor,
+                 dH: Optional[torch.Tensor] = None):
+    """Backward of gat_forward: dW, da_src, da_dst, the work dT, and dH (every row) unless dH is None."""
+    ld_g, f_out = _mat(G)
+    ld_o, _ = _mat(H_out)
+    ld_h, f_in = _mat(H)
+    ld_t, _ = _mat(T)
+    ld_dt, _ = _mat(dT)
+    ld_dh = _mat(dH)[0] if dH is not None else 0
+    what = "gnn_gat_backward"
+    _need(g.agg == "gat", what, "the graph was not created for attention")
+    _weights(what, W, f_in, f_out)
+    _weights(what, dW, f_in, f_out)
+    for name, t in (("a_src", a_src), ("a_dst", a_dst), ("da_src", da_src), ("da_dst", da_dst)):
+        _vec(what, t, f_out, name)
+    _vec(what, scores, g.n_total + g.n_local, "scores")
+    _vec(what, alpha, max(g.nnz, 0), "alpha")
+    _need(H_out.dtype == H.dtype == T.dtype, what, "H_out, H and T share the activations' dtype")
+    _need(all(t is None or t.dtype == G.dtype for t in (dT, dH)), what, "G, dT and dH share the gradients' dtype")
+    _need(not (H.dtype == torch.float32 and G.dtype != torch.float32), what, "fp32 activations take fp32 gradients")
+    _need(_rows(G) >= g.n_local and _rows(H_out) >= g.n_local and _rows(H) >= g.n_total and _rows(T) >= g.n_total
+          and _rows(dT) >= g.n_total and _width(dT) >= f_out, what, "row counts of G, H_out, H, T and dT")
+    _need(dH is None or (_rows(dH) >= g.n_total and _width(dH) >= f_in), what,
+          "dH needs n_local + n_halo rows of f_in columns")
+    _check(_lib().gnn_gat_backward(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(H), ld_h, f_in,
+                                   _ptr(W), _ptr(a_src), _ptr(a_dst), f_out, int(relu), _ptr(T), ld_t, _ptr(scores),
+                                   _ptr(alpha), _ptr(dW), _ptr(da_src), _ptr(da_dst), _ptr(dT), ld_dt, _ptr(dH), ld_dh,
+                                   _dtype(H), _dtype(G), ctypes.c_void_p(_stream())), what)
+
+
+def gather_rows(src: torch.Tensor, ids: torch.Tensor, dst: torch.Tensor, err: Optional[torch.Tensor] = None):
+    """dst[i] = src[ids[i]] over the columns of dst's view (a bit-exact row copy)."""
+    ld_s, _ = _mat(src)
+    ld_d, f = _mat(dst)
+    what = "gnn_gather_rows"
+    _need(src.dtype == dst.dtype and ids.dtype == torch.int64, what, "src and dst share a dtype; int64 ids")
+    _need(_numel(ids) >= _rows(dst) and _width(src) >= f, what, "an id per dst row; src as wide as dst's view")
+    _need(err is None or err.dtype == torch.int32, what, "int32 error word")
+    _check(_lib().gnn_gather_rows(_ptr(src), ld_s, _rows(src), _ptr(ids), _rows(dst), _ptr(dst), ld_d, f,
+                                  _dtype(dst), _ptr(err), ctypes.c_void_p(_stream())), what)
+
+
+def scatter_add_rows(src: torch.Tensor, ids: torch.Tensor, dst: torch.Tensor, err: Optional[torch.Tensor] = None):
+    """dst[ids[i]] += src[i] over the columns of src's view (fp32 sums; ids distinct)."""
+    ld_s, f = _mat(src)
+    ld_d, _ = _mat(dst)
+    what = "gnn_scatter_add_rows"
+    _need(src.dtype == dst.dtype and ids.dtype == torch.int64, what, "src and dst share a dtype; int64 ids")
+    _need(_numel(ids) >= _rows(src) and _width(dst) >= f, what, "an id per src row; dst as wide as src's view")
+    _need(err is None or err.dtype == torch.int32, what, "int32 error word")
+    _check(_lib().gnn_scatter_add_rows(_ptr(src), ld_s, _ptr(ids), _rows(src), _ptr(dst), ld_d, _rows(dst), f,
+                                       _dtype(src), _ptr(err), ctypes.c_void_p(_stream())), what)
 
 
 def launch_count() -> int:
@@ -386,17 +481,23 @@ def layer_forward(g: Graph, H: torch.Tensor, W: torch.Tensor, relu: bool, Z: tor
 def layer_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tensor, W: torch.Tensor, relu: bool,
                    dW: torch.Tensor, f_in: int, dZ: Optional[torch.Tensor] = None, dH: Optional[torch.Tensor] = None,
                    want_halo_grad: bool = False):
-    """dW = Z^T dY; with dH: dZ = dY W^T and dH = A_block^T dZ (halo rows too if want_halo_grad)."""
+    """dW = Z^T dY; with dH: dZ = dY W^T and dH = A_block^T dZ (halo rows too if want_halo_grad).
+
+    The activations (H_out, Z) share one dtype, the gradients (G, dZ, dH) another:
+    fp32 activations take fp32 gradients, bf16 activations bf16 or fp32 gradients."""
     ld_g, f_out = _mat(G)
     ld_o, _ = _mat(H_out)
     ld_z, _ = _mat(Z)
     ld_dz = _mat(dZ)[0] if dZ is not None else 0
     ld_dh = _mat(dH)[0] if dH is not None else 0
     what = "gnn_layer_backward"
-    K, Kp = _k(g, f_in), _z_width(g, f_in, G.dtype)
+    K, Kp = _k(g, f_in), _z_width(g, f_in, Z.dtype)
     _weights(what, W, K, f_out)
     _weights(what, dW, K, f_out)
-    _need(all(t is None or t.dtype == G.dtype for t in (H_out, Z, dZ, dH)), what, "activations share one dtype")
+    _need(H_out.dtype == Z.dtype, what, "H_out and Z share the activations' dtype")
+    _need(all(t is None or t.dtype == G.dtype for t in (dZ, dH)), what, "G, dZ and dH share the gradients' dtype")
+    _need(not (Z.dtype == torch.float32 and G.dtype != torch.float32), what,
+          "fp32 activations take fp32 gradients")
     _need(_rows(G) >= g.n_local and _rows(H_out) >= g.n_local and _rows(Z) >= g.n_local, what,
           "G, H_out and Z need n_local rows")
     _need(_width(Z) >= Kp, what, "Z is narrower than the aggregation output")
@@ -405,7 +506,7 @@ def layer_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tens
           "dH needs n_local rows (n_local + n_halo with the halo gradient) of f_in columns")
     _check(_lib().gnn_layer_backward(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(Z), ld_z,
                                      _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(dZ), ld_dz, _ptr(dH), ld_dh,
-                                     int(want_halo_grad), _dtype(G), ctypes.c_void_p(_stream())),
+                                     int(want_halo_grad), _dtype(Z), _dtype(G), ctypes.c_void_p(_stream())),
            "gnn_layer_backward")
 
 
@@ -413,18 +514,20 @@ def _softmax_args(what: str, logits, labels, G, row_loss, loss):
     n, C = int(logits.shape[0]), int(logits.shape[1])
     _need(labels.dtype == torch.int32 and row_loss.dtype == torch.float32 and loss.dtype == torch.float32, what,
           "int32 labels, float32 row_loss and loss")
-    _need(G.dtype == logits.dtype and _rows(G) >= n and _width(G) >= C, what, "G shaped like the logits")
+    _need(G.dtype in (torch.float32, torch.bfloat16) and _rows(G) >= n and _width(G) >= C, what,
+          "G (fp32 or bf16) shaped like the logits")
     _need(_numel(labels) >= n and _numel(row_loss) >= n and _numel(loss) >= 1, what,
           "a label and a row_loss entry per row, one loss")
 
 
 def softmax_ce(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_loss: torch.Tensor,
                loss: torch.Tensor):
+    """Mean softmax cross-entropy of the rows of logits; G (in its own dtype) = (softmax - onehot) / n."""
     ld, C = _mat(logits)
     ld_g, _ = _mat(G)
     _softmax_args("gnn_softmax_ce", logits, labels, G, row_loss, loss)
     _check(_lib().gnn_softmax_ce(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g, _ptr(row_loss),
-                                 _ptr(loss), _dtype(logits), ctypes.c_void_p(_stream())), "gnn_softmax_ce")
+                                 _ptr(loss), _dtype(logits), _dtype(G), ctypes.c_void_p(_stream())), "gnn_softmax_ce")
 
 
 def softmax_ce_partial(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tensor, row_loss: torch.Tensor,
@@ -434,7 +537,7 @@ def softmax_ce_partial(logits: torch.Tensor, labels: torch.Tensor, G: torch.Tens
     ld_g, _ = _mat(G)
     _softmax_args("gnn_softmax_ce_partial", logits, labels, G, row_loss, loss)
     _check(_lib().gnn_softmax_ce_partial(_ptr(logits), ld, logits.shape[0], C, _ptr(labels), _ptr(G), ld_g,
-                                         _ptr(row_loss), _ptr(loss), int(n_mean), _dtype(logits),
+                                         _ptr(row_loss), _ptr(loss), int(n_mean), _dtype(logits), _dtype(G),
                                          ctypes.c_void_p(_stream())), "gnn_softmax_ce_partial")
 
 

@@ -38,7 +38,8 @@ from .partition_model import PartitionModel, ld_for
 
 class MultiPartitionTrainer:
     def __init__(self, parts, widths: Sequence[int], agg: str, dtype: torch.dtype, n_table: int,
-                 mode: str = "sync", sync_every: int = 0, device="cuda", narrow: bool = False):
+                 mode: str = "sync", sync_every: int = 0, device="cuda", narrow: bool = False,
+                 grad_dtype: torch.dtype = torch.float32):
         assert mode in ("sync", "stale")
         self.parts = list(parts)
         self.widths = list(widths)
@@ -46,8 +47,8 @@ class MultiPartitionTrainer:
         self.mode, self.sync_every = mode, sync_every
         self.dtype = dtype
         self.n_table = n_table
-        self.models: List[PartitionModel] = [PartitionModel(p, widths, agg, dtype, device, narrow=narrow)
-                                             for p in self.parts]
+        self.models: List[PartitionModel] = [PartitionModel(p, widths, agg, dtype, device, narrow=narrow,
+                                                            grad_dtype=grad_dtype) for p in self.parts]
         self.n_rows = sum(m.n_local for m in self.models)
         dev = torch.device(device)
         # representation tables (current and, for the stale schedule, next) and gradient tables

@@ -39,11 +39,18 @@ class PartitionModel:
 
     part: an object with rowptr, colidx (int32 numpy), n_local, n_halo, deg (float32 numpy or
     None), local_ids, halo_ids (int64 numpy), n_table.
-    widths: [f_0, ..., f_L]; agg "gcn" | "sage"; dtype torch.float32 | torch.bfloat16.
+    widths: [f_0, ..., f_L]; agg "gcn" | "sage"; dtype torch.float32 | torch.bfloat16: the activations
+    (features, tables, Z, layer outputs).  grad_dtype: the activation gradients (G, dZ, dH); fp32 by default,
+    bf16 allowed with bf16 activations.
     """
 
     def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda",
-                 overlap: bool = False, narrow: bool = False):
+                 overlap: bool = False, narrow: bool = False, grad_dtype: torch.dtype = torch.float32):
+        if dtype == torch.float32 and grad_dtype != torch.float32:
+            raise ValueError("fp32 activations take fp32 gradients")
+        if narrow and grad_dtype != dtype:
+            raise ValueError("the multiplication-first layers store their gradients in the activations' dtype")
+        self.grad_dtype = grad_dtype
         self.widths = list(widths)
         # overlap: pulls and pushes run on a second stream, concurrently with the layers (DIGEST
         # system design, Fig. 1c: the table traffic is decoupled from the computation).  The rows a
@@ -75,11 +82,9 @@ class PartitionModel:
         self.narrow = [narrow and not sage and widths[l + 1] < widths[l] for l in range(self.L)]
         self.Z = [None if self.narrow[l] else padded(nL, self.Kp[l], dtype, dev) for l in range(self.L)]
         self.T = [padded(nT, widths[l + 1], dtype, dev) if self.narrow[l] else None for l in range(self.L)]
-        self.P = padded(nT, max([widths[l + 1] for l in range(self.L) if self.narrow[l]] + [1]), dtype, dev) \
+        self.P = padded(nT, max([widths[l + 1] for l in range(self.L) if self.narrow[l]] + [1]), grad_dtype, dev) \
             if any(self.narrow) else None
-        self.dZ = padded(nL, max(self.Kp[1:] + [1]), dtype, dev)
-        self.dH = [None] + [padded(nT, widths[l], dtype, dev) for l in range(1, self.L)]
-        self.G_last = padded(nL, widths[-1], dtype, dev)
+        self._alloc_grads()
         self.W: List[torch.Tensor] = []
         self.dW: List[torch.Tensor] = []
         for l in range(self.L):
@@ -90,6 +95,24 @@ class PartitionModel:
         self.labels = torch.zeros(nL, dtype=torch.int32, device=dev)
         self.row_loss = torch.zeros(max(nL, 1), dtype=torch.float32, device=dev)
         self.loss = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def _alloc_grads(self):
+        nL, nT, gdt, dev = self.n_local, self.n_local + self.n_halo, self.grad_dtype, self.device
+        self.dZ = padded(nL, max(self.Kp[1:] + [1]), gdt, dev)
+        self.dH = [None] + [padded(nT, self.widths[l], gdt, dev) for l in range(1, self.L)]
+        self.G_last = padded(nL, self.widths[-1], gdt, dev)
+
+    def set_grad_dtype(self, grad_dtype: torch.dtype):
+        """Store the activation gradients in another dtype from the next step on
+        (the gradient buffers are reallocated)."""
+        if self.dtype == torch.float32 and grad_dtype != torch.float32:
+            raise ValueError("fp32 activations take fp32 gradients")
+        if any(self.narrow) and grad_dtype != self.dtype:
+            raise ValueError("the multiplication-first layers store their gradients in the activations' dtype")
+        if grad_dtype != self.grad_dtype:
+            self.dZ = self.dH = self.G_last = None
+            self.grad_dtype = grad_dtype
+            self._alloc_grads()
 
     # ---- views ------------------------------------------------------------
     def layer_out(self, l: int) -> torch.Tensor:
@@ -148,8 +171,13 @@ class PartitionModel:
         else:
             gnn.layer_forward(self.graph, self.H[l], self.W[l], l < self.L - 1, self.Z[l], self.layer_out(l))
 
-    def loss_grad(self):
-        gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)
+    def loss_grad(self, n_mean: Optional[int] = None):
+        """Mean softmax cross-entropy of the local rows and its gradient; with n_mean, this partition's share of
+        the mean over n_mean rows held by several partitions."""
+        if n_mean is None:
+            gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)
+        else:
+            gnn.softmax_ce_partial(self.out_last, self.labels, self.G_last, self.row_loss, self.loss, n_mean)
 
     def backward(self, want_halo_grad: bool = True):
         for l in reversed(range(self.L)):

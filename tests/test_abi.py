@@ -71,6 +71,7 @@ def test_host_side_argument_checks(lib):
     assert lib.gnn_sage_half_offset(41, 0) == 44
     lib.gnn_status_string.restype = ctypes.c_char_p
     assert lib.gnn_status_string(5) == b"bad index data on the device"
+    assert lib.gnn_status_string(6) == b"a bounded wait on the device ran out"
     lib.gnn_last_cuda_error.restype = ctypes.c_char_p
     assert isinstance(lib.gnn_last_cuda_error(), bytes) and lib.gnn_last_cuda_error()
 

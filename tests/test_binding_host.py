@@ -66,17 +66,28 @@ def _parts(P, N=60, seed=3):
     return [partition_from_dense(A, np.sort(b))[0] for b in blocks], N
 
 
-def _model(agg="gcn", dtype=torch.float32, narrow=False, widths=(12, 16, 6)):
+def _model(agg="gcn", dtype=torch.float32, narrow=False, widths=(12, 16, 6), grad_dtype=torch.float32):
     parts, N = _parts(2)
     part = parts[0]
     assert part.n_halo > 0
-    return PartitionModel(part, list(widths), agg, dtype, "cpu", narrow=narrow), part
+    return PartitionModel(part, list(widths), agg, dtype, "cpu", narrow=narrow, grad_dtype=grad_dtype), part
 
 
-@pytest.mark.parametrize("agg,dtype,narrow", [("gcn", torch.float32, False), ("gcn", torch.bfloat16, True),
-                                              ("sage", torch.bfloat16, False), ("sage", torch.float32, False)])
-def test_partition_epoch_passes_the_binding_checks(lib, agg, dtype, narrow):
-    m, part = _model(agg, dtype, narrow, widths=(12, 20, 16, 6))
+def test_model_rejects_unsupported_precision_pairs():
+    with pytest.raises(ValueError):
+        _model(dtype=torch.float32, grad_dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        _model(dtype=torch.bfloat16, narrow=True, grad_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("agg,dtype,narrow,grad_dtype", [("gcn", torch.float32, False, torch.float32),
+                                                         ("gcn", torch.bfloat16, True, torch.bfloat16),
+                                                         ("gcn", torch.bfloat16, False, torch.float32),
+                                                         ("sage", torch.bfloat16, False, torch.float32),
+                                                         ("sage", torch.bfloat16, False, torch.bfloat16),
+                                                         ("sage", torch.float32, False, torch.float32)])
+def test_partition_epoch_passes_the_binding_checks(lib, agg, dtype, narrow, grad_dtype):
+    m, part = _model(agg, dtype, narrow, widths=(12, 20, 16, 6), grad_dtype=grad_dtype)
     for l in range(m.L):
         m.tables[l] = padded(part.n_table, m.widths[l], dtype, "cpu")
     lib.calls.clear()
@@ -157,6 +168,10 @@ def test_binding_rejects_undersized_or_mistyped_buffers(lib):
                                    dH=padded(nL, f, torch.float32, "cpu"), want_halo_grad=True),  # no halo rows
         lambda: gnn.softmax_ce(Ho, torch.zeros(nL, dtype=torch.int64), Ho.clone(), torch.zeros(nL),
                                torch.zeros(1)),                                    # int64 labels
+        lambda: gnn.layer_backward(g, Ho.bfloat16(), Ho, Z, W, True, torch.zeros((f, 16)), f),  # fp32 acts, bf16 G
+        lambda: gnn.layer_backward(g, Ho, Ho.bfloat16(), Z, W, True, torch.zeros((f, 16)), f),  # H_out and Z differ
+        lambda: gnn.layer_backward(g, Ho, Ho, Z, W, True, torch.zeros((f, 16)), f, dZ=Z.bfloat16(),
+                                   dH=padded(nT, f, torch.float32, "cpu"), want_halo_grad=True),  # dZ not like G
         lambda: gnn.halo_grad_send(g, H[:nL], m.halo_ids, torch.zeros((part.n_table, f))),  # dH without halo rows
         lambda: gnn.halo_push_quantized(g, H[:nL], m.local_ids, torch.zeros((part.n_table, 8), dtype=torch.uint8),
                                         torch.zeros((part.n_table, 2)), 4, 0),      # code rows too short

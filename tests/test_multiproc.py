@@ -132,3 +132,116 @@ def test_two_partitions_exchange_through_table_gloo():
         assert p.exitcode == 0
     for _, e_h, e_dw in res:
         assert e_h < 1e-12 and e_dw < 1e-10
+
+
+# ---------------------------------------------------------------------------
+# The process-per-partition driver (DistributedPartitionTrainer): each rank
+# holds one partition of one graph, halo rows travel by all-to-all every layer,
+# the halo gradients J go back to their owners, dW is all-reduced.  The ranks'
+# layers are computed by the oracle here (tests/_oracle_model.py), so this
+# checks the driver's exchange plan and schedule on CPU ranks; the GPU test
+# runs the same driver on libgnn.
+# ---------------------------------------------------------------------------
+
+DWIDTHS = [6, 8, 5, 4]
+DN = 90
+
+
+def _dist_problem(agg, world, seed=31):
+    from tests._problems import partition_from_dense, random_sym_adjacency
+
+    A = random_sym_adjacency(DN, 0.08, seed)
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(DN)
+    blocks = [np.sort(b) for b in np.array_split(perm, world)]
+    K = [(2 if agg == "sage" else 1) * w for w in DWIDTHS[:-1]]
+    X = rng.standard_normal((DN, DWIDTHS[0]))
+    Ws = [rng.standard_normal((K[l], DWIDTHS[l + 1])) * 0.5 for l in range(len(DWIDTHS) - 1)]
+    y = rng.integers(0, DWIDTHS[-1], DN).astype(np.int32)
+    full, _ = partition_from_dense(A, np.arange(DN))
+    parts = [partition_from_dense(A, b)[0] for b in blocks]
+    return A, parts, full, X, Ws, y
+
+
+def _dist_worker(rank, world, port, agg, mode, sync_every, epochs, q):
+    sys.path.insert(0, ROOT)
+    import torch
+
+    from sparse_aggregation_dense_gb300 import DistributedPartitionTrainer
+    from tests._oracle_model import NumpyRowOps, OracleModel
+
+    _init(rank, world, port)
+    A, parts, full, X, Ws, y = _dist_problem(agg, world)
+    part = parts[rank]
+    t = DistributedPartitionTrainer(part, DWIDTHS, agg, torch.float64, mode=mode, sync_every=sync_every,
+                                    model_factory=lambda p: OracleModel(p, DWIDTHS, agg, Ws), ops=NumpyRowOps)
+    m = t.model
+    m.H[0][:m.n_local] = torch.from_numpy(X[t.part.local_ids])
+    m.labels = y[t.part.local_ids]
+    out = []
+    for _ in range(epochs):
+        t.epoch()
+        out.append((m.out_last.numpy().copy(), float(m.loss.item()), [d.numpy().copy() for d in m.dW],
+                    [h.numpy().copy() for h in m.H]))
+    q.put((rank, t.part.local_ids.copy(), t.part.halo_ids.copy(), out))
+    dist.destroy_process_group()
+
+
+def _run_dist(world, agg, mode="sync", sync_every=0, epochs=1):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dist_worker, args=(r, world, port, agg, mode, sync_every, epochs, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=300) for _ in range(world)), key=lambda r: r[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    return res
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("agg", ["gcn", "sage"])
+def test_process_per_partition_sync_epoch_equals_whole_graph(world, agg):
+    import oracle
+
+    res = _run_dist(world, agg)
+    A, parts, full, X, Ws, y = _dist_problem(agg, world)
+    ref = oracle.epoch(full, [X] + [np.zeros((DN, f)) for f in DWIDTHS[1:-1]], Ws, y, agg)
+    for rank, lid, hid, out in res:
+        logits, loss, dW, H = out[0]
+        assert np.max(np.abs(logits - ref["Hout"][-1][lid])) < 1e-12
+        assert abs(loss - ref["loss"]) < 1e-12
+        for l in range(len(Ws)):  # every layer: exact only with the J rows returned to their owners
+            assert np.max(np.abs(dW[l] - ref["dW"][l])) < 1e-11 * max(1.0, np.abs(ref["dW"][l]).max()), l
+        # the halo rows of every layer input arrived from their owners (ordered by owner)
+        for l in range(1, len(DWIDTHS) - 1):
+            assert np.max(np.abs(H[l][len(lid):] - ref["Hout"][l - 1][hid])) < 1e-12
+    assert sorted(np.concatenate([r[1] for r in res]).tolist()) == list(range(DN))
+
+
+def test_process_per_partition_stale_reads_previous_epoch_and_forced_sync_equals_sync():
+    import oracle
+
+    world, agg = 2, "gcn"
+    stale = _run_dist(world, agg, "stale", epochs=2)
+    A, parts, full, X, Ws, y = _dist_problem(agg, world)
+    # epoch 1 reads zero tables for layers >= 1, epoch 2 the rows of epoch 1
+    tables = [X] + [np.zeros((DN, f)) for f in DWIDTHS[1:-1]]
+    for e in range(2):
+        nxt = [X] + [np.zeros((DN, f)) for f in DWIDTHS[1:-1]]
+        for rank, lid, hid, out in stale:
+            p = [q for q in parts if np.array_equal(np.sort(q.local_ids), np.sort(lid))][0]
+            r = oracle.epoch(p, tables, Ws, y[p.local_ids], agg)
+            assert np.max(np.abs(out[e][0] - r["Hout"][-1])) < 1e-12
+            for l in range(1, len(DWIDTHS) - 1):
+                nxt[l][p.local_ids] = r["Hout"][l - 1]
+        tables = nxt
+    forced = _run_dist(world, agg, "stale", sync_every=1, epochs=2)
+    sync = _run_dist(world, agg, "sync", epochs=2)
+    for a, b in zip(forced, sync):
+        for ea, eb in zip(a[3], b[3]):
+            assert np.array_equal(ea[0], eb[0]) and ea[1] == eb[1]
+            assert all(np.array_equal(x, z) for x, z in zip(ea[2], eb[2]))
