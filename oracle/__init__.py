@@ -398,11 +398,13 @@ def gat_layer_backward(part, fwd: dict, H: np.ndarray, G: np.ndarray, W: np.ndar
     G = _f64(G)
     dY = G * (fwd["Hout"] > 0) if relu else G
     dT, ds_src, ds_dst = gat_attend_backward(part, fwd["T"], fwd["s_src"], fwd["s_dst"], fwd["alpha"], dY)
+    if grad_bf16:
+        dT = round_bf16(dT)  # stored after the attention-weighted sum, then after the score terms
     dT = dT + ds_src[:, None] * _f64(a_src)[None, :]
     dT[:nL] += ds_dst[:, None] * _f64(a_dst)[None, :]
     da_src = fwd["T"].T @ ds_src
     da_dst = fwd["T"][:nL].T @ ds_dst
-    dTp = round_bf16(dT) if bf16 else dT
+    dTp = round_bf16(dT) if (bf16 or grad_bf16) else dT
     dW, dH = update_backward(dTp, dTp, _f64(H), _f64(W), relu=False, want_dz=True)
     if grad_bf16:
         dH = round_bf16(dH)
