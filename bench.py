@@ -459,6 +459,46 @@ def measure_other_precision(m, stream, steps: int, ef: int):
             "steps": steps}
 
 
+def measure_gat(workload: str, steps: int = 5):
+    """A 3-layer graph-attention epoch (GatModel) on another workload: ms per step and edge x feature / s
+    (the attention-weighted sums counted like the GCN aggregations)."""
+    import torch
+
+    from sparse_aggregation_dense_gb300 import GatModel
+
+    w = workload_by_name(workload)
+    part = w.make(SEED)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    widths = list(w.widths)
+    m = GatModel(part, widths, tdt, "cuda")
+    rng = np.random.default_rng(SEED)
+    for l in range(m.L):
+        m.tables[l] = torch.empty((part.n_table, m.H[l].stride(0)), dtype=tdt, device="cuda")[:, :widths[l]]
+        fill_table(m.tables[l], part.n_table, widths[l], w.dtype == "bf16", SEED, 800 + l, "normal")
+        m.W[l].copy_(torch.from_numpy(synth.glorot(widths[l], widths[l + 1], SEED, 810 + l)))
+        m.a_src[l].copy_(torch.from_numpy((rng.standard_normal(widths[l + 1]) * 0.3).astype(np.float32)))
+        m.a_dst[l].copy_(torch.from_numpy((rng.standard_normal(widths[l + 1]) * 0.3).astype(np.float32)))
+    m.H[0][:part.n_local] = m.tables[0][torch.from_numpy(part.local_ids).cuda()]
+    m.labels.copy_(torch.from_numpy(synth.labels(part.n_local, widths[-1], SEED, ids=part.local_ids)))
+    for _ in range(3):
+        m.step()
+    m.check_errors()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(steps):
+        m.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    m.check_errors()
+    ms = e0.elapsed_time(e1) / steps
+    ef = part.nnz * 2 * sum(widths[1:])  # the attention-weighted sums, forward and backward, at T's width
+    return {"workload": w.name, "widths": widths, "dtype": w.dtype, "grad_dtype": "f32", "ms_per_step": ms,
+            "value": ef / (ms / 1e3), "unit": UNIT, "steps": steps,
+            "note": "3-layer single-head GAT epoch (pull, attention forward, push, loss, attention backward with "
+                    "halo gradients) through the C ABI"}
+
+
 def measure_h2d(x_pin, dst, stream, reps: int = 3) -> float:
     """GB/s of the e2e leg's feature copy alone (pinned host -> device)."""
     import torch
@@ -584,10 +624,15 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, True)
-    codec = measure_codec(m, part, w, tdt, stream)
-    other_ms = measure_other_schedule(m, stream, max(3, min(args.steps, 5)))
-    other_prec = measure_other_precision(m, stream, max(3, min(args.steps, 5)), ef) if bf and not args.narrow else None
-    h2d_gbs = measure_h2d(x_pin, h0, stream)
+    if args.quick:  # tuning runs: the timed step and its breakdown only
+        codec, other_ms, other_prec, h2d_gbs = None, float("nan"), None, float("nan")
+    else:
+        codec = measure_codec(m, part, w, tdt, stream)
+        other_ms = measure_other_schedule(m, stream, max(3, min(args.steps, 5)))
+        other_prec = measure_other_precision(m, stream, max(3, min(args.steps, 5)), ef) if bf and not args.narrow \
+            else None
+        h2d_gbs = measure_h2d(x_pin, h0, stream)
+    gat = None if (args.quick or not args.gat_workload) else measure_gat(args.gat_workload)
     h2d = int(x_pin.numel() * x_pin.element_size() + y_pin.numel() * 4)
     d2h = int(4 + sum(d.numel() * 4 for d in m.dW))
 
@@ -650,6 +695,7 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "h2d_gbs_feature_copy_alone": round(h2d_gbs, 1)},
         "other_precision": other_prec,
+        "gat": gat,
         "gpu_launches": int(launches),
         "halo_codec": codec,
         "schedule": "sequential" if args.sequential else "overlapped (pulls and pushes on a second stream)",
@@ -702,6 +748,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work timed for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=3.0, help="oracle work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gat-workload", default="rmat131k",
+                    help="workload of the graph-attention epoch reported beside the step ('' to skip)")
+    ap.add_argument("--quick", action="store_true",
+                    help="time the step only (no codec, other schedule, other precision or H2D figures)")
     ap.add_argument("--narrow", action="store_true",
                     help="GCN layers whose output is narrower than their input multiply first: A (H W)")
     ap.add_argument("--grad-dtype", choices=["f32", "bf16"], default="f32",

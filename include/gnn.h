@@ -354,6 +354,26 @@ gnn_status gnn_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const
 gnn_status gnn_scatter_add_rows(const void *src, int64_t ld_src, const int64_t *ids, int64_t n, void *dst,
                                 int64_t ld_dst, int64_t n_dst, int64_t f, gnn_dtype dtype, int *err, void *stream);
 
+/* The low-bit codec on rows that travel as a message between processes
+ * (Sylvie page, Quantizer / Dequantizer: halo rows in the forward pass and
+ * the feature gradients J in the backward pass cross the network as b-bit
+ * codes).  Same code and draw layout as gnn_halo_push_quantized, with row i of
+ * the message in place of table row r:
+ * Quantise: codes row i and scale_zero[2i], [2i + 1] from X[i, 0:f], the
+ *   draws keyed by keys[i] (e.g. the vertex's global id) and seed.
+ *   X device n x ld_x, dtype; keys device int64[n]; codes device n x ld_codes.
+ * Dequantise: dst[ids[i], 0:f] = (add ? dst[ids[i], 0:f] : 0) + code * scale +
+ *   zero (fp32 multiply, add, add, each rounded once, stored as dtype); ids
+ *   NULL means row i.  The ids of one call are distinct.  An id outside
+ *   [0, n_dst) leaves its row alone and sets bit 0 of *err (nullable).
+ * GNN_EINVAL for another b, a bad ld_codes or other host-checkable errors. */
+gnn_status gnn_quantize_rows(const void *X, int64_t ld_x, int64_t n, int64_t f, const int64_t *keys, int bits,
+                             uint64_t seed, uint8_t *codes, int64_t ld_codes, float *scale_zero, gnn_dtype dtype,
+                             void *stream);
+gnn_status gnn_dequantize_rows(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n, int64_t f,
+                               int bits, const int64_t *ids, void *dst, int64_t ld_dst, int64_t n_dst, int add,
+                               gnn_dtype dtype, int *err, void *stream);
+
 /* Synchronise the device, then return and clear the graph's device error word:
  * GNN_OK, GNN_ETIMEOUT (a kernel of one of the graph's calls gave up on a
  * bounded wait - every wait on the device gives up after about 2 s, records

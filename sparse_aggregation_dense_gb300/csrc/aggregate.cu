@@ -458,23 +458,41 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
         const uint32_t colmask = p.colmask;
         const bool tagged = colmask == kColMask;
         const int hot_tier = p.hot_tier;
-        uint32_t s_i = 0;
+        uint32_t s_i = 0;  // batches issued
+        int p_slot = 0;
+        uint32_t p_phase = 0;
         bool ok = true;
-        Item x;
+        // the window being issued (raw column ids, weight bits; lane j: entry
+        // wb + j of item x) and the next one, loaded a window ahead so issuing
+        // never waits on an index load; the item after x is looked up an item
+        // ahead for the same reason
+        Item x, xn;
         int64_t it = q0 - P;
+        bool have = next_work_item(it, x, P, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1,
+                                   rowptr, n_rows);
+        int64_t itn = it;
+        bool have_n = have && next_work_item(itn, xn, P, n_items, n_chunks, chunk_row, chunk_begin, chunk_end,
+                                             group_r0, group_r1, rowptr, n_rows);
+        auto load_window = [&](const Item &y, int32_t base, uint32_t &raw, uint32_t &wbits) {
+            raw = 0;
+            wbits = 0;
+            if (base + lane < y.e - y.b) {
+                raw = ld_stream_u32(colidx + y.b + base + lane, pol_stream);
+                wbits = ld_stream_u32(wts + y.b + base + lane, pol_stream);
+            }
+        };
+        uint32_t raw = 0, wbits = 0, raw_n = 0, wbits_n = 0;
+        int32_t wb = 0;
+        if (have) load_window(x, 0, raw, wbits);
 #pragma unroll 1
-        while (ok && next_work_item(it, x, P, n_items, n_chunks, chunk_row, chunk_begin, chunk_end, group_r0, group_r1,
-                                    rowptr, n_rows)) {
+        while (ok && have) {
             const int32_t n = x.e - x.b;
-#pragma unroll 1
-            for (int32_t wb = 0; wb < n && ok; wb += 32) {
+            const bool more_in_item = wb + 32 < n;
+            if (more_in_item) load_window(x, wb + 32, raw_n, wbits_n);
+            else if (have_n) load_window(xn, 0, raw_n, wbits_n);
+            {
                 const int nb = n - wb < 32 ? n - wb : 32;  // entries of this window
                 const bool valid = lane < nb;
-                uint32_t raw = 0, wbits = 0;
-                if (valid) {
-                    raw = ld_stream_u32(colidx + x.b + wb + lane, pol_stream);
-                    wbits = ld_stream_u32(wts + x.b + wb + lane, pol_stream);
-                }
                 const uint32_t ends = __ballot_sync(0xffffffffu, wbits >> 31);  // last entries of rows
                 const uint32_t wa = wbits & 0x7fffffffu;
                 const int tier = tagged ? (int)(raw >> kTierShift) : 0;
@@ -486,8 +504,8 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
                 const int32_t c3 = __shfl_down_sync(0xffffffffu, col, 3);
 #pragma unroll 1
                 for (int k0 = 0; k0 < nb; k0 += BE) {
-                    const int slot = (int)(s_i % NS);
-                    if (!warp_wait(&empty[slot], ((s_i / NS) & 1u) ^ 1u, &abort_flag, p.wait_ns)) {
+                    const int slot = p_slot;
+                    if (!warp_wait(&empty[slot], p_phase ^ 1u, &abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -511,7 +529,23 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
                                         &full[slot], pol);
                     }
                     ++s_i;
+                    if (++p_slot == NS) {
+                        p_slot = 0;
+                        p_phase ^= 1u;
+                    }
                 }
+            }
+            raw = raw_n;
+            wbits = wbits_n;
+            if (more_in_item) {
+                wb += 32;
+            } else {
+                wb = 0;
+                have = have_n;
+                x = xn;
+                if (have)
+                    have_n = next_work_item(itn, xn, P, n_items, n_chunks, chunk_row, chunk_begin, chunk_end,
+                                            group_r0, group_r1, rowptr, n_rows);
             }
         }
         if (!ok) {
@@ -588,7 +622,8 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
             for (int k = 0; k < NP; ++k) acc[v][k] = 0ull;
         }
     };
-    uint32_t s_c = 0;
+    int c_slot = 0;
+    uint32_t c_phase = 0;
     bool ok = true;
 #pragma unroll 1
     for (int64_t it = q0; it < n_items && ok; it += P) {
@@ -603,8 +638,8 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
         }
 #pragma unroll 1
         for (int32_t off = 0; off < n; off += BE) {
-            const int slot = (int)(s_c % NS);
-            if (!warp_wait(&full[slot], (s_c / NS) & 1u, &abort_flag, p.wait_ns)) {
+            const int slot = c_slot;
+            if (!warp_wait(&full[slot], c_phase, &abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -620,7 +655,7 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
 #pragma unroll 1
                     for (int k = 0; k < cnt; ++k) accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
                 }
-            } else {
+            } else if constexpr (BE <= 8) {
 #pragma unroll
                 for (int k = 0; k < BE; ++k) {
                     if (k < cnt) {
@@ -628,13 +663,23 @@ __global__ void __launch_bounds__(PPC * 64, MINB)
                         if (em & (1u << k)) finish_row(r++, x.r1);
                     }
                 }
+            } else {
+                // larger batches: one copy of the row end in the code
+#pragma unroll 1
+                for (int k = 0; k < cnt; ++k) {
+                    accumulate_entry<T, VW, VPT, BE>(acc, sr + k * BOX, ws[k]);
+                    if (em & (1u << k)) finish_row(r++, x.r1);
+                }
             }
             // the slot was read through the generic proxy; the next gathers into it
             // are async-proxy writes
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) bar_arrive(&empty[slot]);
-            ++s_c;
+            if (++c_slot == NS) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
         }
         if (!ok) break;
         if (x.chunk) {
@@ -756,20 +801,49 @@ gnn_status launch_cfg(const AggParams &p, const Schedule &sc, float *partial, in
     return GNN_OK;
 }
 
+// pipeline shape of the aggregation (GNN_AGG_PIPE, for tuning): 0 = by row
+// size (measured best on the R-MAT partitions: four pairs per block with three
+// slots of 8 or 16 entries for rows of up to 512 bytes; two pairs with three
+// slots of 8 entries for 1 KB rows); 1 = two pairs with six slots; 2 = batches
+// of 16 entries for 512-byte rows, two pairs with three slots
+int agg_pipe() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("GNN_AGG_PIPE");
+        v = e ? atoi(e) : kAggPipe;
+        if (v < 0 || v > 2) v = kAggPipe;
+    }
+    return v;
+}
+
 template <typename T>
 gnn_status launch_typed(const AggParams &p, const Schedule &sc, float *partial, int64_t pld, cudaStream_t s) {
-    // a slot holds 2-16 KB of gathered rows (whole groups of four); four pairs
-    // per block; the pairs a SM holds are set by shared memory and registers
+    // a slot holds 2-16 KB of gathered rows (whole groups of four); the pairs a
+    // SM holds are set by shared memory and registers, the bytes in flight by
+    // pairs x slots
     const int64_t bytes = p.f * (int64_t)sizeof(T);
-    if (bytes <= 128) return launch_cfg<T, 4, 1, 16, 4, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 256) return launch_cfg<T, 8, 1, 16, 3, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 512) return launch_cfg<T, 16, 1, 8, 3, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1024) return launch_cfg<T, 16, 2, 4, 3, 4, 4>(p, sc, partial, pld, s);
-    if (bytes <= 1536) return launch_cfg<T, 16, 3, 4, 3, 4, 3>(p, sc, partial, pld, s);
-    if (bytes <= 2048) return launch_cfg<T, 16, 4, 4, 2, 4, 2>(p, sc, partial, pld, s);
-    if (bytes <= 2560) return launch_cfg<T, 16, 5, 4, 2, 4, 2>(p, sc, partial, pld, s);
-    if (bytes <= 3072) return launch_cfg<T, 16, 6, 4, 2, 4, 2>(p, sc, partial, pld, s);
-    if (bytes <= 4096) return launch_cfg<T, 16, 8, 4, 2, 2, 2>(p, sc, partial, pld, s);
+    const int pipe = agg_pipe();
+    if (bytes <= 128) return launch_cfg<T, 4, 1, 16, 4, 4, 3>(p, sc, partial, pld, s);
+    if (bytes <= 256) {
+        if (pipe == 1) return launch_cfg<T, 8, 1, 16, 6, 2, 6>(p, sc, partial, pld, s);
+        return launch_cfg<T, 8, 1, 16, 3, 4, 4>(p, sc, partial, pld, s);
+    }
+    if (bytes <= 512) {
+        if (pipe == 1) return launch_cfg<T, 16, 1, 8, 6, 2, 6>(p, sc, partial, pld, s);
+        if (pipe == 2) return launch_cfg<T, 16, 1, 16, 3, 2, 4>(p, sc, partial, pld, s);
+        return launch_cfg<T, 16, 1, 8, 3, 4, 4>(p, sc, partial, pld, s);
+    }
+    if (bytes <= 1024) {
+        if (pipe == 1) return launch_cfg<T, 16, 2, 4, 6, 2, 6>(p, sc, partial, pld, s);
+        return launch_cfg<T, 16, 2, 8, 3, 2, 4>(p, sc, partial, pld, s);
+    }
+    // wider rows: two pairs per block with three or four slots (deeper rings
+    // measured better than more pairs for 1 KB rows)
+    if (bytes <= 1536) return launch_cfg<T, 16, 3, 4, 4, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2048) return launch_cfg<T, 16, 4, 4, 3, 2, 4>(p, sc, partial, pld, s);
+    if (bytes <= 2560) return launch_cfg<T, 16, 5, 4, 3, 2, 3>(p, sc, partial, pld, s);
+    if (bytes <= 3072) return launch_cfg<T, 16, 6, 4, 3, 2, 2>(p, sc, partial, pld, s);
+    if (bytes <= 4096) return launch_cfg<T, 16, 8, 4, 3, 1, 2>(p, sc, partial, pld, s);
     return GNN_EUNSUPPORTED;
 }
 

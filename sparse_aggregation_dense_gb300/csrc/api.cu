@@ -926,6 +926,27 @@ gnn_status gnn_gat_backward(gnn_graph *g, const void *G, int64_t ld_g, const voi
                              grad_dtype, wg, wg_bytes, s);
 }
 
+gnn_status gnn_quantize_rows(const void *X, int64_t ld_x, int64_t n, int64_t f, const int64_t *keys, int bits,
+                             uint64_t seed, uint8_t *codes, int64_t ld_codes, float *scale_zero, gnn_dtype dtype,
+                             void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || !codec_args_ok(codes, ld_codes, scale_zero, n, bits, f)) return GNN_EINVAL;
+    if (n == 0) return GNN_OK;
+    if (!keys || !operand_ok(X, n, ld_x, f, dtype)) return GNN_EINVAL;
+    return launch_quantize_rows(X, ld_x, n, f, keys, bits, seed, codes, ld_codes, scale_zero, dtype,
+                                as_stream(stream));
+}
+
+gnn_status gnn_dequantize_rows(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n, int64_t f,
+                               int bits, const int64_t *ids, void *dst, int64_t ld_dst, int64_t n_dst, int add,
+                               gnn_dtype dtype, int *err, void *stream) {
+    if (!dtype_ok(dtype) || n < 0 || n_dst < 0 || !codec_args_ok(codes, ld_codes, scale_zero, n, bits, f))
+        return GNN_EINVAL;
+    if (n == 0) return GNN_OK;
+    if (!operand_ok(dst, n_dst > 0 ? 1 : 0, ld_dst, f, dtype) || (!ids && n_dst < n)) return GNN_EINVAL;
+    return launch_dequantize_rows(codes, ld_codes, scale_zero, n, f, bits, ids, dst, ld_dst, n_dst, add, dtype, err,
+                                  as_stream(stream));
+}
+
 gnn_status gnn_gather_rows(const void *src, int64_t ld_src, int64_t n_src, const int64_t *ids, int64_t n, void *dst,
                            int64_t ld_dst, int64_t f, gnn_dtype dtype, int *err, void *stream) {
     if (!dtype_ok(dtype) || n < 0 || n_src < 0 || f <= 0) return GNN_EINVAL;

@@ -250,6 +250,60 @@ __global__ void __launch_bounds__(256) codec_pull_kernel(const uint8_t *__restri
     }
 }
 
+// Rows as a message between processes: row i of X is quantised into codes row
+// i, its draws keyed by keys[i] (the vertex's global id) as a table row would be
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const T *__restrict__ X, int64_t ld_x,
+                                                            const int64_t *__restrict__ keys, int64_t n,
+                                                            uint8_t *__restrict__ codes, int64_t ld_codes,
+                                                            float *__restrict__ scale_zero, int64_t f, uint64_t seed) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw)
+        quantize_row<T, BITS>(X + i * ld_x, keys[i], codes + i * ld_codes, ld_codes, scale_zero + 2 * i, f, seed,
+                              lane);
+}
+
+// dst[ids[i]] (+)= code * scale + zero of codes row i (ids null: row i); the
+// ids of one launch are distinct; the sum is fp32, stored as T
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256) dequantize_rows_kernel(const uint8_t *__restrict__ codes, int64_t ld_codes,
+                                                              const float *__restrict__ scale_zero, int64_t n,
+                                                              const int64_t *__restrict__ ids, T *__restrict__ dst,
+                                                              int64_t ld_dst, int64_t n_dst, int64_t f, int add,
+                                                              int *err) {
+    using W = typename CodeWord<BITS>::type;
+    constexpr int B = (1 << BITS) - 1;
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        const int64_t r = ids ? ids[i] : i;
+        if (r < 0 || r >= n_dst) {
+            if (lane == 0 && err) atomicOr(err, kErrIndex);
+            continue;
+        }
+        const float s = __ldg(scale_zero + 2 * i), z = __ldg(scale_zero + 2 * i + 1);
+        const uint8_t *crow = codes + i * ld_codes;
+        T *out = dst + r * ld_dst;
+        for (int c0 = lane * 8; c0 < (int)f; c0 += 256) {
+            const W word = __ldg(reinterpret_cast<const W *>(crow + c0 / 8 * BITS));
+            float y[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int q = (int)((word >> (k * BITS)) & (W)B);
+                y[k] = __fadd_rn(__fmul_rn((float)q, s), z);
+            }
+            if (add) {
+                float o[8];
+                load8(out, c0, (int)f, o);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[k] = __fadd_rn(o[k], y[k]);
+            }
+            store8(out, c0, (int)f, y);
+        }
+    }
+}
+
 template <typename F>
 gnn_status dispatch_bits(int bits, F &&fn) {
     switch (bits) {
@@ -283,6 +337,43 @@ gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
             { codec_push_kernel<float, BITS><<<blocks, 256, 0, s>>>(static_cast<const float *>(H), ld_h, ids, n_rows,
                                                                    n_table, g->claim, gen, codes, ld_codes, scale_zero,
                                                                    f, seed, g->err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+gnn_status launch_quantize_rows(const void *X, int64_t ld_x, int64_t n, int64_t f, const int64_t *keys, int bits,
+                                uint64_t seed, uint8_t *codes, int64_t ld_codes, float *scale_zero, gnn_dtype dt,
+                                cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)ceil_div(n * 32, 256);
+    return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
+        constexpr int BITS = decltype(Bc)::value;
+        if (dt == GNN_BF16)
+            { quantize_rows_kernel<__nv_bfloat16, BITS><<<blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16 *>(X), ld_x, keys, n, codes, ld_codes, scale_zero, f, seed); GNN_LAUNCHED(1); }
+        else
+            { quantize_rows_kernel<float, BITS><<<blocks, 256, 0, s>>>(static_cast<const float *>(X), ld_x, keys, n,
+                                                                      codes, ld_codes, scale_zero, f, seed); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        return GNN_OK;
+    });
+}
+
+gnn_status launch_dequantize_rows(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n,
+                                  int64_t f, int bits, const int64_t *ids, void *dst, int64_t ld_dst, int64_t n_dst,
+                                  int add, gnn_dtype dt, int *err, cudaStream_t s) {
+    if (n == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n * 32, 256), (int64_t)num_sms() * 16);
+    return dispatch_bits(bits, [&](auto Bc) -> gnn_status {
+        constexpr int BITS = decltype(Bc)::value;
+        if (dt == GNN_BF16)
+            { dequantize_rows_kernel<__nv_bfloat16, BITS><<<blocks, 256, 0, s>>>(
+                codes, ld_codes, scale_zero, n, ids, static_cast<__nv_bfloat16 *>(dst), ld_dst, n_dst, f, add, err); GNN_LAUNCHED(1); }
+        else
+            { dequantize_rows_kernel<float, BITS><<<blocks, 256, 0, s>>>(codes, ld_codes, scale_zero, n, ids,
+                                                                        static_cast<float *>(dst), ld_dst, n_dst, f,
+                                                                        add, err); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
         return GNN_OK;
     });

@@ -28,6 +28,8 @@ constexpr int kGroupNnz = 512;   // entry window of a row group
 constexpr int kGroupRows = 256;  // rows of a row group at most
 // rows wider than this are aggregated in column slices of this many bytes (0: never)
 constexpr int64_t kAggSliceBytes = 0;
+// pipeline shape of the aggregation (see agg_pipe in aggregate.cu)
+constexpr int kAggPipe = 0;
 
 // Column ids of the graph's CSR copies carry a 5-bit "hotness tier" in bits
 // 27..31 (when the column count is below 2^27): tier t holds the columns of
@@ -207,6 +209,12 @@ gnn_status launch_scatter_add_rows(const void *src, int64_t ld_src, const int64_
 gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                              uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
                              uint64_t seed, gnn_dtype dt, cudaStream_t s);
+gnn_status launch_quantize_rows(const void *X, int64_t ld_x, int64_t n, int64_t f, const int64_t *keys, int bits,
+                                uint64_t seed, uint8_t *codes, int64_t ld_codes, float *scale_zero, gnn_dtype dt,
+                                cudaStream_t s);
+gnn_status launch_dequantize_rows(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n,
+                                  int64_t f, int bits, const int64_t *ids, void *dst, int64_t ld_dst, int64_t n_dst,
+                                  int add, gnn_dtype dt, int *err, cudaStream_t s);
 gnn_status launch_codec_pull(const uint8_t *codes, int64_t ld_codes, const float *scale_zero, int64_t n_table,
                              int bits, const int64_t *ids, int64_t n_ids, void *H, int64_t ld_h, int64_t row0,
                              int64_t f, gnn_dtype dt, int *err, cudaStream_t s);

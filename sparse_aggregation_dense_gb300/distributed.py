@@ -25,6 +25,13 @@ ABI) and moves rows between ranks with ``torch.distributed``:
 * the loss is each rank's share of the mean over all ranks' rows, and the
   parameter gradients dW are all-reduced (summed).
 
+With ``codec_bits`` the rows and the J rows cross as b-bit codes with a
+per-row scale and zero point (Sylvie page, Quantizer / Dequantizer): the
+sender quantises (``gnn_quantize_rows``, stochastic rounding keyed by the
+vertex's global id, the epoch, layer and direction), the receiver
+dequantises into the halo rows or adds into its own rows
+(``gnn_dequantize_rows``).
+
 Schedules: "sync" exchanges each layer's fresh rows before that layer (the
 epoch computes exactly the unpartitioned layer); "stale" exchanges at the
 start of the epoch the rows every rank computed in the previous epoch, and adds
@@ -135,6 +142,8 @@ class _LibOps:
 
     gather_rows = staticmethod(gnn.gather_rows)
     scatter_add_rows = staticmethod(gnn.scatter_add_rows)
+    quantize_rows = staticmethod(gnn.quantize_rows)
+    dequantize_rows = staticmethod(gnn.dequantize_rows)
 
 
 class DistributedPartitionTrainer:
@@ -147,8 +156,12 @@ class DistributedPartitionTrainer:
 
     def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, mode: str = "sync",
                  sync_every: int = 0, device="cuda", grad_dtype: torch.dtype = torch.float32, group=None,
-                 model_factory=None, ops=None):
+                 model_factory=None, ops=None, codec_bits: Optional[int] = None, codec_seed: int = 0):
         assert mode in ("sync", "stale")
+        assert codec_bits in (None, 1, 2, 4, 8)
+        # Sylvie's low-bit messages: halo rows and returned J rows cross as b-bit
+        # codes with a per-row scale and zero point (None: exact rows)
+        self.codec_bits, self.codec_seed = codec_bits, codec_seed
         self.rank, self.world = dist.get_rank(group), dist.get_world_size(group)
         self.mode, self.sync_every = mode, sync_every
         self.comm = _Comm(group)
@@ -179,10 +192,28 @@ class DistributedPartitionTrainer:
         self.recv_J = [None] + [torch.zeros((n_send, _full_rows(m.dH[l]).shape[1]), dtype=m.dH[l].dtype,
                                             device=dev) for l in range(1, self.L)]
         self.J_pending = [None] * self.L  # stale schedule: J rows received last epoch, added this epoch
+        if codec_bits:
+            lid = torch.from_numpy(np.asarray(self.part.local_ids, np.int64)).to(dev)
+            self.send_keys = lid[self.send_pos]  # global ids of the rows sent: the draws' keys
+            self.halo_keys = torch.from_numpy(np.asarray(self.part.halo_ids, np.int64)).to(dev)
+            n_halo = m.n_halo
+            self.codes_send = [self._codes(n_send, self.widths[l], dev) for l in range(self.L)]
+            self.codes_recv = [self._codes(n_halo, self.widths[l], dev) for l in range(self.L)]
+            self.codesJ_send = [None] + [self._codes(n_halo, self.widths[l], dev) for l in range(1, self.L)]
+            self.codesJ_recv = [None] + [self._codes(n_send, self.widths[l], dev) for l in range(1, self.L)]
         n_rows = torch.tensor([float(m.n_local)], dtype=torch.float64)
         dist.all_reduce(n_rows, group=group)
         self.n_rows = int(n_rows.item())
         self.epoch_index = 0
+
+    def _codes(self, n: int, f: int, dev):
+        """A message of n rows of f b-bit codes: (codes uint8 n x ld, scale / zero point float32 n x 2)."""
+        return (torch.zeros((n, gnn.codec_row_bytes(f, self.codec_bits)), dtype=torch.uint8, device=dev),
+                torch.zeros((n, 2), dtype=torch.float32, device=dev))
+
+    def _seed(self, l: int, backward: bool) -> int:
+        """Draws differ per epoch, layer and direction."""
+        return self.codec_seed + (self.epoch_index << 9) + (l << 1) + int(backward)
 
     # ---- the two exchanges -----------------------------------------------
     def _send_rows(self, l: int):
@@ -193,23 +224,47 @@ class DistributedPartitionTrainer:
     def _exchange_rows(self, l: int):
         """All-to-all of the gathered rows of layer l into the halo rows of its input."""
         m = self.model
+        if self.codec_bits:
+            f = self.widths[l]
+            (cs, zs), (cr, zr) = self.codes_send[l], self.codes_recv[l]
+            self.ops.quantize_rows(self.send_rows[l][:, :f], self.send_keys, cs, zs, self.codec_bits,
+                                   self._seed(l, False))
+            self.comm.all_to_all(cr, cs, self.plan.recv_counts, self.plan.send_counts)
+            self.comm.all_to_all(zr, zs, self.plan.recv_counts, self.plan.send_counts)
+            self.ops.dequantize_rows(cr, zr, self.codec_bits, m.H[l][m.n_local:m.n_local + m.n_halo])
+            return
         recv = _full_rows(m.H[l])[m.n_local:m.n_local + m.n_halo]
         self.comm.all_to_all(recv, self.send_rows[l], self.plan.recv_counts, self.plan.send_counts)
 
     def _return_J(self, l: int):
-        """The halo rows of dH go back to their owners (into recv_J[l])."""
+        """The halo rows of dH go back to their owners (into recv_J[l], or its codes)."""
         m = self.model
+        if self.codec_bits:
+            f = self.widths[l]
+            (cs, zs), (cr, zr) = self.codesJ_send[l], self.codesJ_recv[l]
+            self.ops.quantize_rows(m.dH[l][m.n_local:m.n_local + m.n_halo], self.halo_keys, cs, zs, self.codec_bits,
+                                   self._seed(l, True))
+            self.comm.all_to_all(cr, cs, self.plan.send_counts, self.plan.recv_counts)
+            self.comm.all_to_all(zr, zs, self.plan.send_counts, self.plan.recv_counts)
+            return
         J = _full_rows(m.dH[l])[m.n_local:m.n_local + m.n_halo]
         self.comm.all_to_all(self.recv_J[l], J, self.plan.send_counts, self.plan.recv_counts)
 
-    def _add_J(self, l: int, J: torch.Tensor):
-        """dH[l][v] += the J rows other ranks returned for v, one rank after another."""
+    def _add_J(self, l: int, J):
+        """dH[l][v] += the J rows other ranks returned for v, one rank after another
+        (J: rows, or (codes, scale / zero point) with the codec)."""
         m = self.model
         f = self.widths[l]
         off = self.plan.send_off
         for q in range(self.world):
             a, b = int(off[q]), int(off[q + 1])
-            if b > a:
+            if b <= a:
+                continue
+            if self.codec_bits:
+                codes, sz = J
+                self.ops.dequantize_rows(codes[a:b], sz[a:b], self.codec_bits, m.dH[l][:m.n_local],
+                                         ids=self.send_pos[a:b], add=True)
+            else:
                 self.ops.scatter_add_rows(J[a:b, :f], self.send_pos[a:b], m.dH[l][:m.n_local])
 
     # ---- one epoch --------------------------------------------------------
@@ -234,15 +289,16 @@ class DistributedPartitionTrainer:
             m.layer_backward(l, want_halo_grad=True)
             if l == 0:
                 continue
+            received = self.codesJ_recv[l] if self.codec_bits else self.recv_J[l]
             if sync:
                 self._return_J(l)
-                self._add_J(l, self.recv_J[l])
+                self._add_J(l, received)
                 self.J_pending[l] = None
             else:
                 if self.J_pending[l] is not None:
                     self._add_J(l, self.J_pending[l])
                 self._return_J(l)
-                self.J_pending[l] = self.recv_J[l].clone()
+                self.J_pending[l] = tuple(t.clone() for t in received) if self.codec_bits else received.clone()
         for l in range(self.L):
             self.comm.all_reduce_sum(m.dW[l])
         self.epoch_index += 1

@@ -32,7 +32,7 @@ EXPORTS = (
     "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv",
     "gnn_layer_forward_narrow", "gnn_layer_backward_narrow", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc", "gnn_debug_expire_next_wait", "gnn_gather_rows", "gnn_scatter_add_rows",
-    "gnn_gat_forward", "gnn_gat_backward",
+    "gnn_gat_forward", "gnn_gat_backward", "gnn_quantize_rows", "gnn_dequantize_rows",
 )
 
 PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
@@ -86,6 +86,8 @@ def _lib():
         L.gnn_gat_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, i64, vp, vp, vp, i64, i32, vp, i64, vp, vp, vp,
                                        vp, vp, vp, i64, vp, i64, i32, i32, vp]
         L.gnn_gather_rows.argtypes = [vp, i64, i64, vp, i64, vp, i64, i64, i32, vp, vp]
+        L.gnn_quantize_rows.argtypes = [vp, i64, i64, i64, vp, i32, ctypes.c_uint64, vp, i64, vp, i32, vp]
+        L.gnn_dequantize_rows.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp, i64, i64, i32, i32, vp, vp]
         L.gnn_scatter_add_rows.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i32, vp, vp]
         L.gnn_launch_count.argtypes = []
         L.gnn_launch_count.restype = i64
@@ -320,6 +322,33 @@ def gat_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, H: torch.Tensor
                                    _ptr(W), _ptr(a_src), _ptr(a_dst), f_out, int(relu), _ptr(T), ld_t, _ptr(scores),
                                    _ptr(alpha), _ptr(dW), _ptr(da_src), _ptr(da_dst), _ptr(dT), ld_dt, _ptr(dH), ld_dh,
                                    _dtype(H), _dtype(G), ctypes.c_void_p(_stream())), what)
+
+
+def quantize_rows(X: torch.Tensor, keys: torch.Tensor, codes: torch.Tensor, scale_zero: torch.Tensor, bits: int,
+                  seed: int):
+    """Rows of X's view as b-bit codes (codes row i, scale_zero[i]); draws keyed by keys[i] and seed."""
+    ld_x, f = _mat(X)
+    what = "gnn_quantize_rows"
+    _codec_args(what, codes, scale_zero, keys, f, bits)
+    _need(_numel(keys) >= _rows(X) and codes.shape[0] >= _rows(X), what, "a key and a code row per row of X")
+    _check(_lib().gnn_quantize_rows(_ptr(X), ld_x, _rows(X), f, _ptr(keys), int(bits),
+                                    ctypes.c_uint64(seed & (2**64 - 1)), _ptr(codes), codes.stride(0),
+                                    _ptr(scale_zero), _dtype(X), ctypes.c_void_p(_stream())), what)
+
+
+def dequantize_rows(codes: torch.Tensor, scale_zero: torch.Tensor, bits: int, dst: torch.Tensor,
+                    ids: Optional[torch.Tensor] = None, add: bool = False, n: Optional[int] = None,
+                    err: Optional[torch.Tensor] = None):
+    """dst[ids[i]] (+)= code * scale + zero of codes row i, over the columns of dst's view (ids None: row i)."""
+    ld_d, f = _mat(dst)
+    n = codes.shape[0] if n is None else n
+    what = "gnn_dequantize_rows"
+    _codec_args(what, codes, scale_zero, ids if ids is not None else torch.zeros(0, dtype=torch.int64), f, bits)
+    _need(ids is None or _numel(ids) >= n, what, "an id per code row")
+    _need(err is None or err.dtype == torch.int32, what, "int32 error word")
+    _check(_lib().gnn_dequantize_rows(_ptr(codes), codes.stride(0), _ptr(scale_zero), n, f, int(bits), _ptr(ids),
+                                      _ptr(dst), ld_d, _rows(dst), int(add), _dtype(dst), _ptr(err),
+                                      ctypes.c_void_p(_stream())), what)
 
 
 def gather_rows(src: torch.Tensor, ids: torch.Tensor, dst: torch.Tensor, err: Optional[torch.Tensor] = None):

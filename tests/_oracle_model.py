@@ -67,3 +67,19 @@ class NumpyRowOps:
         idx = ids.long()
         assert idx.unique().numel() == idx.numel()
         dst[idx] += src
+
+    @staticmethod
+    def quantize_rows(X, keys, codes, sz, bits, seed):
+        c, z = oracle.quantize_rows(X.numpy().astype(np.float32), keys.numpy(), bits, seed, ld_codes=codes.shape[1])
+        codes[:] = torch.from_numpy(c)
+        sz[:] = torch.from_numpy(z)
+
+    @staticmethod
+    def dequantize_rows(codes, sz, bits, dst, ids=None, add=False):
+        f = dst.shape[1]
+        y = torch.from_numpy(oracle.dequantize_rows(codes.numpy(), sz.numpy(), f, bits).astype(np.float64))
+        idx = torch.arange(codes.shape[0]) if ids is None else ids.long()
+        if add:
+            dst[idx] += y
+        else:
+            dst[idx] = y

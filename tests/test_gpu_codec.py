@@ -181,3 +181,49 @@ def test_codec_bad_ids_and_arguments():
         narrow = torch.zeros((part.n_table, 8), dtype=torch.uint8, device="cuda")  # row pitch not a multiple of 16
         gnn.halo_pull_quantized(g, narrow, sz, bits, torch.from_numpy(part.halo_ids).cuda(), Hin)
     assert_ok(g)
+
+
+# ---------------------------------------------------------------------------
+# the codec on rows of a message between processes (gnn_quantize_rows /
+# gnn_dequantize_rows): codes keyed by the rows' global ids, dequantised into
+# place or added onto rows of another matrix
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+@pytest.mark.parametrize("f", [5, 64, 256, 300])
+def test_message_rows_codec_matches_oracle(dt, bits, f):
+    rng = np.random.default_rng(bits * 1000 + f)
+    n = 2000
+    X_h = gen_matrix(n, f, dt, SEED, 900 + bits)
+    X = to_device(X_h, dt, f)
+    keys = rng.permutation(10 * n)[:n].astype(np.int64)
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.full((n, ldc), 0xCD, dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+    seed = 0xABC + bits
+    gnn.quantize_rows(X, torch.from_numpy(keys).cuda(), codes, sz, bits, seed)
+    ref_c, ref_sz = oracle.quantize_rows(_values(X_h, dt, f), keys, bits, seed, ldc)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_c)
+    np.testing.assert_array_equal(sz.cpu().numpy().view(np.uint32), ref_sz.view(np.uint32))
+    # dequantise into place
+    tdt = torch_dtype(dt)
+    Y = padded(n, f, tdt, "cuda")
+    gnn.dequantize_rows(codes, sz, bits, Y)
+    ref_y = oracle.dequantize_rows(ref_c, ref_sz, f, bits)
+    ref_y = oracle.round_bf16(ref_y.astype(np.float64)) if dt == "bf16" else ref_y.astype(np.float64)
+    np.testing.assert_array_equal(Y.float().cpu().numpy().astype(np.float64), ref_y)
+    # dequantise and add onto distinct rows of another matrix
+    m_rows = 3 * n
+    D_h = gen_matrix(m_rows, f, dt, SEED, 950 + bits)
+    D = to_device(D_h, dt, f)
+    ids = rng.permutation(m_rows)[:n].astype(np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gnn.dequantize_rows(codes, sz, bits, D, ids=torch.from_numpy(ids).cuda(), add=True, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    base = widen(D_h, dt, f).astype(np.float32)
+    want = base.copy()
+    want[ids] = base[ids] + oracle.dequantize_rows(ref_c, ref_sz, f, bits)  # one fp32 rounding per element
+    want = oracle.round_bf16(want.astype(np.float64)) if dt == "bf16" else want.astype(np.float64)
+    np.testing.assert_array_equal(D.float().cpu().numpy().astype(np.float64), want)

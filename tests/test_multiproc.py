@@ -163,7 +163,7 @@ def _dist_problem(agg, world, seed=31):
     return A, parts, full, X, Ws, y
 
 
-def _dist_worker(rank, world, port, agg, mode, sync_every, epochs, q):
+def _dist_worker(rank, world, port, agg, mode, sync_every, epochs, q, codec_bits=None):
     sys.path.insert(0, ROOT)
     import torch
 
@@ -174,7 +174,8 @@ def _dist_worker(rank, world, port, agg, mode, sync_every, epochs, q):
     A, parts, full, X, Ws, y = _dist_problem(agg, world)
     part = parts[rank]
     t = DistributedPartitionTrainer(part, DWIDTHS, agg, torch.float64, mode=mode, sync_every=sync_every,
-                                    model_factory=lambda p: OracleModel(p, DWIDTHS, agg, Ws), ops=NumpyRowOps)
+                                    model_factory=lambda p: OracleModel(p, DWIDTHS, agg, Ws), ops=NumpyRowOps,
+                                    codec_bits=codec_bits, codec_seed=77)
     m = t.model
     m.H[0][:m.n_local] = torch.from_numpy(X[t.part.local_ids])
     m.labels = y[t.part.local_ids]
@@ -187,11 +188,11 @@ def _dist_worker(rank, world, port, agg, mode, sync_every, epochs, q):
     dist.destroy_process_group()
 
 
-def _run_dist(world, agg, mode="sync", sync_every=0, epochs=1):
+def _run_dist(world, agg, mode="sync", sync_every=0, epochs=1, codec_bits=None):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_dist_worker, args=(r, world, port, agg, mode, sync_every, epochs, q))
+    procs = [ctx.Process(target=_dist_worker, args=(r, world, port, agg, mode, sync_every, epochs, q, codec_bits))
              for r in range(world)]
     for p in procs:
         p.start()
@@ -245,3 +246,32 @@ def test_process_per_partition_stale_reads_previous_epoch_and_forced_sync_equals
         for ea, eb in zip(a[3], b[3]):
             assert np.array_equal(ea[0], eb[0]) and ea[1] == eb[1]
             assert all(np.array_equal(x, z) for x, z in zip(ea[2], eb[2]))
+
+
+def test_process_per_partition_low_bit_messages():
+    # Sylvie's codec on the wire: every halo row a rank receives is exactly the
+    # owner's row quantised (keyed by the vertex's global id) and dequantised;
+    # with 8-bit codes the epoch's gradients stay near the exact ones
+    import oracle
+
+    world, agg = 2, "gcn"
+    res = _run_dist(world, agg, codec_bits=8)
+    exact = _run_dist(world, agg)
+    owner_rows = {}
+    for rank, lid, hid, out in res:
+        H = out[0][3]
+        for l in range(len(DWIDTHS) - 1):
+            for i, v in enumerate(lid):
+                owner_rows[(l, int(v))] = H[l][i]
+    for rank, lid, hid, out in res:
+        H = out[0][3]
+        nL = len(lid)
+        for l in range(len(DWIDTHS) - 1):
+            sent = np.stack([owner_rows[(l, int(u))] for u in hid])
+            codes, sz = oracle.quantize_rows(sent.astype(np.float32), hid, 8, 77 + (l << 1))
+            want = oracle.dequantize_rows(codes, sz, DWIDTHS[l], 8)
+            np.testing.assert_array_equal(H[l][nL:], want.astype(np.float64))
+    for (_, _, _, a), (_, _, _, b) in zip(res, exact):
+        for l in range(len(DWIDTHS) - 1):
+            err = np.abs(a[0][2][l] - b[0][2][l]).max() / np.abs(b[0][2][l]).max()
+            assert 0 < err < 0.05, (l, err)
