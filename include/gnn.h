@@ -138,12 +138,13 @@ gnn_status gnn_halo_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t f, c
  * Push with quantisation: for v < n_local, row h = H[v, 0:f] is stored at
  * table row r = local_ids[v] as
  *   scale_zero[2r] = s = (max h - min h) / B,  scale_zero[2r + 1] = min h,
- *   code c = min(B, max(0, floor((h[c] - min h) / s + u))),  c < f,
- * with u uniform in [0, 1) (stochastic rounding), or code 0 where s = 0.
- * u of element c of row r is 24 bits of output k = r * 2^15 + floor(c/2) + 1
- * of a SplitMix64 stream seeded with `seed` (bits 40..63 for even c, 16..39
- * for odd c), so the codes are reproducible.  Arithmetic is IEEE fp32, one
- * rounding per operation.
+ *   code c = min(B, floor((h[c] - min h) * (1 / s) + u)),  c < f,
+ * with u uniform in [0, 1) (stochastic rounding), or code 0 where s = 0 (or
+ * where the sum is not a number).  u of element c of row r is 16 bits of
+ * output k = r * 2^14 + floor(c/4) + 1 of a SplitMix64 stream seeded with
+ * `seed` (bits 48..63, 32..47, 16..31, 0..15 for c % 4 = 0, 1, 2, 3), so the
+ * codes are reproducible.  Arithmetic is IEEE fp32, one rounding per
+ * operation (1 / s is the row's rounded reciprocal).
  *   codes      device, n_table x ld_codes bytes; ld_codes a multiple of 16 and
  *              at least b * ceil(f / 8); code c of a row sits in bits
  *              [c b, c b + b) (little-endian); the row's remaining bytes are

@@ -433,7 +433,10 @@ double oracle_softmax_ce(const double *logits, int64_t ld_l, int64_t n, int64_t 
 /* uniform in [0, 1), kept in [0, B]; the recovered value is q * s + z.      */
 /* A constant row (s = 0) gets code 0 everywhere and is recovered exactly.  */
 /* The arithmetic is IEEE single precision, one rounding per operation      */
-/* (no fused multiply-add), so the codes are a pure function of the inputs. */
+/* (no fused multiply-add), so the codes are a pure function of the inputs; */
+/* the division by s is taken as a multiplication by the rounded           */
+/* reciprocal 1 / s of the row (t = (h[c] - z) * (1 / s)), and a value whose */
+/* t + u is not a number (h[c] = z with an infinite reciprocal) gets 0.     */
 /* ------------------------------------------------------------------------ */
 
 /* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number  */
@@ -446,14 +449,14 @@ uint64_t oracle_splitmix64(uint64_t seed, uint64_t k) {
     return z ^ (z >> 31);
 }
 
-/* the uniform u of element c of table row r: output k = r * 2^15 + c / 2 + 1 */
-/* serves elements 2j and 2j + 1, through its bits 40..63 and 16..39; 24    */
-/* bits scaled to [0, 1)                                                     */
+/* the uniform u of element c of table row r: output k = r * 2^14 + c / 4 + 1 */
+/* serves elements 4j .. 4j + 3, through its bits 48..63, 32..47, 16..31    */
+/* and 0..15; 16 bits scaled to [0, 1)                                       */
 static float codec_uniform(uint64_t seed, int64_t r, int64_t c) {
-    const uint64_t k = ((uint64_t)r << 15) + (uint64_t)(c >> 1) + 1u;
+    const uint64_t k = ((uint64_t)r << 14) + (uint64_t)(c >> 2) + 1u;
     const uint64_t z = oracle_splitmix64(seed, k);
-    const uint32_t u24 = (c & 1) ? (uint32_t)((z >> 16) & 0xFFFFFFu) : (uint32_t)(z >> 40);
-    return (float)u24 * (1.0f / 16777216.0f);
+    const uint32_t u16 = (uint32_t)(z >> (48 - 16 * (c & 3))) & 0xFFFFu;
+    return (float)u16 * (1.0f / 65536.0f);
 }
 
 /* Quantise n rows of f fp32 values (row i at x + i * ld_x, table id ids[i]) */
@@ -472,15 +475,14 @@ void oracle_codec_quantize(const float *x, int64_t ld_x, int64_t n, int64_t f, c
         }
         const float range = mx - mn;
         const float s = range / (float)B;
+        const float inv = s > 0.0f ? 1.0f / s : 0.0f;
         memset(row, 0, (size_t)ld_codes);
         for (int64_t c = 0; c < f; ++c) {
             int q = 0;
             if (s > 0.0f) {
-                const float t = (h[c] - mn) / s;
+                const float t = (h[c] - mn) * inv;
                 const float v = t + codec_uniform(seed, ids[i], c);
-                q = (int)floorf(v);
-                if (q < 0) q = 0;
-                if (q > B) q = B;
+                q = !(v >= 0.0f) ? 0 : (v >= (float)B ? B : (int)floorf(v));
             }
             const int64_t bit = c * bits;
             row[bit >> 3] |= (uint8_t)(q << (bit & 7));

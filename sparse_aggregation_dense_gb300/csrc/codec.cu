@@ -10,11 +10,13 @@
 // Pull side (dequantiser): the halo row is recovered as code * s + min.
 //
 // The draws come from a counter-based generator, SplitMix64 (Steele, Lea and
-// Flood, OOPSLA 2014): element c of table row r uses output k = r * 2^15 +
-// c / 2 + 1 of the stream seeded with the caller's seed, bits 40..63 for even
-// c and 16..39 for odd c, as a 24-bit fraction.  All arithmetic is IEEE
-// single precision with one rounding per operation (explicit _rn intrinsics,
-// nothing fused), so the codes depend on the inputs and the seed only.
+// Flood, OOPSLA 2014): element c of table row r uses output k = r * 2^14 +
+// c / 4 + 1 of the stream seeded with the caller's seed, bits 48..63, 32..47,
+// 16..31 or 0..15 for c % 4 = 0, 1, 2, 3, as a 16-bit fraction.  All
+// arithmetic is IEEE single precision with one rounding per operation
+// (explicit _rn intrinsics, nothing fused), the division by s taken as a
+// multiplication by the row's rounded reciprocal 1 / s, so the codes depend
+// on the inputs and the seed only.
 //
 // Layout: codes of table row r at codes + r * ld_codes (bytes, a multiple of
 // 16), code c in bits [c * b, c * b + b) little-endian, bytes past the last
@@ -102,36 +104,35 @@ struct CodeWord<8> {
     using type = unsigned long long;
 };
 
-// RN(a / s) for a >= 0, s > 0, given r = RN(1 / s) and that s lies in
-// [2^-64, 2^64) (`fast`).  A reciprocal-based candidate with one correction
-// step (Markstein: q0 = RN(a r), q = RN(q0 + r RN(a - q0 s))) is accepted
-// only when one more fma proves it: the remainder a - q s (exact here, or
-// rounded by at most 2^-24 of itself) must lie inside s times the half-gap
-// to q's neighbour on that side (ulp(q) / 2; ulp(q) / 4 below a power of
-// two), shrunk by 2^-22 to absorb that rounding.  Everything the test does
-// not settle (near-ties, out-of-range operands) takes the IEEE division, so
-// the result is the correctly rounded quotient in every case.
-__device__ __forceinline__ float div_rn(float a, float s, float r, bool fast) {
-    const uint32_t ab = __float_as_uint(a);
-    if (fast && ab >= 0x1f800000u && ab < 0x5f800000u) {  // a in [2^-64, 2^64)
-        const float q0 = __fmul_rn(a, r);
-        const float q = __fmaf_rn(__fmaf_rn(-q0, s, a), r, q0);
-        const uint32_t qb = __float_as_uint(q);
-        const uint32_t eq = qb >> 23;  // biased exponent of q (q >= 0)
-        if (eq >= 26u && eq <= 254u) {
-            const float rem = __fmaf_rn(-q, s, a);
-            float h = __fmul_rn(__fmul_rn(__uint_as_float((eq - 24u) << 23), s),  // 2^(E(q) - 24) s
-                                __uint_as_float(0x3f7ffffcu));                      // x (1 - 2^-22)
-            if ((qb & 0x7fffffu) == 0u && rem < 0.f) h = __fmul_rn(h, 0.5f);
-            if (fabsf(rem) < h) return q;
-        }
-    } else if (fast && ab == 0u) {
-        return 0.f;
+
+// the codes of the 8 values x of a lane's piece (columns c0 .. c0 + 7 of the
+// row, the draws of the row starting at z_row): t = (x - mn) * inv, plus a
+// 16-bit uniform, floored and kept in [0, B]; codes past column f are 0
+template <int BITS>
+__device__ __forceinline__ typename CodeWord<BITS>::type encode8(const float (&x)[8], int c0, int f, float mn,
+                                                                 float inv, uint64_t z_row) {
+    using W = typename CodeWord<BITS>::type;
+    constexpr int B = (1 << BITS) - 1;
+    const uint64_t zz[2] = {splitmix64_mix(z_row + (uint64_t)(c0 >> 2) * kGamma),
+                            splitmix64_mix(z_row + (uint64_t)((c0 >> 2) + 1) * kGamma)};
+    W word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t u16 = (uint32_t)(zz[e >> 2] >> (48 - 16 * (e & 3))) & 0xffffu;
+        const float u = __fsub_rn(__uint_as_float(0x3f800000u | (u16 << 7)), 1.0f);  // u16 / 2^16, exact
+        const float v = __fadd_rn(__fmul_rn(__fsub_rn(x[e], mn), inv), u);
+        int q = v >= 0.f ? __float2int_rd(v) : 0;  // not a number: 0
+        q = q > B ? B : q;
+        word |= (W)q << (e * BITS);
     }
-    return __fdiv_rn(a, s);
+    const int valid = f - c0;
+    if (valid < 8) word &= (W)(((W)1 << (valid * BITS)) - 1);
+    return word;
 }
 
-// quantise one row h into its codes and (scale, zero point); one warp
+// quantise one row h into its codes and (scale, zero point); one warp.  The
+// lane's first piece (all of a row of up to 256 values) is loaded once and
+// kept in registers for both passes.
 template <typename T, int BITS>
 __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id, uint8_t *__restrict__ crow,
                                              int64_t ld_codes, float *__restrict__ sz, int64_t f64, uint64_t seed,
@@ -139,9 +140,17 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
     const int f = (int)f64;  // a row's width fits 32 bits
+    float x0[8];
+    load8(h, lane * 8, f, x0);
     // min and max of the row
     float mn = INFINITY, mx = -INFINITY;
-    for (int c0 = lane * 8; c0 < f; c0 += 256) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (lane * 8 + k < f) {
+            mn = fminf(mn, x0[k]);
+            mx = fmaxf(mx, x0[k]);
+        }
+    for (int c0 = lane * 8 + 256; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);
 #pragma unroll
@@ -157,36 +166,16 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)B);
-    const uint32_t sb = __float_as_uint(s);
-    const bool fast = sb >= 0x1f800000u && sb < 0x5f800000u;  // s in [2^-64, 2^64)
-    const float r = fast ? __frcp_rn(s) : 0.f;
-    const int used = (f + 7) / 8 * BITS;  // code bytes of the row (whole 8-value words)
-    // value pair c / 2 of the row takes draw (id << 15) + c / 2 + 1
-    const uint64_t z_row = seed + (((uint64_t)id << 15) + 1u) * kGamma;
-    for (int c0 = lane * 8; c0 < f; c0 += 256) {
+    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;  // the rounded reciprocal 1 / s
+    const int used = (f + 7) / 8 * BITS;             // code bytes of the row (whole 8-value words)
+    // value c of the row takes bits of draw (id << 14) + c / 4 + 1
+    const uint64_t z_row = seed + (((uint64_t)id << 14) + 1u) * kGamma;
+    if (lane * 8 < f)
+        *reinterpret_cast<W *>(crow + lane * BITS) = s > 0.f ? encode8<BITS>(x0, lane * 8, f, mn, inv, z_row) : (W)0;
+    for (int c0 = lane * 8 + 256; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);
-        W word = 0;
-        if (s > 0.f) {
-            const uint64_t z0 = z_row + (uint64_t)(c0 >> 1) * kGamma;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint64_t z = splitmix64_mix(z0 + (uint64_t)j * kGamma);
-                const float u[2] = {(float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f),
-                                    (float)(uint32_t)((z >> 16) & 0xFFFFFFu) * (1.0f / 16777216.0f)};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float t = div_rn(__fsub_rn(x[2 * j + e], mn), s, r, fast);
-                    int q = (int)floorf(__fadd_rn(t, u[e]));
-                    q = q < 0 ? 0 : (q > B ? B : q);
-                    word |= (W)q << ((2 * j + e) * BITS);
-                }
-            }
-            // codes of the values past f (computed from zeros) are cleared
-            const int valid = f - c0;
-            if (valid < 8) word &= (W)(((W)1 << (valid * BITS)) - 1);
-        }
-        *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = word;
+        *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = s > 0.f ? encode8<BITS>(x, c0, f, mn, inv, z_row) : (W)0;
     }
     // bytes past the codes are zero
     for (int64_t b = used + lane; b < ld_codes; b += 32) crow[b] = 0;

@@ -43,12 +43,12 @@ def test_grid_row_is_exact_and_packed_little_endian():
 
 def test_one_bit_middle_value_follows_its_draw():
     # b = 1, row [0, 0.5, 1]: the middle value rounds up exactly when its
-    # uniform draw (24 bits of its SplitMix64 output) is >= 1/2
+    # uniform draw (16 bits of its SplitMix64 output) is >= 1/2
     x = np.array([[0.0, 0.5, 1.0]], np.float32)
     for r in range(64):
         codes, _ = oracle.quantize_rows(x, np.array([r]), 1, seed=11)
-        # element 1 takes bits 16..39 of output k = r * 2^15 + 0 + 1
-        u = ((oracle.splitmix64(11, (r << 15) + 1) >> 16) & 0xFFFFFF) / 2.0**24
+        # element 1 takes bits 32..47 of output k = r * 2^14 + 0 + 1
+        u = ((oracle.splitmix64(11, (r << 14) + 1) >> 32) & 0xFFFF) / 2.0**16
         assert (codes[0, 0] >> 1) & 1 == (1 if u >= 0.5 else 0)
         assert codes[0, 0] & 1 == 0 and (codes[0, 0] >> 2) & 1 == 1
 
