@@ -21,13 +21,14 @@ constexpr int kRowsPerGroup = 8;  // rows a lane group moves at once (their load
 // `ix`, -1 = skip the row).  Full 16-byte vectors first, every row's load
 // issued before the stores, then (when nbytes is not a multiple of 16) the
 // element tail.  GATHER: the ids index the source (pull); else the
-// destination (push).
+// destination (push).  The vectors copied are q0, q0 + LPR, ... of each row
+// (q0 = sub unless the caller moved the first one itself).
 template <int LPR, bool GATHER>
 __device__ __forceinline__ void copy_rows(const char *__restrict__ src, int64_t sbytes, char *__restrict__ dst,
                                           int64_t dbytes, int64_t first, const int64_t (&ix)[kRowsPerGroup],
-                                          int64_t nbytes, int es, int sub) {
+                                          int64_t nbytes, int es, int sub, int64_t q0) {
     const int64_t nvec = nbytes / 16;
-    for (int64_t q = sub; q < nvec; q += LPR) {
+    for (int64_t q = q0; q < nvec; q += LPR) {
         uint4 v[kRowsPerGroup];
 #pragma unroll
         for (int k = 0; k < kRowsPerGroup; ++k) {
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(256, 3) pull_kernel(const char *__restrict__ t
             }
         }
     }
-    copy_rows<LPR, true>(table, row_bytes_t, H, row_bytes_h, row0 + i0, ix, nbytes, es, sub);
+    copy_rows<LPR, true>(table, row_bytes_t, H, row_bytes_h, row0 + i0, ix, nbytes, es, sub, sub);
 }
 
 // claim word = (generation << 2) | min(count, 2)
@@ -115,6 +116,15 @@ __global__ void __launch_bounds__(256, 3) push_copy_kernel(const char *__restric
     const int64_t v0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
     if (v0 >= n) return;
+    // The source rows are consecutive: the first vector of each is loaded
+    // before the ids and claim words, so those loads are in flight together
+    // instead of one after the other; only the stores wait for the ids.
+    const int nsrc = n - v0 < kRowsPerGroup ? (int)(n - v0) : kRowsPerGroup;
+    const bool lead = sub < nbytes / 16;
+    uint4 head[kRowsPerGroup];
+#pragma unroll
+    for (int k = 0; k < kRowsPerGroup; ++k)
+        if (lead && k < nsrc) head[k] = __ldg(reinterpret_cast<const uint4 *>(H + (v0 + k) * row_bytes_h) + sub);
     int64_t ix[kRowsPerGroup];
 #pragma unroll
     for (int k = 0; k < kRowsPerGroup; ++k) {
@@ -129,7 +139,10 @@ __global__ void __launch_bounds__(256, 3) push_copy_kernel(const char *__restric
         }
         ix[k] = id;
     }
-    copy_rows<LPR, false>(H, row_bytes_h, table, row_bytes_t, v0, ix, nbytes, es, sub);
+#pragma unroll
+    for (int k = 0; k < kRowsPerGroup; ++k)
+        if (lead && ix[k] >= 0) reinterpret_cast<uint4 *>(table + ix[k] * row_bytes_t)[sub] = head[k];
+    copy_rows<LPR, false>(H, row_bytes_h, table, row_bytes_t, v0, ix, nbytes, es, sub, sub + LPR);
 }
 
 int lanes_per_row(int64_t nbytes) {
