@@ -148,6 +148,42 @@ def aggregation_bytes(part, w, elem: int, narrow: bool = False, grad_elem: int =
     return fwd, bwd
 
 
+def cache_floor_bytes(part, w, elem: int, grad_elem: int, l2_bytes: int, narrow: bool = False):
+    """DRAM bytes of one step's aggregation launches under an ideal static cache
+    of l2_bytes: the most-gathered rows that fit stay resident (each read once),
+    every other gather goes to DRAM, and the streamed terms of the compulsory
+    bytes (row pointers, column ids, normalisation, outputs) are read or written
+    once.  For the power-law gathers here this is the reachable floor of a
+    kernel that cannot reorder its gathers; the compulsory bytes assume an
+    infinite cache."""
+    import numpy as np
+
+    fwd_b, bwd_b = aggregation_bytes(part, w, elem, narrow, grad_elem)
+    nT = part.n_total
+    col_counts = np.sort(np.bincount(part.colidx, minlength=nT))[::-1]  # forward: gathers of each input row
+    row_counts = np.sort(np.diff(part.rowptr).astype(np.int64))[::-1]   # backward: gathers of each dZ row
+    nar = narrow_layers(w, narrow)
+    sage = w.agg == "sage"
+
+    def floor(counts, rb, compulsory):
+        # the compulsory bytes read every input row once; a row outside the
+        # cache is read again for each of its gathers after the first
+        k = max(0, min(len(counts), int(l2_bytes // rb)))
+        rest = counts[k:]
+        return compulsory + int(np.maximum(rest - 1, 0).sum()) * rb
+
+    out = []
+    for l, b in zip(range(w.layers), fwd_b):
+        f = w.widths[l + 1] if nar[l] else w.widths[l]
+        out.append(floor(col_counts, f * elem, b))
+    bl = [l for l in range(w.layers - 1, -1, -1) if not (l == 0 and not nar[l])]
+    for l, b in zip(bl, bwd_b):
+        f = w.widths[l + 1] if nar[l] else w.widths[l]
+        rb = (2 * f if sage else f) * grad_elem
+        out.append(floor(row_counts, rb, b))
+    return out
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -161,6 +197,27 @@ def kernel_source_hash() -> str:
     for name in ("aggregate.cu", "setup.cu"):  # the kernel, and the entry order and tiers it streams
         h.update(open(os.path.join(ROOT, "sparse_aggregation_dense_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:12]
+
+
+def small_case_traffic():
+    """Per-launch DRAM bytes of the aggregation on the quarter-size R-MAT case
+    (rmat4m) from the committed ncu summary, if it was taken on the current
+    kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "aggregate_rmat4m.md")
+    if not os.path.exists(p):
+        return None
+    src, rows = None, []
+    for line in open(p):
+        if line.startswith("kernel_source_sha1:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("launch:"):
+            name, gb, ms = [x.strip() for x in line.split(":", 1)[1].split(",")]
+            rows.append({"launch": name, "dram_gb": float(gb), "ncu_ms": float(ms),
+                         "dram_gbs": round(float(gb) / float(ms) * 1e3, 1)})
+    if src != kernel_source_hash() or not rows:
+        return None
+    return {"workload": "rmat4m", "launches": rows, "note": "one step's five aggregation launches under ncu "
+            "(serialised; DRAM bytes per launch); the full-size step is not captured with counters"}
 
 
 def ncu_traffic(workload: str, grad: str):
@@ -593,6 +650,14 @@ def run_ours(args, rank, world, local_rank):
     agg_launches = prof["agg_fwd"][1] + prof["agg_bwd"][1]
     achieved = alg_bytes / (agg_ms / 1e3) / 1e9 if agg_ms > 0 else 0.0
     traffic = ncu_traffic(w.name, "bf16" if gdt == torch.bfloat16 else "f32")
+    l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or 0)
+    cache_aware = None
+    if l2 > 0 and agg_ms > 0:
+        floor_b = sum(cache_floor_bytes(part, w, 2 if bf else 4, 2 if gdt == torch.bfloat16 else 4, l2, args.narrow))
+        ach = floor_b / (agg_ms / args.steps / 1e3) / 1e9
+        cache_aware = {"model": "ideal static cache of the L2 size holding the most-gathered rows, every other "
+                                "gather from DRAM, streamed terms once", "l2_bytes": l2, "bytes_per_step": floor_b,
+                       "achieved": ach, "frac": ach / hbm if hbm else None}
     breakdown = {k: round(v[0] / args.steps, 3) for k, v in prof.items()}
     breakdown["other"] = round(ms_local - sum(v[0] for v in prof.values()) / args.steps, 3)
 
@@ -613,9 +678,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        h0.copy_(x_pin, non_blocking=True)
-        m.labels.copy_(y_pin, non_blocking=True)
+    # the first step's inputs are copied before it; every later step's inputs are staged during the step
+    # before it (features once layer 0 has read them, labels once the loss has), on a copy stream
+    h0.copy_(x_pin, non_blocking=True)
+    m.labels.copy_(y_pin, non_blocking=True)
+    for i in range(e2e_steps):
+        if i + 1 < e2e_steps:
+            m.stage_inputs(x_pin, y_pin)
         m.step()
         loss_pin.copy_(m.loss, non_blocking=True)
         for d, hp in zip(m.dW, dw_pin):
@@ -686,6 +755,8 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_step": sum(fwd_b) + sum(bwd_b),
             "launch_groups": agg_launches,
             "ms_per_step": round(agg_ms / args.steps, 3),
+            "cache_aware": cache_aware,
+            "traffic_small_case": small_case_traffic(),
         },
         "breakdown_ms_per_step": breakdown,
         "breakdown_note": "library event timing per kernel group; in the overlapped schedule pull and push run "
@@ -693,6 +764,8 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": total_ef / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "input_staging": "each step's inputs after the first are copied during the step before it, on a "
+                                 "copy stream (features once layer 0 has read H[0], labels once the loss has)",
                 "h2d_gbs_feature_copy_alone": round(h2d_gbs, 1)},
         "other_precision": other_prec,
         "gat": gat,
@@ -738,6 +811,49 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def gather_ceiling(reps: int = 5):
+    """Throughput of the aggregation kernel on uniform random columns (2^21 rows of 48 entries) gathered from
+    tables of 2^15 .. 2^23 rows: from tables that L2 holds the kernel's own per-entry limit, from tables far
+    larger than L2 its DRAM-bound rate.  Prints one JSON line."""
+    import numpy as np
+    import torch
+    from sparse_aggregation_dense_gb300 import gnn, padded
+
+    torch.cuda.set_device(0)
+    nL, deg = 1 << 21, 48
+    rng = np.random.default_rng(SEED)
+    rows = []
+    for K in (1 << 15, 1 << 18, 1 << 21, 1 << 23):
+        cols = np.sort(rng.integers(0, K, (nL, deg), dtype=np.int64), axis=1).astype(np.int32).ravel()
+        rowptr = (np.arange(nL + 1, dtype=np.int64) * deg).astype(np.int32)
+        nH = max(0, K - nL)  # every column id is below n_local + n_halo
+        g = gnn.graph_create(torch.from_numpy(rowptr).cuda(), torch.from_numpy(cols).cuda(), nL, nH, None, "gcn")
+        for f, dt in ((128, torch.bfloat16), (256, torch.bfloat16), (256, torch.float32)):
+            H = padded(nL + nH, f, dt, "cuda")
+            H.normal_()
+            Z = padded(nL, f, dt, "cuda")
+            for _ in range(3):
+                gnn.aggregate_forward_noalloc(g, H, Z)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                gnn.aggregate_forward_noalloc(g, H, Z)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            rb = f * (2 if dt == torch.bfloat16 else 4)
+            rows.append({"table_rows": K, "table_mb": round((nL + nH) * rb / 2**20), "row_bytes": rb, "ms": round(ms, 3),
+                         "entries_per_s": nL * deg / (ms / 1e3), "gathered_tbs": nL * deg * rb / (ms / 1e3) / 1e12})
+            del H, Z
+        if gnn.get_error(g) != gnn.GNN_OK:
+            raise RuntimeError("device error word set")
+        gnn.graph_destroy(g)
+        torch.cuda.empty_cache()
+    print(json.dumps({"gather_ceiling": rows, "entries": nL * deg,
+                      "note": "aggregation kernel (gnn_aggregate_forward_noalloc), uniform random columns"}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -758,7 +874,11 @@ def main(argv=None):
                     help="storage of the activation gradients of bf16 workloads (default fp32)")
     ap.add_argument("--sequential", action="store_true",
                     help="pulls and pushes in line on the compute stream instead of on a second stream")
+    ap.add_argument("--gather-ceiling", action="store_true",
+                    help="measure the aggregation's gather throughput on uniform random columns and exit")
     args = ap.parse_args(argv)
+    if args.gather_ceiling:
+        return gather_ceiling()
     if args.narrow and args.grad_dtype != "bf16" and workload_by_name(args.workload).dtype == "bf16":
         args.grad_dtype = "bf16"  # the multiplication-first layers keep their gradients in the activations' dtype
     if args.warmup < 3 and args.impl == "ours" and not args.workload.endswith("-tiny"):

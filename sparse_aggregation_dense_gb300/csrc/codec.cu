@@ -144,12 +144,20 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id
     load8(h, lane * 8, f, x0);
     // min and max of the row
     float mn = INFINITY, mx = -INFINITY;
+    if (lane * 8 + 8 <= f) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (lane * 8 + k < f) {
+        for (int k = 0; k < 8; ++k) {
             mn = fminf(mn, x0[k]);
             mx = fmaxf(mx, x0[k]);
         }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (lane * 8 + k < f) {
+                mn = fminf(mn, x0[k]);
+                mx = fmaxf(mx, x0[k]);
+            }
+    }
     for (int c0 = lane * 8 + 256; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);

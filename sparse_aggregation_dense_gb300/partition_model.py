@@ -95,6 +95,10 @@ class PartitionModel:
         self.labels = torch.zeros(nL, dtype=torch.int32, device=dev)
         self.row_loss = torch.zeros(max(nL, 1), dtype=torch.float32, device=dev)
         self.loss = torch.zeros(1, dtype=torch.float32, device=dev)
+        # inputs of the next epoch staged by stage_inputs, and the event its copies complete
+        self._staged = None
+        self._inputs_ready = None
+        self._copy_stream = None
 
     def _alloc_grads(self):
         nL, nT, gdt, dev = self.n_local, self.n_local + self.n_halo, self.grad_dtype, self.device
@@ -126,14 +130,65 @@ class PartitionModel:
     def dZ_view(self, l: int) -> torch.Tensor:
         return self.dZ[:, :self.Kp[l]]
 
+    # ---- input staging ----------------------------------------------------
+    def stage_inputs(self, x: torch.Tensor, y: torch.Tensor):
+        """Copy the next epoch's inputs while the next call of step() runs: x, the features of the local rows
+        (n_local x f_0, or n_local x the row stride of H[0] with its padding columns), and y, the n_local
+        labels, both pinned host tensors.  The features are copied once layer 0 has read H[0] (after its
+        backward for a multiplication-first layer 0), the labels once the loss has read them, on a copy
+        stream; the epoch after that waits for both copies before it starts."""
+        if x.shape[0] != self.n_local or y.shape[0] != self.n_local:
+            raise ValueError("stage_inputs takes n_local rows of features and n_local labels")
+        if self._copy_stream is None:
+            self._copy_stream = torch.cuda.Stream(device=self.device)
+        self._staged = (x, y)
+
+    def _h0_local(self, width: int) -> torch.Tensor:
+        ld = self.H[0].stride(0)
+        if width == ld:
+            return self.H[0].as_strided((self.n_local + self.n_halo, ld), (ld, 1))[:self.n_local]
+        return self.H[0][:self.n_local]
+
+    def _copy_after(self, src: torch.Tensor, dst: torch.Tensor):
+        """dst <- src on the copy stream, after the work queued so far on the current stream."""
+        done = torch.cuda.Event()
+        done.record(torch.cuda.current_stream(self.device))
+        self._copy_stream.wait_event(done)
+        with torch.cuda.stream(self._copy_stream):
+            dst.copy_(src, non_blocking=True)
+
+    def _wait_inputs(self):
+        if self._inputs_ready is not None:
+            torch.cuda.current_stream(self.device).wait_event(self._inputs_ready)
+            self._inputs_ready = None
+
+    def _stage_features(self, l: int, after_backward: bool):
+        if self._staged is not None and l == 0 and self.narrow[0] == after_backward:
+            x = self._staged[0]
+            self._copy_after(x, self._h0_local(x.shape[1]))
+
+    def _stage_labels(self):
+        if self._staged is not None:
+            self._copy_after(self._staged[1], self.labels)
+
+    def _staging_done(self):
+        """End of the epoch's backward: both copies are queued; the next epoch waits for them."""
+        if self._staged is not None:
+            ready = torch.cuda.Event()
+            ready.record(self._copy_stream)
+            self._inputs_ready = ready
+            self._staged = None
+
     # ---- one epoch --------------------------------------------------------
     def forward(self):
+        self._wait_inputs()
         if self.overlap:
             return self._forward_overlapped()
         for l in range(self.L):
             if self.n_halo:
                 gnn.halo_pull(self.graph, self.tables[l], self.halo_ids, self.H[l])
             self._layer_forward(l)
+            self._stage_features(l, False)
             if l + 1 < self.L:
                 gnn.halo_push(self.graph, self.layer_out(l), self.local_ids, self.tables[l + 1])
 
@@ -151,6 +206,7 @@ class PartitionModel:
         for l in range(self.L):
             main.wait_event(pulled[l])
             self._layer_forward(l)
+            self._stage_features(l, False)
             if l + 1 < self.L:
                 done = torch.cuda.Event()
                 done.record(main)
@@ -178,6 +234,7 @@ class PartitionModel:
             gnn.softmax_ce(self.out_last, self.labels, self.G_last, self.row_loss, self.loss)
         else:
             gnn.softmax_ce_partial(self.out_last, self.labels, self.G_last, self.row_loss, self.loss, n_mean)
+        self._stage_labels()
 
     def backward(self, want_halo_grad: bool = True):
         for l in reversed(range(self.L)):
@@ -198,6 +255,9 @@ class PartitionModel:
         else:
             gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
                                l < self.L - 1, self.dW[l], self.widths[l])
+        self._stage_features(l, True)
+        if l == 0:
+            self._staging_done()
 
     def step(self):
         self.forward()

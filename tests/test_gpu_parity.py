@@ -567,6 +567,45 @@ def test_overlapped_epoch_matches_sequential(case):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("name", ["rmat131k", "sage2m", "rmat16m"])
+def test_staged_inputs_match_synchronous_copies(name, overlap):
+    # three epochs whose inputs change every epoch: copied before each step on
+    # the compute stream, or staged during the previous step on the copy stream
+    w = TINY[name]
+    part = w.make(0)
+    dt = w.dtype
+    xs = []
+    for e in range(3):
+        x = gen_matrix(part.n_local, w.widths[0], dt, SEED, 900 + e)  # n_local x the row stride of H[0]
+        x = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(x)
+        xs.append(x.pin_memory())
+    ys = [torch.from_numpy(synth.labels(part.n_local, w.widths[-1], SEED, 910 + e)).pin_memory() for e in range(3)]
+    results = []
+    for staged in (False, True):
+        m, _, _, _ = _load_model(w, part)
+        if overlap:
+            m.overlap, m.side = True, torch.cuda.Stream()
+        h0 = m._h0_local(xs[0].shape[1])
+        if staged:
+            h0.copy_(xs[0], non_blocking=True)
+            m.labels.copy_(ys[0], non_blocking=True)
+        for e in range(3):
+            if staged:
+                if e + 1 < 3:
+                    m.stage_inputs(xs[e + 1], ys[e + 1])
+            else:
+                h0.copy_(xs[e], non_blocking=True)
+                m.labels.copy_(ys[e], non_blocking=True)
+            m.step()
+        m.check_errors()
+        torch.cuda.synchronize()
+        results.append([m.loss.cpu(), m.out_last.float().cpu()] + [d.cpu() for d in m.dW] +
+                       [t.float().cpu() for t in m.tables[1:]])
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+
+
 # ---------------------------------------------------------------------------
 # narrow layers (multiplication first: A (H W)) against the textbook order
 # ---------------------------------------------------------------------------
