@@ -552,8 +552,8 @@ def measure_gat(workload: str, steps: int = 5):
     ef = part.nnz * 2 * sum(widths[1:])  # the attention-weighted sums, forward and backward, at T's width
     return {"workload": w.name, "widths": widths, "dtype": w.dtype, "grad_dtype": "f32", "ms_per_step": ms,
             "value": ef / (ms / 1e3), "unit": UNIT, "steps": steps,
-            "note": "3-layer single-head GAT epoch (pull, attention forward, push, loss, attention backward with "
-                    "halo gradients) through the C ABI"}
+            "note": f"{len(widths) - 1}-layer single-head GAT epoch (pull, attention forward, push, loss, attention "
+                    "backward with halo gradients) through the C ABI"}
 
 
 def measure_h2d(x_pin, dst, stream, reps: int = 3) -> float:
@@ -843,7 +843,7 @@ def gather_ceiling(reps: int = 5):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / reps
             rb = f * (2 if dt == torch.bfloat16 else 4)
-            rows.append({"table_rows": K, "table_mb": round((nL + nH) * rb / 2**20), "row_bytes": rb, "ms": round(ms, 3),
+            rows.append({"table_rows": K, "table_mb": round(K * rb / 2**20), "row_bytes": rb, "ms": round(ms, 3),
                          "entries_per_s": nL * deg / (ms / 1e3), "gathered_tbs": nL * deg * rb / (ms / 1e3) / 1e12})
             del H, Z
         if gnn.get_error(g) != gnn.GNN_OK:

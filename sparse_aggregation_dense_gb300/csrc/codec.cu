@@ -105,25 +105,62 @@ struct CodeWord<8> {
 };
 
 
+// packed IEEE single-precision pairs (two independent roundings, the same
+// results as two scalar _rn operations)
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // the codes of the 8 values x of a lane's piece (columns c0 .. c0 + 7 of the
 // row, the draws of the row starting at z_row): t = (x - mn) * inv, plus a
-// 16-bit uniform, floored and kept in [0, B]; codes past column f are 0
-template <int BITS>
+// 16-bit uniform, floored and kept in [0, B]; codes past column f are 0.
+// FINITE: the row's values, its scale and its reciprocal are finite, so every
+// sum of a value inside the row is a number >= 0 and the floor needs no test
+// (a value past f may give any code; it is cleared).
+template <int BITS, bool FINITE>
 __device__ __forceinline__ typename CodeWord<BITS>::type encode8(const float (&x)[8], int c0, int f, float mn,
                                                                  float inv, uint64_t z_row) {
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
     const uint64_t zz[2] = {splitmix64_mix(z_row + (uint64_t)(c0 >> 2) * kGamma),
                             splitmix64_mix(z_row + (uint64_t)((c0 >> 2) + 1) * kGamma)};
+    const unsigned long long mn2 = pack2(mn, mn), inv2 = pack2(inv, inv), one2 = pack2(1.0f, 1.0f);
     W word = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const uint32_t u16 = (uint32_t)(zz[e >> 2] >> (48 - 16 * (e & 3))) & 0xffffu;
-        const float u = __fsub_rn(__uint_as_float(0x3f800000u | (u16 << 7)), 1.0f);  // u16 / 2^16, exact
-        const float v = __fadd_rn(__fmul_rn(__fsub_rn(x[e], mn), inv), u);
-        int q = v >= 0.f ? __float2int_rd(v) : 0;  // not a number: 0
-        q = q > B ? B : q;
-        word |= (W)q << (e * BITS);
+    for (int e = 0; e < 8; e += 2) {
+        // 16 bits of the draw as the fraction bits of 1.x, minus 1: u16 / 2^16, exact
+        const uint32_t w0 = (uint32_t)(zz[e >> 2] >> (48 - 16 * (e & 3))) & 0xffffu;
+        const uint32_t w1 = (uint32_t)(zz[e >> 2] >> (32 - 16 * (e & 3))) & 0xffffu;
+        const unsigned long long u2 =
+            sub2(pack2(__uint_as_float(0x3f800000u | (w0 << 7)), __uint_as_float(0x3f800000u | (w1 << 7))), one2);
+        const unsigned long long v2 = add2(mul2(sub2(pack2(x[e], x[e + 1]), mn2), inv2), u2);
+        const float v[2] = {__uint_as_float((uint32_t)v2), __uint_as_float((uint32_t)(v2 >> 32))};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            int q;
+            if constexpr (FINITE) {
+                q = __float2int_rd(v[k]);
+            } else {
+                q = v[k] >= 0.f ? __float2int_rd(v[k]) : 0;  // not a number: 0
+            }
+            q = q > B ? B : q;
+            word |= (W)(uint32_t)q << ((e + k) * BITS);
+        }
     }
     const int valid = f - c0;
     if (valid < 8) word &= (W)(((W)1 << (valid * BITS)) - 1);
@@ -178,12 +215,16 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id
     const int used = (f + 7) / 8 * BITS;             // code bytes of the row (whole 8-value words)
     // value c of the row takes bits of draw (id << 14) + c / 4 + 1
     const uint64_t z_row = seed + (((uint64_t)id << 14) + 1u) * kGamma;
-    if (lane * 8 < f)
-        *reinterpret_cast<W *>(crow + lane * BITS) = s > 0.f ? encode8<BITS>(x0, lane * 8, f, mn, inv, z_row) : (W)0;
+    const bool finite = isfinite(mn) && isfinite(mx) && isfinite(inv);  // the same for the whole warp
+    auto encode = [&](const float (&x)[8], int c0) -> W {
+        if (!(s > 0.f)) return (W)0;
+        return finite ? encode8<BITS, true>(x, c0, f, mn, inv, z_row) : encode8<BITS, false>(x, c0, f, mn, inv, z_row);
+    };
+    if (lane * 8 < f) *reinterpret_cast<W *>(crow + lane * BITS) = encode(x0, lane * 8);
     for (int c0 = lane * 8 + 256; c0 < f; c0 += 256) {
         float x[8];
         load8(h, c0, f, x);
-        *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = s > 0.f ? encode8<BITS>(x, c0, f, mn, inv, z_row) : (W)0;
+        *reinterpret_cast<W *>(crow + c0 / 8 * BITS) = encode(x, c0);
     }
     // bytes past the codes are zero
     for (int64_t b = used + lane; b < ld_codes; b += 32) crow[b] = 0;

@@ -184,8 +184,10 @@ __global__ void gat_rank1_kernel(TG *__restrict__ dT, int64_t ld, int64_t n_tota
     stf(dT + u * ld + c, d);
 }
 
-// partial[b][c] = sum over the rows of chunk b of w[u] T[u][c] (rows in order);
-// the host-side launch then adds the chunks' partials in chunk order
+// partial[b][c] = sum over the rows of chunk b of w[u] T[u][c]: four running
+// sums over the rows u = r0 + 4i + j (j = 0..3), so four loads are in flight,
+// added as (s0 + s1) + (s2 + s3); the host-side launch then adds the chunks'
+// partials in chunk order (a fixed order: the result is reproducible)
 template <typename TA>
 __global__ void gat_colsum_kernel(const TA *__restrict__ Tm, int64_t ld, int64_t n_rows, int64_t f,
                                   const float *__restrict__ w, int64_t rows_per_chunk, float *__restrict__ partial) {
@@ -193,9 +195,14 @@ __global__ void gat_colsum_kernel(const TA *__restrict__ Tm, int64_t ld, int64_t
     const int64_t r0 = bch * rows_per_chunk;
     const int64_t r1 = min(n_rows, r0 + rows_per_chunk);
     for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < f; c += (int64_t)gridDim.x * blockDim.x) {
-        float s = 0.f;
-        for (int64_t u = r0; u < r1; ++u) s = fmaf(w[u], ldf(Tm + u * ld + c), s);
-        partial[bch * f + c] = s;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t u = r0;
+        for (; u + 4 <= r1; u += 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[j] = fmaf(w[u + j], ldf(Tm + (u + j) * ld + c), s[j]);
+        }
+        for (int j = 0; u < r1; ++u, ++j) s[j] = fmaf(w[u], ldf(Tm + u * ld + c), s[j]);
+        partial[bch * f + c] = (s[0] + s[1]) + (s[2] + s[3]);
     }
 }
 
@@ -346,10 +353,12 @@ gnn_status launch_gat_rank1(void *dT, int64_t ld, int64_t n_total, int64_t n_loc
     return GNN_OK;
 }
 
-size_t gat_colsum_ws_floats(int64_t n_rows, int64_t f) {
-    const int64_t chunks = std::min<int64_t>(std::max<int64_t>(ceil_div(n_rows, 4096), 1), 1024);
-    return (size_t)chunks * (size_t)f;
+// chunks of at least 256 rows, at most 4096 chunks
+int64_t gat_colsum_chunks(int64_t n_rows) {
+    return std::min<int64_t>(std::max<int64_t>(ceil_div(n_rows, 256), 1), 4096);
 }
+
+size_t gat_colsum_ws_floats(int64_t n_rows, int64_t f) { return (size_t)gat_colsum_chunks(n_rows) * (size_t)f; }
 
 gnn_status launch_gat_colsum(const void *T, int64_t ld, int64_t n_rows, int64_t f, const float *w, float *out,
                              float *ws, gnn_dtype dt, cudaStream_t s) {
@@ -358,7 +367,7 @@ gnn_status launch_gat_colsum(const void *T, int64_t ld, int64_t n_rows, int64_t 
         GNN_CUDA_TRY(cudaMemsetAsync(out, 0, (size_t)f * sizeof(float), s));
         return GNN_OK;
     }
-    const int64_t chunks = std::min<int64_t>(std::max<int64_t>(ceil_div(n_rows, 4096), 1), 1024);
+    const int64_t chunks = gat_colsum_chunks(n_rows);
     const int64_t rpc = ceil_div(n_rows, chunks);
     dim3 grid((unsigned)ceil_div(f, 128), (unsigned)chunks);
     if (dt == GNN_BF16)

@@ -308,11 +308,10 @@ int num_sms() {
     return n;
 }
 
-size_t update_tc_wt_bytes(int64_t Kp, int64_t N) {
-    return (size_t)round_up(N, 16) * (size_t)round_up(Kp, kBK) * 2;
-}
+namespace {
 
-bool update_fwd_tc_supported(int64_t Kp, int64_t N) {
+// one pass holds all of W (Kp x N) in shared memory next to two Z stages
+bool fwd_pass_ok(int64_t Kp, int64_t N) {
     const int64_t N_pad = round_up(N, 16);
     const int64_t KC = ceil_div(Kp, kBK);
     if (N_pad > 256 || KC < 1) return false;
@@ -320,8 +319,43 @@ bool update_fwd_tc_supported(int64_t Kp, int64_t N) {
     return w + 2 * kTileBytes + kOutBytes + sizeof(Bars) + 1024 <= kSmemLimit;
 }
 
+// output columns per pass: all N, or slices of 128 when W does not fit (the
+// passes read Z again; each writes its own columns of the output)
+constexpr int64_t kNSlice = 128;
+int64_t fwd_slice(int64_t Kp, int64_t N) {
+    if (fwd_pass_ok(Kp, N)) return N;
+    if (N > kNSlice && fwd_pass_ok(Kp, kNSlice)) return kNSlice;
+    return 0;
+}
+
+gnn_status fwd_tc_pass(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
+                       int relu, void *out, int64_t ld_o, void *wt_ws, int *err, cudaStream_t s);
+
+}  // namespace
+
+size_t update_tc_wt_bytes(int64_t Kp, int64_t N) {
+    const int64_t ns = fwd_slice(Kp, N);
+    return (size_t)round_up(ns > 0 ? ns : N, 16) * (size_t)round_up(Kp, kBK) * 2;
+}
+
+bool update_fwd_tc_supported(int64_t Kp, int64_t N) { return fwd_slice(Kp, N) > 0; }
+
 gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w,
                                 int64_t N, int relu, void *out, int64_t ld_o, void *wt_ws, int *err, cudaStream_t s) {
+    const int64_t ns = fwd_slice(Kp, N);
+    if (ns <= 0) return GNN_EUNSUPPORTED;
+    for (int64_t n0 = 0; n0 < N; n0 += ns) {
+        const gnn_status st = fwd_tc_pass(Z, ld_z, n, Kp, Wp + n0, ld_w, N - n0 < ns ? N - n0 : ns, relu,
+                                          static_cast<__nv_bfloat16 *>(out) + n0, ld_o, wt_ws, err, s);
+        if (st != GNN_OK) return st;
+    }
+    return GNN_OK;
+}
+
+namespace {
+
+gnn_status fwd_tc_pass(const void *Z, int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
+                       int relu, void *out, int64_t ld_o, void *wt_ws, int *err, cudaStream_t s) {
     const int64_t N_pad = round_up(N, 16);
     const int64_t KC = ceil_div(Kp, kBK);
     const int64_t K_pad = KC * kBK;
@@ -346,5 +380,7 @@ gnn_status launch_update_fwd_tc(const void *Z, int64_t ld_z, int64_t n, int64_t 
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }
+
+}  // namespace
 
 }  // namespace gnn

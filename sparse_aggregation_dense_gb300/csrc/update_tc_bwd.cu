@@ -548,12 +548,30 @@ gnn_status launch_grad_to_bf16(const float *G, int64_t ld_g, const void *Hout, i
     return GNN_OK;
 }
 
-bool update_bwd_tc_supported(int64_t Kp, int64_t N) {
+namespace {
+
+// columns of Z (rows of W and dW) per pass: all Kp, or slices of 256 when the
+// wgrad accumulator or the dgrad's resident W of the whole Kp does not fit; the
+// slices are independent (dZ[:, k0:k1] = dY W[k0:k1]^T, dW[k0:k1] = Z[:, k0:k1]^T dY)
+constexpr int64_t kKSlice = 256;
+int64_t bwd_slice(int64_t Kp, int64_t N) {
     BwdPlan p;
-    return plan_bwd(Kp, N, 1, &p);
+    if (plan_bwd(Kp, N, 1, &p)) return Kp;
+    if (Kp > kKSlice && plan_bwd(kKSlice, N, 1, &p)) return kKSlice;
+    return 0;
 }
 
-size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp, int64_t N) {
+gnn_status bwd_tc_pass(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
+                       int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N, float *dWp,
+                       void *dZ, int64_t ld_dz, bool dz_f32, void *ws, int *err, cudaStream_t s);
+
+}  // namespace
+
+bool update_bwd_tc_supported(int64_t Kp, int64_t N) { return bwd_slice(Kp, N) > 0; }
+
+size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp_all, int64_t N) {
+    const int64_t ks = bwd_slice(Kp_all, N);
+    const int64_t Kp = ks > 0 ? ks : Kp_all;
     const int64_t tiles = ceil_div(n, kWRows);
     const int64_t grid = tiles < num_sms() ? tiles : num_sms();
     const int64_t kpad = round_up(Kp, 16), npad = round_up(N, 16);
@@ -563,6 +581,24 @@ size_t update_bwd_tc_ws_bytes(int64_t n, int64_t Kp, int64_t N) {
 gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
                                 int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N,
                                 float *dWp, void *dZ, int64_t ld_dz, bool dz_f32, void *ws, int *err, cudaStream_t s) {
+    const int64_t ks = bwd_slice(Kp, N);
+    if (ks <= 0) return GNN_EUNSUPPORTED;
+    const int64_t dzb = dz_f32 ? 4 : 2;
+    for (int64_t k0 = 0; k0 < Kp; k0 += ks) {
+        const gnn_status st = bwd_tc_pass(
+            G, ld_g, Hout, ld_h, relu, static_cast<const char *>(Z) + k0 * 2, ld_z, n, Kp - k0 < ks ? Kp - k0 : ks,
+            Wp + k0 * ld_w, ld_w, N, dWp + k0 * N, dZ ? static_cast<char *>(dZ) + k0 * dzb : nullptr, ld_dz, dz_f32,
+            ws, err, s);
+        if (st != GNN_OK) return st;
+    }
+    return GNN_OK;
+}
+
+namespace {
+
+gnn_status bwd_tc_pass(const void *G, int64_t ld_g, const void *Hout, int64_t ld_h, int relu, const void *Z,
+                       int64_t ld_z, int64_t n, int64_t Kp, const float *Wp, int64_t ld_w, int64_t N, float *dWp,
+                       void *dZ, int64_t ld_dz, bool dz_f32, void *ws, int *err, cudaStream_t s) {
     BwdPlan p;
     if (!plan_bwd(Kp, N, relu, &p)) return GNN_EUNSUPPORTED;
     if (n == 0) {
@@ -614,5 +650,7 @@ gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, i
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }
+
+}  // namespace
 
 }  // namespace gnn

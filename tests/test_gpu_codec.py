@@ -57,13 +57,14 @@ def test_push_quantized_matches_oracle(name, bits):
 
 
 def _special_rows(n, f, rng):
-    """Rows that reach every branch of the quantiser's division: magnitudes
-    far below and above the reciprocal test's range, integer rows (exact
-    quotients), rows whose quotients are powers of two, constant rows (zero
-    scale), two-valued rows and numerators just above zero."""
+    """Rows that reach every branch of the quantiser: magnitudes far below and
+    above 1, integer rows (exact quotients), rows whose quotients are powers of
+    two, constant rows (zero scale), two-valued rows, numerators just above
+    zero, a range so small that the reciprocal of the scale is infinite, and
+    rows holding an infinite value (infinite scale)."""
     H = np.empty((n, f), np.float32)
     for i in range(n):
-        kind = i % 8
+        kind = i % 10
         x = rng.standard_normal(f)
         if kind == 0:
             x = x * 2.0 ** -70
@@ -80,9 +81,13 @@ def _special_rows(n, f, rng):
             x = np.full(f, 1.5)
         elif kind == 6:
             x = np.where(rng.random(f) < 0.5, -3.0, 5.0)
-        else:  # values a hair above the minimum: tiny numerators
+        elif kind == 7:  # values a hair above the minimum: tiny numerators
             x = np.abs(x)
             x[:3] = [0.0, 2.0 ** -70, 2.0 ** -64]
+        elif kind == 8:  # range 2^-140 (subnormal): 1 / scale overflows
+            x = np.where(rng.random(f) < 0.5, 0.0, 2.0 ** -140)
+        else:  # an infinite value: the scale is infinite
+            x[rng.integers(0, f)] = np.inf
         H[i] = x.astype(np.float32)
     return H
 
