@@ -184,6 +184,7 @@ static void destroy_graph(gnn_graph *g) {
     cudaFree(g->wfwd);
     cudaFree(g->wbwd);
     cudaFree(g->t2b);
+    cudaFree(g->erow);
     cudaFree(g->err);
     cudaFree(g->ws);
     cudaFree(g->claim);
@@ -300,6 +301,8 @@ gnn_status gnn_graph_create(const int32_t *rowptr, const int32_t *colidx, int64_
         TRY_CUDA(cudaFreeAsync(tc, s));
     }
     if (gat && nnz > 0) {
+        TRY_CUDA(cudaMalloc((void **)&g->erow, (size_t)nnz * sizeof(int32_t)));
+        TRY(launch_entry_rows(g->rowptr, n_local, g->erow, s));
         TRY(launch_gat_entry_map(fperm, tperm, g->permT, nnz, g->t2b, iota, s));
         TRY_CUDA(cudaFreeAsync(iota, s));
         if (fperm) TRY_CUDA(cudaFreeAsync(fperm, s));

@@ -108,31 +108,75 @@ __global__ void gat_mask_kernel(const TG *__restrict__ G, int64_t ld_g, const TA
     Y[r * ld_y + c] = (!Hout || ldf(Hout + r * ld_h + c) > 0.f) ? g : TG(0.f);
 }
 
-// The softmax backward of row v: dalpha_e = dY[v] . T[col_e] (stored in dz),
-// then dz_e = alpha_e (dalpha_e - sum_e' alpha_e' dalpha_e') * LeakyReLU'(z_e)
-// and ds_dst[v] = sum_e dz_e.  One warp per row; each dot product is split over
-// the lanes and reduced with shuffles.
-template <typename TG, typename TA>
-__global__ void __launch_bounds__(256) gat_edge_backward_kernel(
+// four consecutive values c .. c + 3 of a row as fp32 (values at or past f: 0)
+__device__ __forceinline__ void ld4(const float *p, int64_t c, int64_t f, float (&v)[4]) {
+    if (c + 4 <= f) {
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(p + c));
+        v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = c + j < f ? p[c + j] : 0.f;
+    }
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16 *p, int64_t c, int64_t f, float (&v)[4]) {
+    if (c + 4 <= f) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(p + c));
+        v[0] = __uint_as_float(q.x << 16), v[1] = __uint_as_float(q.x & 0xffff0000u);
+        v[2] = __uint_as_float(q.y << 16), v[3] = __uint_as_float(q.y & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = c + j < f ? __bfloat162float(p[c + j]) : 0.f;
+    }
+}
+
+// The score gradient's first factor for every entry e of the block (library
+// order): dz[e] = dY[row e] . T[col e].  G lanes per entry (four values per
+// lane per step), so the work spreads evenly whatever the row lengths; the
+// row of each entry comes from the graph's entry-row map.
+template <typename TG, typename TA, int G>
+__global__ void __launch_bounds__(256) gat_sddmm_kernel(const int32_t *__restrict__ erow,
+                                                        const uint32_t *__restrict__ colidx, uint32_t colmask,
+                                                        int64_t nnz, const TG *__restrict__ dY, int64_t ld_y,
+                                                        const TA *__restrict__ Tm, int64_t ld_t, int64_t f,
+                                                        float *__restrict__ dz) {
+    constexpr int EPW = 32 / G;  // entries per warp and step
+    const int lane = threadIdx.x & 31, sub = lane % G;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t kb = warp * EPW; kb < nnz; kb += nw * EPW) {  // the same trip count for the whole warp
+        const int64_t k = kb + lane / G;
+        float p = 0.f;
+        if (k < nnz) {
+            const TG *y = dY + (int64_t)erow[k] * ld_y;
+            const TA *t = Tm + (int64_t)(colidx[k] & colmask) * ld_t;
+            for (int64_t c = 4 * sub; c < f; c += 4 * G) {
+                float a[4], b[4];
+                ld4(y, c, f, a);
+                ld4(t, c, f, b);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) p = fmaf(a[j], b[j], p);
+            }
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+        if (k < nnz && sub == 0) dz[k] = p;
+    }
+}
+
+// The softmax backward of row v, from dz[e] = dY[v] . T[col_e]:
+// dz_e <- alpha_e (dz_e - sum_e' alpha_e' dz_e') * LeakyReLU'(z_e), and
+// ds_dst[v] = sum_e dz_e.  One warp per row, the lanes over its entries.
+__global__ void __launch_bounds__(256) gat_softmax_backward_kernel(
     const int32_t *__restrict__ rowptr, const uint32_t *__restrict__ colidx, uint32_t colmask, int64_t n_local,
     const float *__restrict__ s_src, const float *__restrict__ s_dst, const float *__restrict__ alpha,
-    const TG *__restrict__ dY, int64_t ld_y, const TA *__restrict__ Tm, int64_t ld_t, int64_t f,
     float *__restrict__ dz, float *__restrict__ ds_dst) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n_local; v += nw) {
         const int32_t b = rowptr[v], e = rowptr[v + 1];
-        const TG *y = dY + v * ld_y;
         float dsum = 0.f;
-        for (int32_t k = b; k < e; ++k) {
-            const TA *t = Tm + (int64_t)(colidx[k] & colmask) * ld_t;
-            float p = 0.f;
-            for (int64_t c = lane; c < f; c += 32) p = fmaf(ldf(y + c), ldf(t + c), p);
-            p = warp_sum(p);
-            if (lane == 0) dz[k] = p;
-            dsum = fmaf(unflag(alpha[k]), p, dsum);
-        }
-        __syncwarp();
+        for (int32_t k = b + lane; k < e; k += 32) dsum = fmaf(unflag(alpha[k]), dz[k], dsum);
+        dsum = warp_sum(dsum);
         const float sd = s_dst[v];
         float s = 0.f;
         for (int32_t k = b + lane; k < e; k += 32) {
@@ -145,6 +189,14 @@ __global__ void __launch_bounds__(256) gat_edge_backward_kernel(
         s = warp_sum(s);
         if (lane == 0) ds_dst[v] = s;
     }
+}
+
+// entry-row map of a CSR: erow[k] = v for k in [rowptr[v], rowptr[v + 1])
+__global__ void entry_rows_kernel(const int32_t *__restrict__ rowptr, int64_t n_rows, int32_t *__restrict__ erow) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n_rows; v += nw)
+        for (int32_t k = rowptr[v] + lane; k < rowptr[v + 1]; k += 32) erow[k] = (int32_t)v;
 }
 
 // Over the transpose: ds_src[u] = sum of dz over the entries holding column u,
@@ -309,21 +361,37 @@ gnn_status launch_gat_edge_backward(const gnn_graph *g, const float *s_src, cons
                                     const void *dY, int64_t ld_y, const void *T, int64_t ld_t, int64_t f, float *dz,
                                     float *ds_dst, gnn_dtype dt, gnn_dtype gdt, cudaStream_t s) {
     if (g->n_local == 0) return GNN_OK;
-    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(g->n_local * 32, 256), (int64_t)num_sms() * 16);
     const uint32_t cm = g->fwd.tagged ? kColMask : 0xffffffffu;
     const uint32_t *ci = reinterpret_cast<const uint32_t *>(g->colidx);
-    if (gdt == GNN_F32 && dt == GNN_BF16)
-        { gat_edge_backward_kernel<float, __nv_bfloat16><<<blocks, 256, 0, s>>>(
-            g->rowptr, ci, cm, g->n_local, s_src, s_dst, alpha, static_cast<const float *>(dY), ld_y,
-            static_cast<const __nv_bfloat16 *>(T), ld_t, f, dz, ds_dst); GNN_LAUNCHED(1); }
-    else if (gdt == GNN_F32)
-        { gat_edge_backward_kernel<float, float><<<blocks, 256, 0, s>>>(
-            g->rowptr, ci, cm, g->n_local, s_src, s_dst, alpha, static_cast<const float *>(dY), ld_y,
-            static_cast<const float *>(T), ld_t, f, dz, ds_dst); GNN_LAUNCHED(1); }
-    else
-        { gat_edge_backward_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(
-            g->rowptr, ci, cm, g->n_local, s_src, s_dst, alpha, static_cast<const __nv_bfloat16 *>(dY), ld_y,
-            static_cast<const __nv_bfloat16 *>(T), ld_t, f, dz, ds_dst); GNN_LAUNCHED(1); }
+    if (g->nnz > 0) {
+        if (!g->erow) return GNN_EINVAL;
+        constexpr int G = 8;
+        const unsigned eb = (unsigned)std::min<int64_t>(ceil_div(g->nnz * G, 256), (int64_t)num_sms() * 32);
+        if (gdt == GNN_F32 && dt == GNN_BF16)
+            { gat_sddmm_kernel<float, __nv_bfloat16, G><<<eb, 256, 0, s>>>(
+                g->erow, ci, cm, g->nnz, static_cast<const float *>(dY), ld_y,
+                static_cast<const __nv_bfloat16 *>(T), ld_t, f, dz); GNN_LAUNCHED(1); }
+        else if (gdt == GNN_F32)
+            { gat_sddmm_kernel<float, float, G><<<eb, 256, 0, s>>>(g->erow, ci, cm, g->nnz,
+                                                                    static_cast<const float *>(dY), ld_y,
+                                                                    static_cast<const float *>(T), ld_t, f, dz); GNN_LAUNCHED(1); }
+        else
+            { gat_sddmm_kernel<__nv_bfloat16, __nv_bfloat16, G><<<eb, 256, 0, s>>>(
+                g->erow, ci, cm, g->nnz, static_cast<const __nv_bfloat16 *>(dY), ld_y,
+                static_cast<const __nv_bfloat16 *>(T), ld_t, f, dz); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+    }
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(g->n_local * 32, 256), (int64_t)num_sms() * 16);
+    { gat_softmax_backward_kernel<<<blocks, 256, 0, s>>>(g->rowptr, ci, cm, g->n_local, s_src, s_dst, alpha, dz,
+                                                         ds_dst); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
+gnn_status launch_entry_rows(const int32_t *rowptr, int64_t n_rows, int32_t *erow, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n_rows * 32, 256), (int64_t)num_sms() * 16);
+    { entry_rows_kernel<<<blocks, 256, 0, s>>>(rowptr, n_rows, erow); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
     return GNN_OK;
 }

@@ -82,6 +82,7 @@ struct gnn_graph {
     // aggregation's order, the block entry (in the block's aggregation order)
     // it came from
     int32_t *t2b = nullptr;
+    int32_t *erow = nullptr;  // graph attention: the row of every block entry
     // per-entry weights of the block (forward) and of its transpose (backward),
     // in the aggregation's order
     float *wfwd = nullptr, *wbwd = nullptr;
@@ -153,6 +154,8 @@ gnn_status launch_iota(int32_t *out, int64_t n, cudaStream_t s);
 // (null: not sorted), permT[k_stable] = e_original; scratch: int32[nnz]
 gnn_status launch_gat_entry_map(const int32_t *fperm, const int32_t *tperm, const int32_t *permT, int64_t nnz,
                                 int32_t *t2b, int32_t *scratch, cudaStream_t s);
+// erow[k] = the row holding entry k of a CSR (rowptr of n_rows rows)
+gnn_status launch_entry_rows(const int32_t *rowptr, int64_t n_rows, int32_t *erow, cudaStream_t s);
 gnn_status launch_gat_scores(const void *T, int64_t ld, int64_t n_total, int64_t n_local, int64_t f,
                              const float *a_src, const float *a_dst, float *s_src, float *s_dst, gnn_dtype dt,
                              cudaStream_t s);
