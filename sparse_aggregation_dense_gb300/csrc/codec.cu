@@ -167,18 +167,16 @@ __device__ __forceinline__ typename CodeWord<BITS>::type encode8(const float (&x
     return word;
 }
 
-// quantise one row h into its codes and (scale, zero point); one warp.  The
-// lane's first piece (all of a row of up to 256 values) is loaded once and
-// kept in registers for both passes.
+// quantise one row h into its codes and (scale, zero point); one warp.  x0 is
+// the lane's first piece (load8 of columns 8 lane ..; all of a row of up to
+// 256 values), loaded by the caller and kept in registers for both passes.
 template <typename T, int BITS>
-__device__ __forceinline__ void quantize_row(const T *__restrict__ h, int64_t id, uint8_t *__restrict__ crow,
-                                             int64_t ld_codes, float *__restrict__ sz, int64_t f64, uint64_t seed,
-                                             int lane) {
+__device__ __forceinline__ void quantize_row(const T *__restrict__ h, const float (&x0)[8], int64_t id,
+                                             uint8_t *__restrict__ crow, int64_t ld_codes, float *__restrict__ sz,
+                                             int64_t f64, uint64_t seed, int lane) {
     using W = typename CodeWord<BITS>::type;
     constexpr int B = (1 << BITS) - 1;
     const int f = (int)f64;  // a row's width fits 32 bits
-    float x0[8];
-    load8(h, lane * 8, f, x0);
     // min and max of the row
     float mn = INFINITY, mx = -INFINITY;
     if (lane * 8 + 8 <= f) {
@@ -246,13 +244,17 @@ __global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H
     const int lane = threadIdx.x & 31;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n; v += nw) {
+        // the row's values do not depend on its id: their load overlaps the id and claim-word loads
+        float x0[8];
+        load8(H + v * ld_h, lane * 8, (int)f, x0);
         const int64_t id = ids[v];
         if (id < 0 || id >= n_table) continue;  // reported by the claim pass
         if (claim[id] != ((gen << 2) | 1u)) {
             if (lane == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
             continue;
         }
-        quantize_row<T, BITS>(H + v * ld_h, id, codes + id * ld_codes, ld_codes, scale_zero + 2 * id, f, seed, lane);
+        quantize_row<T, BITS>(H + v * ld_h, x0, id, codes + id * ld_codes, ld_codes, scale_zero + 2 * id, f, seed,
+                              lane);
     }
 }
 
@@ -297,9 +299,12 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const T *__restrict_
                                                             float *__restrict__ scale_zero, int64_t f, uint64_t seed) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw)
-        quantize_row<T, BITS>(X + i * ld_x, keys[i], codes + i * ld_codes, ld_codes, scale_zero + 2 * i, f, seed,
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nw) {
+        float x0[8];
+        load8(X + i * ld_x, lane * 8, (int)f, x0);
+        quantize_row<T, BITS>(X + i * ld_x, x0, keys[i], codes + i * ld_codes, ld_codes, scale_zero + 2 * i, f, seed,
                               lane);
+    }
 }
 
 // dst[ids[i]] (+)= code * scale + zero of codes row i (ids null: row i); the
