@@ -188,6 +188,7 @@ static void destroy_graph(gnn_graph *g) {
     cudaFree(g->err);
     cudaFree(g->ws);
     cudaFree(g->claim);
+    cudaFree(g->push_ok);
     free_schedule(&g->fwd);
     free_schedule(&g->bwd);
     delete g;

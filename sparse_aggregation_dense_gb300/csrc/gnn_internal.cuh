@@ -95,6 +95,8 @@ struct gnn_graph {
     uint32_t *claim = nullptr;
     int64_t claim_n = 0;
     uint32_t claim_gen = 0;
+    uint8_t *push_ok = nullptr;  // per pushed row: its id may be written (after the claim pass)
+    int64_t push_ok_n = 0;
     // event timing (gnn_profile_enable)
     struct ProfRec {
         int kind;

@@ -106,12 +106,28 @@ __global__ void push_claim_kernel(const int64_t *__restrict__ ids, int64_t n, in
     }
 }
 
+// after the claim pass: ok[v] = 1 when row v's id is in range and was claimed
+// once (a repeated id sets the error word and its rows are not copied).  The
+// copy then reads one byte per row in row order instead of a claim word at a
+// random place behind the id's load.
+__global__ void push_ok_kernel(const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
+                               const uint32_t *__restrict__ claim, uint32_t gen, uint8_t *__restrict__ ok, int *err) {
+    const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= n) return;
+    const int64_t id = ids[v];
+    uint8_t good = 0;
+    if (id >= 0 && id < n_table) {  // out-of-range ids are reported by the claim pass
+        if (claim[id] == ((gen << 2) | 1u)) good = 1;
+        else atomicOr(err, 1);  // repeated id: no copy of it is written
+    }
+    ok[v] = good;
+}
+
 template <int LPR>
 __global__ void __launch_bounds__(256, 3) push_copy_kernel(const char *__restrict__ H, int64_t row_bytes_h,
-                                                        const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
-                                                        const uint32_t *__restrict__ claim, uint32_t gen,
-                                                        char *__restrict__ table, int64_t row_bytes_t, int64_t nbytes,
-                                                        int es, int *err) {
+                                                        const int64_t *__restrict__ ids, int64_t n,
+                                                        const uint8_t *__restrict__ ok, char *__restrict__ table,
+                                                        int64_t row_bytes_t, int64_t nbytes, int es) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t v0 = (t / LPR) * kRowsPerGroup;
     const int sub = (int)(t % LPR);
@@ -128,16 +144,8 @@ __global__ void __launch_bounds__(256, 3) push_copy_kernel(const char *__restric
     int64_t ix[kRowsPerGroup];
 #pragma unroll
     for (int k = 0; k < kRowsPerGroup; ++k) {
-        ix[k] = -1;
         const int64_t v = v0 + k;
-        if (v >= n) continue;
-        const int64_t id = __ldg(ids + v);
-        if (id < 0 || id >= n_table) continue;  // reported by the claim pass
-        if (claim[id] != ((gen << 2) | 1u)) {
-            if (sub == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
-            continue;
-        }
-        ix[k] = id;
+        ix[k] = (v < n && __ldg(ok + v)) ? __ldg(ids + v) : -1;
     }
 #pragma unroll
     for (int k = 0; k < kRowsPerGroup; ++k)
@@ -212,20 +220,37 @@ gnn_status launch_push_claim(gnn_graph *g, const int64_t *ids, int64_t n_rows, i
     return GNN_OK;
 }
 
+gnn_status ensure_push_ok(gnn_graph *g, int64_t n_rows) {
+    if (g->push_ok_n >= n_rows) return GNN_OK;
+    // grow the per-row flags; ordered after earlier work on the device
+    GNN_CUDA_TRY(cudaDeviceSynchronize());
+    if (g->push_ok) GNN_CUDA_TRY(cudaFree(g->push_ok));
+    g->push_ok = nullptr;
+    g->push_ok_n = 0;
+    GNN_CUDA_TRY(cudaMalloc((void **)&g->push_ok, (size_t)n_rows));
+    g->push_ok_n = n_rows;
+    return GNN_OK;
+}
+
 gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
                        void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
     if (n_rows == 0) return GNN_OK;
     uint32_t gen = 0;
-    gnn_status st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
+    gnn_status st = ensure_push_ok(g, n_rows);
     if (st != GNN_OK) return st;
+    st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
+    if (st != GNN_OK) return st;
+    { push_ok_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, s>>>(ids, n_rows, n_table, g->claim, gen, g->push_ok,
+                                                                     g->err); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
     const int64_t nbytes = f * es;
     const int lpr = lanes_per_row(nbytes);
     return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
         constexpr int LPR = decltype(L)::value;
         const int64_t blocks = ceil_div(ceil_div(n_rows, kRowsPerGroup) * LPR, 256);
         { push_copy_kernel<LPR><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const char *>(H), ld_h * es, ids, n_rows,
-                                                               n_table, g->claim, gen, static_cast<char *>(table),
-                                                               ld_t * es, nbytes, es, g->err); GNN_LAUNCHED(1); }
+                                                               g->push_ok, static_cast<char *>(table), ld_t * es,
+                                                               nbytes, es); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
         return GNN_OK;
     });
