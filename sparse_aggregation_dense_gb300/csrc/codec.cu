@@ -232,27 +232,22 @@ __device__ __forceinline__ void quantize_row(const T *__restrict__ h, const floa
     }
 }
 
-// Quantise pushed rows: row v of H goes to table row ids[v] if the claim pass
-// saw that id exactly once (else the row is skipped and the error word set).
+// Quantise pushed rows: row v of H goes to table row ids[v] if the push checks
+// passed it (id in range and seen once; else the row is skipped).
 template <typename T, int BITS>
 __global__ void __launch_bounds__(256) codec_push_kernel(const T *__restrict__ H, int64_t ld_h,
-                                                         const int64_t *__restrict__ ids, int64_t n, int64_t n_table,
-                                                         const uint32_t *__restrict__ claim, uint32_t gen,
-                                                         uint8_t *__restrict__ codes, int64_t ld_codes,
-                                                         float *__restrict__ scale_zero, int64_t f, uint64_t seed,
-                                                         int *err) {
+                                                         const int64_t *__restrict__ ids, int64_t n,
+                                                         const uint8_t *__restrict__ ok, uint8_t *__restrict__ codes,
+                                                         int64_t ld_codes, float *__restrict__ scale_zero, int64_t f,
+                                                         uint64_t seed) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < n; v += nw) {
         // the row's values do not depend on its id: their load overlaps the id and claim-word loads
         float x0[8];
         load8(H + v * ld_h, lane * 8, (int)f, x0);
+        if (!ok[v]) continue;  // id out of range or repeated (reported by the checks)
         const int64_t id = ids[v];
-        if (id < 0 || id >= n_table) continue;  // reported by the claim pass
-        if (claim[id] != ((gen << 2) | 1u)) {
-            if (lane == 0) atomicOr(err, 1);  // repeated id: no copy of it is written
-            continue;
-        }
         quantize_row<T, BITS>(H + v * ld_h, x0, id, codes + id * ld_codes, ld_codes, scale_zero + 2 * id, f, seed,
                               lane);
     }
@@ -364,8 +359,7 @@ gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
                              uint8_t *codes, int64_t ld_codes, float *scale_zero, int64_t n_table, int bits,
                              uint64_t seed, gnn_dtype dt, cudaStream_t s) {
     if (n_rows == 0) return GNN_OK;
-    uint32_t gen = 0;
-    gnn_status st = launch_push_claim(g, ids, n_rows, n_table, &gen, s);
+    gnn_status st = launch_push_checks(g, ids, n_rows, n_table, s);
     if (st != GNN_OK) return st;
     // one warp per row: the quantisation is arithmetic-heavy and a bounded
     // grid looping over the rows measured slower
@@ -374,12 +368,11 @@ gnn_status launch_codec_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t 
         constexpr int BITS = decltype(Bc)::value;
         if (dt == GNN_BF16)
             { codec_push_kernel<__nv_bfloat16, BITS><<<blocks, 256, 0, s>>>(
-                static_cast<const __nv_bfloat16 *>(H), ld_h, ids, n_rows, n_table, g->claim, gen, codes, ld_codes,
-                scale_zero, f, seed, g->err); GNN_LAUNCHED(1); }
+                static_cast<const __nv_bfloat16 *>(H), ld_h, ids, n_rows, g->push_ok, codes, ld_codes, scale_zero, f,
+                seed); GNN_LAUNCHED(1); }
         else
             { codec_push_kernel<float, BITS><<<blocks, 256, 0, s>>>(static_cast<const float *>(H), ld_h, ids, n_rows,
-                                                                   n_table, g->claim, gen, codes, ld_codes, scale_zero,
-                                                                   f, seed, g->err); GNN_LAUNCHED(1); }
+                                                                   g->push_ok, codes, ld_codes, scale_zero, f, seed); GNN_LAUNCHED(1); }
         GNN_CUDA_TRY(cudaGetLastError());
         return GNN_OK;
     });

@@ -199,6 +199,9 @@ gnn_status ensure_claim(gnn_graph *g, int64_t n_table);
 // (ids seen more than once are reported and skipped by the copy)
 gnn_status launch_push_claim(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, uint32_t *gen_out,
                              cudaStream_t s);
+// the checks of a push: the claim pass, then g->push_ok[v] = 1 for every row
+// whose id is in range and claimed once (repeated ids set the error word)
+gnn_status launch_push_checks(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, cudaStream_t s);
 // halo-gradient return: send J rows into an fp32 gradient table, receive the sums
 gnn_status launch_grad_send(gnn_graph *g, const void *dH, int64_t ld_dh, int64_t f, const int64_t *halo_ids,
                             float *gtable, int64_t ld_gt, int64_t n_table, gnn_dtype dt, cudaStream_t s);

@@ -232,9 +232,7 @@ gnn_status ensure_push_ok(gnn_graph *g, int64_t n_rows) {
     return GNN_OK;
 }
 
-gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
-                       void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
-    if (n_rows == 0) return GNN_OK;
+gnn_status launch_push_checks(gnn_graph *g, const int64_t *ids, int64_t n_rows, int64_t n_table, cudaStream_t s) {
     uint32_t gen = 0;
     gnn_status st = ensure_push_ok(g, n_rows);
     if (st != GNN_OK) return st;
@@ -243,6 +241,14 @@ gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows
     { push_ok_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, s>>>(ids, n_rows, n_table, g->claim, gen, g->push_ok,
                                                                      g->err); GNN_LAUNCHED(1); }
     GNN_CUDA_TRY(cudaGetLastError());
+    return GNN_OK;
+}
+
+gnn_status launch_push(gnn_graph *g, const void *H, int64_t ld_h, int64_t n_rows, int64_t f, const int64_t *ids,
+                       void *table, int64_t ld_t, int64_t n_table, int es, cudaStream_t s) {
+    if (n_rows == 0) return GNN_OK;
+    gnn_status st = launch_push_checks(g, ids, n_rows, n_table, s);
+    if (st != GNN_OK) return st;
     const int64_t nbytes = f * es;
     const int lpr = lanes_per_row(nbytes);
     return dispatch_lpr(lpr, [&](auto L) -> gnn_status {
