@@ -876,9 +876,17 @@ def main(argv=None):
                     help="pulls and pushes in line on the compute stream instead of on a second stream")
     ap.add_argument("--gather-ceiling", action="store_true",
                     help="measure the aggregation's gather throughput on uniform random columns and exit")
+    ap.add_argument("--gat-only", action="store_true",
+                    help="time the graph-attention epoch of --gat-workload alone and exit")
     args = ap.parse_args(argv)
     if args.gather_ceiling:
         return gather_ceiling()
+    if args.gat_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        print(json.dumps({"gat": measure_gat(args.gat_workload, steps=max(1, args.steps))}))
+        return None
     if args.narrow and args.grad_dtype != "bf16" and workload_by_name(args.workload).dtype == "bf16":
         args.grad_dtype = "bf16"  # the multiplication-first layers keep their gradients in the activations' dtype
     if args.warmup < 3 and args.impl == "ours" and not args.workload.endswith("-tiny"):
