@@ -418,6 +418,32 @@ def test_ragged_widths(dt, gd, agg, f_in, f_out):
     _run_layer_pair(part, g, agg, dt, f_in, f_out, relu=True, gd=gd)
 
 
+@pytest.mark.parametrize("dt,gd,f_in", [("f32", "f32", 1024), ("bf16", "bf16", 2048), ("bf16", "f32", 1024)])
+def test_maximum_widths(dt, gd, f_in):
+    # rows of 4096 bytes, the widest the aggregation takes (in the activations' and the gradients' types); a
+    # bf16 update with K = 2048 runs its backward in eight 256-column slices
+    part = synth.chunglu_partition(1500, 12000, 16.0, 3, seed=7)
+    g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(), part.n_local,
+                         part.n_halo, torch.from_numpy(part.deg).cuda(), "gcn")
+    _run_layer_pair(part, g, "gcn", dt, f_in, 16, relu=True, gd=gd)
+    # eight columns wider are refused before anything runs: the forward's rows (same dtype), or with fp32
+    # gradients the backward's fp32 rows
+    tdt, gdt = torch_dtype(dt), torch_dtype(gd)
+    fw = f_in + 8
+    H = padded(part.n_total, fw, tdt, "cuda")
+    Z = padded(part.n_local, fw, tdt, "cuda")
+    Ho = padded(part.n_local, 16, tdt, "cuda")
+    W = torch.zeros((fw, 16), device="cuda")
+    with pytest.raises(gnn.GnnError) as e:
+        if dt == gd:
+            gnn.layer_forward(g, H, W, True, Z, Ho)
+        else:
+            gnn.layer_backward(g, padded(part.n_local, 16, gdt, "cuda"), Ho, Z, W, True,
+                               torch.zeros((fw, 16), device="cuda"), fw, dZ=padded(part.n_local, fw, gdt, "cuda"),
+                               dH=padded(part.n_total, fw, gdt, "cuda"), want_halo_grad=True)
+    assert e.value.status == gnn.GNN_EUNSUPPORTED
+
+
 @pytest.mark.parametrize("dt,gd", PRECISIONS)
 @pytest.mark.parametrize("agg", ["gcn", "sage"])
 def test_heavy_rows_and_columns(dt, gd, agg):
