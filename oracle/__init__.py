@@ -43,7 +43,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=gnu11", _SRC, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", "-O3", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=gnu11", _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
