@@ -701,7 +701,8 @@ def run_ours(args, rank, world, local_rank):
         other_prec = measure_other_precision(m, stream, max(3, min(args.steps, 5)), ef) if bf and not args.narrow \
             else None
         h2d_gbs = measure_h2d(x_pin, h0, stream)
-    gat = None if (args.quick or not args.gat_workload) else measure_gat(args.gat_workload)
+    gat = None if (args.quick or not args.gat_workload) else \
+        [measure_gat(x) for x in args.gat_workload.split(",") if x]
     h2d = int(x_pin.numel() * x_pin.element_size() + y_pin.numel() * 4)
     d2h = int(4 + sum(d.numel() * 4 for d in m.dW))
 
@@ -864,8 +865,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work timed for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=3.0, help="oracle work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gat-workload", default="rmat131k",
-                    help="workload of the graph-attention epoch reported beside the step ('' to skip)")
+    ap.add_argument("--gat-workload", default="rmat131k,sage2m",
+                    help="workloads (comma-separated) of the graph-attention epochs reported beside the step "
+                         "('' to skip)")
     ap.add_argument("--quick", action="store_true",
                     help="time the step only (no codec, other schedule, other precision or H2D figures)")
     ap.add_argument("--narrow", action="store_true",
@@ -885,7 +887,8 @@ def main(argv=None):
         import torch
 
         torch.cuda.set_device(0)
-        print(json.dumps({"gat": measure_gat(args.gat_workload, steps=max(1, args.steps))}))
+        print(json.dumps({"gat": [measure_gat(x, steps=max(1, args.steps)) for x in args.gat_workload.split(",")
+                                  if x]}))
         return None
     if args.narrow and args.grad_dtype != "bf16" and workload_by_name(args.workload).dtype == "bf16":
         args.grad_dtype = "bf16"  # the multiplication-first layers keep their gradients in the activations' dtype
