@@ -516,6 +516,29 @@ def measure_other_precision(m, stream, steps: int, ef: int):
             "steps": steps}
 
 
+def measure_other_order(m, stream, steps: int, ef: int):
+    """The step with the backward of GCN layers l > 0 in the other product order: P = A_hat^T dY gathered in
+    bf16, dH = P W^T (bf16 activations, fp32 gradients)."""
+    import torch
+
+    m.set_reorder(True)
+    try:
+        m.step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        m.check_errors()
+        ms = e0.elapsed_time(e1) / steps
+    finally:
+        m.set_reorder(False)
+    return {"backward": "dH = (A_hat^T dY) W^T on layers l > 0, P in bf16", "ms_per_step": ms,
+            "value": ef / (ms / 1e3), "steps": steps}
+
+
 def measure_gat(workload: str, steps: int = 5):
     """A 3-layer graph-attention epoch (GatModel) on another workload: ms per step and edge x feature / s
     (the attention-weighted sums counted like the GCN aggregations)."""
@@ -694,12 +717,14 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, True)
     if args.quick:  # tuning runs: the timed step and its breakdown only
-        codec, other_ms, other_prec, h2d_gbs = None, float("nan"), None, float("nan")
+        codec, other_ms, other_prec, other_order, h2d_gbs = None, float("nan"), None, None, float("nan")
     else:
         codec = measure_codec(m, part, w, tdt, stream)
         other_ms = measure_other_schedule(m, stream, max(3, min(args.steps, 5)))
         other_prec = measure_other_precision(m, stream, max(3, min(args.steps, 5)), ef) if bf and not args.narrow \
             else None
+        other_order = measure_other_order(m, stream, max(3, min(args.steps, 5)), ef) \
+            if bf and w.agg == "gcn" and gdt == torch.float32 and not args.narrow else None
         h2d_gbs = measure_h2d(x_pin, h0, stream)
     gat = None if (args.quick or not args.gat_workload) else \
         [measure_gat(x) for x in args.gat_workload.split(",") if x]
@@ -769,6 +794,7 @@ def run_ours(args, rank, world, local_rank):
                                  "copy stream (features once layer 0 has read H[0], labels once the loss has)",
                 "h2d_gbs_feature_copy_alone": round(h2d_gbs, 1)},
         "other_precision": other_prec,
+        "other_order": other_order,
         "gat": gat,
         "gpu_launches": int(launches),
         "halo_codec": codec,

@@ -222,6 +222,27 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
                               float *dW, void *dZ, int64_t ld_dz, void *dH, int64_t ld_dh, int want_halo_grad,
                               gnn_dtype dtype, gnn_dtype grad_dtype, void *stream);
 
+/* The backward of a GCN layer (gnn_layer_forward's) with the products in the
+ * other order: dH = (A_hat_block^T dY) W^T instead of A_hat_block^T (dY W^T)
+ * (associativity; the chain rule of the CAGNET page's H = sigma(A^T H W)).
+ * The transposed aggregation then gathers the bf16 rows of dY (f_out values)
+ * instead of the fp32 rows of dZ (f_in values).
+ *   dY = G * 1[H_out > 0] (or G) rounded to bf16, as in gnn_layer_backward
+ *   dW = Z^T dY                  device float[f_in x f_out], overwritten
+ *   P  = A_hat_block^T dY        device (n_local or n_local + n_halo) x ld_p,
+ *                                bf16 (fp32 sums, rounded once: it is the
+ *                                operand of the next product)
+ *   dH = P W^T                   device (as P's rows) x ld_dh, fp32
+ * want_halo_grad != 0 computes P and dH for the halo rows too (Sylvie's J).
+ * The results agree with gnn_layer_backward up to the rounding of P.  Only the
+ * GCN aggregation with bf16 activations and fp32 gradients, on the tensor
+ * cores, is taken: other graphs, precision pairs or widths return
+ * GNN_EUNSUPPORTED before anything runs; bad pointers or sizes GNN_EINVAL. */
+gnn_status gnn_layer_backward_reordered(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                                        const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out,
+                                        int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
+                                        int want_halo_grad, gnn_dtype dtype, gnn_dtype grad_dtype, void *stream);
+
 /* The same GCN layer with the multiplication first, for layers whose output
  * is narrower than their input (f_out < f_in): A_hat (H W) = (A_hat H) W, so
  * the aggregations run at width f_out instead of f_in (fewer bytes gathered);

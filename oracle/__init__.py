@@ -528,6 +528,29 @@ def layer_backward(part, T, G: np.ndarray, Hout: np.ndarray, Z: np.ndarray, W: n
     return dW, dZ, dH
 
 
+def layer_backward_reordered(part, T, G: np.ndarray, Hout: np.ndarray, Z: np.ndarray, W: np.ndarray, relu: bool,
+                             bf16: bool = False, rows=None):
+    """(dW, P, dH) of a GCN layer with the backward products in the other order
+    (associativity of the chain rule of H = sigma(A^T H W), CAGNET page, GNN
+    section): dY = G * 1[Hout > 0] (or G); dW = Z^T dY; P = A_hat^T dY over the
+    output rows `rows` (default all n_local + n_halo); dH = P W^T.
+
+    bf16=True: bf16 activations with fp32 gradients as the library's path takes
+    them: dY rounded to bf16 (an operand of the products, as in layer_backward)
+    and P rounded to bf16 once (the operand of dH = P W^T); dH itself is not
+    rounded (fp32 gradient storage).  With bf16=False it equals layer_backward's
+    dH exactly up to the order of the sums."""
+    G, Hout, Z, W = _f64(G), _f64(Hout), _f64(Z), _f64(W)
+    dY = G * (Hout > 0) if relu else G
+    if bf16:
+        dY = round_bf16(dY)
+    dW, _ = update_backward(dY, Hout, Z, W, False, want_dz=False)
+    P = aggregate_backward(part, T, dY, dY.shape[1], "gcn", rows=rows)
+    if bf16:
+        P = round_bf16(P)
+    return dW, P, P @ W.T
+
+
 def epoch(part, tables: Sequence[np.ndarray], Ws: Sequence[np.ndarray], labels_local: np.ndarray, agg: str,
           bf16: bool = False, grad_bf16: bool = False):
     """One full-graph epoch of an L-layer model on one partition.

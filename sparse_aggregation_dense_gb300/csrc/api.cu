@@ -591,6 +591,78 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
     return launch_aggregate(p, g->bwd, grad_dtype, partial, s);
 }
 
+gnn_status gnn_layer_backward_reordered(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
+                                        const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out,
+                                        int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
+                                        int want_halo_grad, gnn_dtype dtype, gnn_dtype grad_dtype, void *stream) {
+    if (g && g->agg == GNN_AGG_GAT) return GNN_EINVAL;  // attention layers: gnn_gat_forward / backward
+    if (!g || !dtype_ok(dtype) || !dtype_ok(grad_dtype) || f_in <= 0 || f_out <= 0 || !W || !dW || !dH)
+        return GNN_EINVAL;
+    // the GCN layer, bf16 activations with fp32 gradients, on the tensor cores
+    if (g->agg != GNN_AGG_GCN_SYM || dtype != GNN_BF16 || grad_dtype != GNN_F32) return GNN_EUNSUPPORTED;
+    const int64_t nL = g->n_local, nT = g->n_local + g->n_halo;
+    const int64_t out_rows = want_halo_grad ? nT : nL;
+    if (!operand_ok(G, nL, ld_g, f_out, GNN_F32) || !operand_ok(Z, nL, ld_z, f_in, GNN_BF16) ||
+        !operand_ok(P, out_rows, ld_p, f_out, GNN_BF16) || !operand_ok(dH, out_rows, ld_dh, f_in, GNN_F32))
+        return GNN_EINVAL;
+    if (relu && !operand_ok(H_out, nL, ld_out, f_out, GNN_BF16)) return GNN_EINVAL;
+    if (f_out * 2 > 4096 || !update_bwd_tc_supported(f_in, f_out) || force_simt_update()) return GNN_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const int64_t ldw = round_up(f_out, 4);
+    const int64_t ldy = round_up(f_out, 8);
+    const size_t wp_bytes = align_up((size_t)f_in * ldw * sizeof(float));
+    const size_t y_bytes = align_up((size_t)(nL > 0 ? nL : 1) * ldy * 2);
+    const size_t wg_bytes = align_up(update_bwd_tc_ws_bytes(out_rows > nL ? out_rows : nL, f_in, f_out));
+    const size_t part_bytes = align_up(aggregate_partial_bytes(g->bwd, f_out));
+    gnn_status st = ensure_workspace(g, wp_bytes + y_bytes + wg_bytes + part_bytes, s);
+    if (st != GNN_OK) return st;
+    char *base = static_cast<char *>(g->ws);
+    float *Wp = reinterpret_cast<float *>(base);
+    void *Y = base + wp_bytes;
+    float *wg = reinterpret_cast<float *>(base + wp_bytes + y_bytes);
+    float *partial = reinterpret_cast<float *>(base + wp_bytes + y_bytes + wg_bytes);
+    { pack_w_kernel<<<(unsigned)ceil_div(f_in * ldw, 256), 256, 0, s>>>(W, f_in, f_out, f_in, f_in, 0, f_in, Wp, ldw,
+                                                                        true); GNN_LAUNCHED(1); }
+    GNN_CUDA_TRY(cudaGetLastError());
+    {
+        // dY = G * 1[H_out > 0] rounded to bf16, and dW = Z^T dY
+        ProfScope prof(g, GNN_PROF_UPD_BWD, s);
+        st = launch_grad_to_bf16(static_cast<const float *>(G), ld_g, relu ? H_out : nullptr, ld_out, nL, f_out, Y,
+                                 ldy, s);
+        if (st == GNN_OK)
+            st = launch_update_bwd_tc(Y, ldy, nullptr, 0, 0, Z, ld_z, nL, f_in, Wp, ldw, f_out, dW, nullptr, 0, true,
+                                      wg, g->err, s);
+    }
+    if (st != GNN_OK) return st;
+    {
+        // P = A_hat^T dY over the output rows (gathering the bf16 dY rows), stored in bf16: the product's operand
+        AggParams p{};
+        p.err = g->err;
+        p.rowptr = g->rowptrT;
+        p.colidx = reinterpret_cast<const uint32_t *>(g->colidxTa ? g->colidxTa : g->colidxT);
+        p.wts = g->wbwd;
+        p.rowscale = g->colw;
+        p.n_rows = out_rows;
+        p.colmask = g->bwd.tagged ? kColMask : 0xffffffffu;
+        p.hot_tier = hot_tier_for(g->bwd, round_up(f_out * 2, 32));
+        p.X = Y;
+        p.ldx = ldy;
+        p.n_x = nL;
+        p.f = f_out;
+        p.self_mode = SELF_NONE;
+        p.out = P;
+        p.ldo = ld_p;
+        p.out_off = 0;
+        ProfScope prof(g, GNN_PROF_AGG_BWD, s);
+        st = launch_aggregate(p, g->bwd, GNN_BF16, partial, s);
+    }
+    if (st != GNN_OK) return st;
+    // dH = P W^T over the output rows, fp32
+    ProfScope prof(g, GNN_PROF_UPD_BWD, s);
+    return launch_update_bwd_tc(P, ld_p, nullptr, 0, 0, nullptr, 0, out_rows, f_in, Wp, ldw, f_out, nullptr, dH, ld_dh,
+                                true, wg, g->err, s);
+}
+
 gnn_status gnn_layer_forward_narrow(gnn_graph *g, const void *H, int64_t ld_h, int64_t f_in, const float *W,
                                     int64_t f_out, int relu, void *T, int64_t ld_t, void *H_out, int64_t ld_out,
                                     gnn_dtype dtype, void *stream) {

@@ -586,9 +586,9 @@ gnn_status launch_update_bwd_tc(const void *G, int64_t ld_g, const void *Hout, i
     const int64_t dzb = dz_f32 ? 4 : 2;
     for (int64_t k0 = 0; k0 < Kp; k0 += ks) {
         const gnn_status st = bwd_tc_pass(
-            G, ld_g, Hout, ld_h, relu, static_cast<const char *>(Z) + k0 * 2, ld_z, n, Kp - k0 < ks ? Kp - k0 : ks,
-            Wp + k0 * ld_w, ld_w, N, dWp + k0 * N, dZ ? static_cast<char *>(dZ) + k0 * dzb : nullptr, ld_dz, dz_f32,
-            ws, err, s);
+            G, ld_g, Hout, ld_h, relu, Z ? static_cast<const char *>(Z) + k0 * 2 : nullptr, ld_z, n,
+            Kp - k0 < ks ? Kp - k0 : ks, Wp + k0 * ld_w, ld_w, N, dWp ? dWp + k0 * N : nullptr,
+            dZ ? static_cast<char *>(dZ) + k0 * dzb : nullptr, ld_dz, dz_f32, ws, err, s);
         if (st != GNN_OK) return st;
     }
     return GNN_OK;
@@ -602,7 +602,7 @@ gnn_status bwd_tc_pass(const void *G, int64_t ld_g, const void *Hout, int64_t ld
     BwdPlan p;
     if (!plan_bwd(Kp, N, relu, &p)) return GNN_EUNSUPPORTED;
     if (n == 0) {
-        GNN_CUDA_TRY(cudaMemsetAsync(dWp, 0, (size_t)Kp * N * sizeof(float), s));
+        if (dWp) GNN_CUDA_TRY(cudaMemsetAsync(dWp, 0, (size_t)Kp * N * sizeof(float), s));
         return GNN_OK;
     }
     const int64_t wtiles = ceil_div(n, kWRows);
@@ -611,20 +611,23 @@ gnn_status bwd_tc_pass(const void *G, int64_t ld_g, const void *Hout, int64_t ld
     __nv_bfloat16 *Wk = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) +
                                                           round_up((int64_t)wgrid * Kp * N * 4, 256));
     CUtensorMap mG, mH, mZ, mW;
-    // wgrad
-    if (!make_map_bf16_2d(&mZ, Z, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_z * 2, 64, kWRows)) return GNN_ECUDA;
-    if (!make_map_bf16_2d(&mG, G, (uint64_t)N, (uint64_t)n, (uint64_t)ld_g * 2, 64, kWRows)) return GNN_ECUDA;
-    if (!make_map_bf16_2d(&mH, relu ? Hout : G, (uint64_t)N, (uint64_t)n, (uint64_t)(relu ? ld_h : ld_g) * 2, 64,
-                          kWRows))
-        return GNN_ECUDA;
-    GNN_CUDA_TRY(cudaFuncSetAttribute(update_wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)p.wsmem));
-    { update_wgrad_tc_kernel<<<(unsigned)wgrid, kThreadsB, p.wsmem, s>>>(mZ, mG, mH, partial, n, (int)Kp, (int)p.MB,
-                                                                        (int)N, (int)p.N_pad, (int)p.NC, p.wstages,
-                                                                        relu, wtiles, err); GNN_LAUNCHED(1); }
-    GNN_CUDA_TRY(cudaGetLastError());
-    { sum_partials_kernel<<<(unsigned)ceil_div(Kp * N, 256), 256, 0, s>>>(partial, wgrid, Kp * N, dWp); GNN_LAUNCHED(1); }
-    GNN_CUDA_TRY(cudaGetLastError());
+    // wgrad (skipped when dWp is null: dZ only)
+    if (dWp) {
+        if (!make_map_bf16_2d(&mZ, Z, (uint64_t)Kp, (uint64_t)n, (uint64_t)ld_z * 2, 64, kWRows)) return GNN_ECUDA;
+        if (!make_map_bf16_2d(&mG, G, (uint64_t)N, (uint64_t)n, (uint64_t)ld_g * 2, 64, kWRows)) return GNN_ECUDA;
+        if (!make_map_bf16_2d(&mH, relu ? Hout : G, (uint64_t)N, (uint64_t)n, (uint64_t)(relu ? ld_h : ld_g) * 2, 64,
+                              kWRows))
+            return GNN_ECUDA;
+        GNN_CUDA_TRY(cudaFuncSetAttribute(update_wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)p.wsmem));
+        { update_wgrad_tc_kernel<<<(unsigned)wgrid, kThreadsB, p.wsmem, s>>>(mZ, mG, mH, partial, n, (int)Kp, (int)p.MB,
+                                                                            (int)N, (int)p.N_pad, (int)p.NC, p.wstages,
+                                                                            relu, wtiles, err); GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+        { sum_partials_kernel<<<(unsigned)ceil_div(Kp * N, 256), 256, 0, s>>>(partial, wgrid, Kp * N, dWp);
+          GNN_LAUNCHED(1); }
+        GNN_CUDA_TRY(cudaGetLastError());
+    }
     if (!dZ) return GNN_OK;
     // dgrad
     { pack_wk_bf16_kernel<<<(unsigned)ceil_div(p.Kp_pad * p.N_pad, 256), 256, 0, s>>>(Wp, ld_w, Kp, N, p.Kp_pad,

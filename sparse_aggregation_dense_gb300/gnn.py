@@ -32,7 +32,7 @@ EXPORTS = (
     "gnn_halo_pull_quantized", "gnn_softmax_ce_partial", "gnn_halo_grad_send", "gnn_halo_grad_recv",
     "gnn_layer_forward_narrow", "gnn_layer_backward_narrow", "gnn_profile_enable", "gnn_profile_read", "gnn_launch_count",
     "gnn_aggregate_forward_noalloc", "gnn_debug_expire_next_wait", "gnn_gather_rows", "gnn_scatter_add_rows",
-    "gnn_gat_forward", "gnn_gat_backward", "gnn_quantize_rows", "gnn_dequantize_rows",
+    "gnn_gat_forward", "gnn_gat_backward", "gnn_quantize_rows", "gnn_dequantize_rows", "gnn_layer_backward_reordered",
 )
 
 PROF_KINDS = ("agg_fwd", "agg_bwd", "upd_fwd", "upd_bwd", "pull", "push")
@@ -68,6 +68,8 @@ def _lib():
         L.gnn_layer_forward.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
         L.gnn_layer_backward.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp, i64, i32,
                                          i32, i32, vp]
+        L.gnn_layer_backward_reordered.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp,
+                                                   i64, i32, i32, i32, vp]
         L.gnn_softmax_ce.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, i32, vp]
         L.gnn_layer_forward_narrow.argtypes = [vp, vp, i64, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp]
         L.gnn_layer_backward_narrow.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp, i64, i64, i32, vp, vp, i64, vp,
@@ -537,6 +539,32 @@ def layer_backward(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tens
                                      _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(dZ), ld_dz, _ptr(dH), ld_dh,
                                      int(want_halo_grad), _dtype(Z), _dtype(G), ctypes.c_void_p(_stream())),
            "gnn_layer_backward")
+
+
+def layer_backward_reordered(g: Graph, G: torch.Tensor, H_out: torch.Tensor, Z: torch.Tensor, W: torch.Tensor,
+                             relu: bool, dW: torch.Tensor, P: torch.Tensor, dH: torch.Tensor,
+                             want_halo_grad: bool = True):
+    """GCN layer backward in the other product order: dW = Z^T dY, P = A_block^T dY (bf16), dH = P W^T (fp32).
+    bf16 activations (H_out, Z) with fp32 gradients (G, dH) only; halo rows too if want_halo_grad."""
+    ld_g, f_out = _mat(G)
+    ld_o, _ = _mat(H_out)
+    ld_z, f_in = _mat(Z)
+    ld_p, _ = _mat(P)
+    ld_dh, _ = _mat(dH)
+    what = "gnn_layer_backward_reordered"
+    rows = g.n_total if want_halo_grad else g.n_local
+    _weights(what, W, f_in, f_out)
+    _weights(what, dW, f_in, f_out)
+    _need(Z.dtype == H_out.dtype == P.dtype == torch.bfloat16 and G.dtype == dH.dtype == torch.float32, what,
+          "bf16 activations and P, fp32 gradients")
+    _need(_rows(G) >= g.n_local and _rows(H_out) >= g.n_local and _rows(Z) >= g.n_local, what,
+          "G, H_out and Z need n_local rows")
+    _need(_rows(P) >= rows and _width(P) >= f_out and _rows(dH) >= rows and _width(dH) >= f_in, what,
+          "P and dH need a row per output row (halo rows too with the halo gradient)")
+    _check(_lib().gnn_layer_backward_reordered(ctypes.c_void_p(g.handle), _ptr(G), ld_g, _ptr(H_out), ld_o, _ptr(Z),
+                                               ld_z, _ptr(W), f_in, f_out, int(relu), _ptr(dW), _ptr(P), ld_p,
+                                               _ptr(dH), ld_dh, int(want_halo_grad), _dtype(Z), _dtype(G),
+                                               ctypes.c_void_p(_stream())), what)
 
 
 def _softmax_args(what: str, logits, labels, G, row_loss, loss):

@@ -41,11 +41,13 @@ class PartitionModel:
     None), local_ids, halo_ids (int64 numpy), n_table.
     widths: [f_0, ..., f_L]; agg "gcn" | "sage"; dtype torch.float32 | torch.bfloat16: the activations
     (features, tables, Z, layer outputs).  grad_dtype: the activation gradients (G, dZ, dH); fp32 by default,
-    bf16 allowed with bf16 activations.
+    bf16 allowed with bf16 activations.  reorder: the backward of GCN layers l > 0 (bf16 activations, fp32
+    gradients) gathers dY instead of dZ: dH = (A_hat^T dY) W^T, the other order of the same products.
     """
 
     def __init__(self, part, widths: Sequence[int], agg: str, dtype: torch.dtype, device="cuda",
-                 overlap: bool = False, narrow: bool = False, grad_dtype: torch.dtype = torch.float32):
+                 overlap: bool = False, narrow: bool = False, grad_dtype: torch.dtype = torch.float32,
+                 reorder: bool = False):
         if dtype == torch.float32 and grad_dtype != torch.float32:
             raise ValueError("fp32 activations take fp32 gradients")
         if narrow and grad_dtype != dtype:
@@ -85,6 +87,10 @@ class PartitionModel:
         self.P = padded(nT, max([widths[l + 1] for l in range(self.L) if self.narrow[l]] + [1]), grad_dtype, dev) \
             if any(self.narrow) else None
         self._alloc_grads()
+        self.reorder = False
+        self.Pr = None
+        if reorder:
+            self.set_reorder(True)
         self.W: List[torch.Tensor] = []
         self.dW: List[torch.Tensor] = []
         for l in range(self.L):
@@ -113,10 +119,26 @@ class PartitionModel:
             raise ValueError("fp32 activations take fp32 gradients")
         if any(self.narrow) and grad_dtype != self.dtype:
             raise ValueError("the multiplication-first layers store their gradients in the activations' dtype")
+        if self.reorder and grad_dtype != torch.float32:
+            raise ValueError("the reordered backward takes fp32 gradients")
         if grad_dtype != self.grad_dtype:
             self.dZ = self.dH = self.G_last = None
             self.grad_dtype = grad_dtype
             self._alloc_grads()
+
+    def _reordered(self, l: int) -> bool:
+        return self.reorder and l > 0 and not self.narrow[l]
+
+    def set_reorder(self, on: bool):
+        """Run the backward of GCN layers l > 0 in the other product order from the next step on: P = A_hat^T dY
+        (bf16, local and halo rows), dH = P W^T.  Needs bf16 activations with fp32 gradients."""
+        if on and (self.agg != "gcn" or self.dtype != torch.bfloat16 or self.grad_dtype != torch.float32):
+            raise ValueError("the reordered backward takes GCN layers with bf16 activations and fp32 gradients")
+        if on and self.Pr is None:
+            nT = self.n_local + self.n_halo
+            self.Pr = padded(nT, max([self.widths[l + 1] for l in range(1, self.L)] + [1]), torch.bfloat16,
+                             self.device)
+        self.reorder = on
 
     # ---- views ------------------------------------------------------------
     def layer_out(self, l: int) -> torch.Tensor:
@@ -247,6 +269,11 @@ class PartitionModel:
             P = self.P[:, :self.widths[l + 1]]
             gnn.layer_backward_narrow(self.graph, self.grad_out(l), self.layer_out(l), self.H[l], self.W[l],
                                       l < self.L - 1, self.dW[l], P, self.dH[l] if l > 0 else None)
+        elif self._reordered(l):
+            rows = self.n_local + self.n_halo if want_halo_grad else self.n_local
+            gnn.layer_backward_reordered(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
+                                         l < self.L - 1, self.dW[l], self.Pr[:rows, :self.widths[l + 1]],
+                                         self.dH[l][:rows], want_halo_grad=want_halo_grad)
         elif l > 0:
             gnn.layer_backward(self.graph, self.grad_out(l), self.layer_out(l), self.Z[l], self.W[l],
                                l < self.L - 1, self.dW[l], self.widths[l], dZ=self.dZ_view(l),

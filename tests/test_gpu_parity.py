@@ -348,6 +348,26 @@ def test_epoch(case):
         close(pushed, ref["Hout"][l - 1], tol, f"pushed table {l}")
 
 
+def test_epoch_reordered_backward():
+    # the epoch with layers l > 0 differentiated in the other product order agrees with the oracle's epoch to the
+    # bf16 tolerance: the two orders differ by the rounding of P = A_hat^T dY to bf16 (|error| <= 2^-9 |P| per
+    # element, a few 1e-3 of dH's scale after the product with W^T)
+    w, part, _ = problem("rmat16m", "tiny")
+    m, tables_h, Ws, y = _load_model(w, part, "f32", reorder=True)
+    m.step()
+    m.check_errors()
+    Wr = [maybe_round(x.astype(np.float64), "bf16") for x in Ws]
+    ref = oracle.epoch(part, [widen(t, "bf16", f) for t, f in zip(tables_h, w.widths)], Wr, y, w.agg, bf16=True)
+    dWb, dHb, n_amb = epoch_bounds(part, ref, Wr, w.agg, True)
+    tol = TOL["bf16"]
+    for l in range(w.layers):
+        close_bounded(m.dW[l].cpu().numpy(), ref["dW"][l], tol, dWb[l], f"dW[{l}] ({n_amb} ambiguous decisions)")
+    for l in range(1, w.layers):
+        close_bounded(to_host(m.dH[l]), ref["dH"][l], tol, dHb[l], f"dH[{l}] (local + halo)")
+    with pytest.raises(ValueError):
+        m.set_grad_dtype(torch.bfloat16)
+
+
 # ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------
@@ -700,3 +720,54 @@ def test_expired_wait_is_reported_and_the_next_call_is_exact(dt):
     assert_ok(g)
     Zr = maybe_round(oracle.aggregate(part, widen(H_h, dt, f_in), f_in, "gcn"), dt)
     close(to_host(Z), Zr, TOL[dt], "Z after the expired wait")
+
+
+@pytest.mark.parametrize("f_in,f_out,relu,halo", [(256, 256, True, True), (128, 256, False, True),
+                                                  (256, 64, True, False), (200, 40, True, True)])
+def test_reordered_backward_matches_oracle(f_in, f_out, relu, halo):
+    # the GCN backward in the other product order (P = A_hat^T dY in bf16, dH = P W^T) against the oracle's
+    # own reading of that order: R-MAT partition, bf16 activations, fp32 gradients, ragged widths included
+    part = TINY["rmat16m"].make(0)
+    nL, nT = part.n_local, part.n_total
+    g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(), nL,
+                         part.n_halo, None, "gcn")
+    bf = torch.bfloat16
+    Zh = synth.features(nL, f_in, ld_for(f_in, bf), SEED, 61, "normal", bf16=True)
+    Oh = synth.features(nL, f_out, ld_for(f_out, bf), SEED, 62, "normal", bf16=True)
+    Gh = synth.features(nL, f_out, ld_for(f_out, torch.float32), SEED, 63, "normal")
+    W = synth.glorot(f_in, f_out, SEED, 64)
+    Z = torch.from_numpy(Zh.view(np.int16)).cuda().view(bf)[:, :f_in]
+    Hout = torch.from_numpy(Oh.view(np.int16)).cuda().view(bf)[:, :f_out]
+    G = torch.from_numpy(Gh).cuda()[:, :f_out]
+    rows = nT if halo else nL
+    dW = torch.full((f_in, f_out), float("nan"), dtype=torch.float32, device="cuda")
+    P = padded(rows, f_out, bf, "cuda")
+    dH = padded(rows, f_in, torch.float32, "cuda")
+    gnn.layer_backward_reordered(g, G, Hout, Z, torch.from_numpy(W).cuda(), relu, dW, P, dH, want_halo_grad=halo)
+    torch.cuda.synchronize()
+    assert gnn.get_error(g) == gnn.GNN_OK
+    Wr = oracle.round_bf16(W.astype(np.float64))
+    dWr, Pr, dHr = oracle.layer_backward_reordered(
+        part, oracle.transpose(part), Gh[:, :f_out], oracle.widen(Oh[:, :f_out], True),
+        oracle.widen(Zh[:, :f_in], True), Wr, relu, bf16=True, rows=None if halo else np.arange(nL))
+    close(dW.cpu().numpy(), dWr, TOL["bf16"], "dW")
+    close(P.float().cpu().numpy(), Pr[:rows], TOL["bf16"], "P")
+    close(dH.cpu().numpy(), dHr[:rows], TOL["bf16"], "dH")
+    gnn.graph_destroy(g)
+
+
+def test_reordered_backward_refuses_other_aggregations():
+    # GraphSAGE graphs (and any precision but bf16 activations with fp32 gradients) are not taken
+    part = TINY["sage2m"].make(0)
+    g = gnn.graph_create(torch.from_numpy(part.rowptr).cuda(), torch.from_numpy(part.colidx).cuda(), part.n_local,
+                         part.n_halo, torch.from_numpy(part.deg).cuda() if part.deg is not None else None, "sage")
+    f = 64
+    bf = torch.bfloat16
+    Z = padded(part.n_local, f, bf, "cuda")
+    G = padded(part.n_local, f, torch.float32, "cuda")
+    W = torch.zeros((f, f), dtype=torch.float32, device="cuda")
+    with pytest.raises(gnn.GnnError) as e:
+        gnn.layer_backward_reordered(g, G, Z, Z, W, False, W.clone(), padded(part.n_total, f, bf, "cuda"),
+                                     padded(part.n_total, f, torch.float32, "cuda"))
+    assert e.value.status == gnn.GNN_EUNSUPPORTED
+    gnn.graph_destroy(g)

@@ -60,6 +60,37 @@ def test_gcn_backward_matches_dense(seed):
     assert _rel(dH, dHd) < 1e-13
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_reordered_backward_is_the_dense_chain_rule(seed):
+    # dH = (A_hat^T dY) W^T, the other order of the same products: against the dense
+    # A_hat_block^T (dY W^T) and the textbook-order oracle; with bf16 rounding, P is
+    # rounded once (dense: the same rounding applied to A_hat^T dY)
+    A, local, part, cols = _tiny(seed)
+    rng = np.random.default_rng(300 + seed)
+    f_in, f_out = 6, 4
+    Z = rng.standard_normal((part.n_local, f_in))
+    W = rng.standard_normal((f_in, f_out))
+    G = rng.standard_normal((part.n_local, f_out))
+    Hout = rng.standard_normal((part.n_local, f_out))
+    T = oracle.transpose(part)
+    Ad = dense_gcn_block(A, local, cols)
+    dY = G * (Hout > 0)
+    dW, P, dH = oracle.layer_backward_reordered(part, T, G, Hout, Z, W, relu=True)
+    assert _rel(dW, Z.T @ dY) < 1e-13
+    assert _rel(P, Ad.T @ dY) < 1e-13
+    assert _rel(dH, Ad.T @ (dY @ W.T)) < 1e-12
+    dW_t, _, dH_t = oracle.layer_backward(part, T, G, Hout, Z, W, "gcn", relu=True)
+    assert _rel(dW, dW_t) < 1e-13 and _rel(dH, dH_t) < 1e-12
+    dWb, Pb, dHb = oracle.layer_backward_reordered(part, T, G, Hout, Z, W, relu=True, bf16=True)
+    dYb = oracle.round_bf16(dY)
+    assert np.array_equal(Pb, oracle.round_bf16(Pb)) and _rel(Pb, oracle.round_bf16(Ad.T @ dYb)) < 1e-13
+    assert _rel(dHb, oracle.round_bf16(Ad.T @ dYb) @ W.T) < 1e-12 and _rel(dWb, Z.T @ dYb) < 1e-13
+    # only the halo-free rows
+    rows = np.arange(part.n_local)
+    _, Pr, dHr = oracle.layer_backward_reordered(part, T, G, Hout, Z, W, relu=True, rows=rows)
+    assert _rel(dHr, dH[:part.n_local]) < 1e-13
+
+
 @pytest.mark.parametrize("seed", [0, 3])
 def test_sage_forward_backward_match_dense(seed):
     A, local, part, cols = _tiny(seed, N=36, nL=20, p=0.2)
