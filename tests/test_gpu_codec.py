@@ -192,11 +192,31 @@ def test_codec_bad_ids_and_arguments():
 # the codec on rows of a message between processes (gnn_quantize_rows /
 # gnn_dequantize_rows): codes keyed by the rows' global ids, dequantised into
 # place or added onto rows of another matrix
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+@pytest.mark.parametrize("f", [3, 40, 64, 100, 128, 200, 256, 300])
+def test_message_rows_special_magnitudes(bits, f):
+    # every branch of the quantiser at widths that take 1, 2 or 4 chunks of 8 values per lane (with ragged
+    # last lanes) and at a width past the eight-lanes-per-row kernels
+    n = 1000
+    Xv = _special_rows(n, f, np.random.default_rng(10 * bits + f))
+    X = padded(n, f, torch.float32, "cuda")
+    X.copy_(torch.from_numpy(Xv).cuda())
+    keys = np.random.default_rng(f).permutation(4 * n)[:n].astype(np.int64)
+    ldc = gnn.codec_row_bytes(f, bits)
+    codes = torch.full((n, ldc), 0x5A, dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+    seed = 123 + bits
+    gnn.quantize_rows(X, torch.from_numpy(keys).cuda(), codes, sz, bits, seed)
+    ref_c, ref_sz = oracle.quantize_rows(Xv, keys, bits, seed, ldc)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_c)
+    np.testing.assert_array_equal(sz.cpu().numpy().view(np.uint32), ref_sz.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("bits", [1, 2, 4, 8])
-@pytest.mark.parametrize("f", [5, 64, 256, 300])
+@pytest.mark.parametrize("f", [5, 64, 100, 128, 200, 256, 300])
 def test_message_rows_codec_matches_oracle(dt, bits, f):
     rng = np.random.default_rng(bits * 1000 + f)
     n = 2000
