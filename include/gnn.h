@@ -236,8 +236,10 @@ gnn_status gnn_layer_backward(gnn_graph *g, const void *G, int64_t ld_g, const v
  * want_halo_grad != 0 computes P and dH for the halo rows too (Sylvie's J).
  * The results agree with gnn_layer_backward up to the rounding of P.  Only the
  * GCN aggregation with bf16 activations and fp32 gradients, on the tensor
- * cores, is taken: other graphs, precision pairs or widths return
- * GNN_EUNSUPPORTED before anything runs; bad pointers or sizes GNN_EINVAL. */
+ * cores, is taken: a GraphSAGE graph, another precision pair or widths past
+ * the tensor-core limits return GNN_EUNSUPPORTED before anything runs; an
+ * attention graph (as for every layer call), bad pointers or sizes
+ * GNN_EINVAL. */
 gnn_status gnn_layer_backward_reordered(gnn_graph *g, const void *G, int64_t ld_g, const void *H_out, int64_t ld_out,
                                         const void *Z, int64_t ld_z, const float *W, int64_t f_in, int64_t f_out,
                                         int relu, float *dW, void *P, int64_t ld_p, void *dH, int64_t ld_dh,
