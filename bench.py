@@ -521,22 +521,29 @@ def measure_other_order(m, stream, steps: int, ef: int):
     bf16, dH = P W^T (bf16 activations, fp32 gradients)."""
     import torch
 
+    from sparse_aggregation_dense_gb300 import gnn
+
     m.set_reorder(True)
     try:
         m.step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gnn.profile_read(m.graph)  # clear
+        gnn.profile_enable(m.graph, True)
         e0.record(stream)
         for _ in range(steps):
             m.step()
         e1.record(stream)
         torch.cuda.synchronize()
+        gnn.profile_enable(m.graph, False)
+        prof = gnn.profile_read(m.graph)
         m.check_errors()
         ms = e0.elapsed_time(e1) / steps
     finally:
         m.set_reorder(False)
     return {"backward": "dH = (A_hat^T dY) W^T on layers l > 0, P in bf16", "ms_per_step": ms,
-            "value": ef / (ms / 1e3), "steps": steps}
+            "value": ef / (ms / 1e3), "steps": steps,
+            "breakdown_ms_per_step": {k: round(v[0] / steps, 3) for k, v in prof.items()}}
 
 
 def measure_gat(workload: str, steps: int = 5):
