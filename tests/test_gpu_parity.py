@@ -215,6 +215,26 @@ def _compact(z_rows: np.ndarray, f_in: int, half: int, sage: bool) -> np.ndarray
     return np.concatenate([z_rows[:, :f_in], z_rows[:, half:half + f_in]], axis=1)
 
 
+def _sampled_transpose(part, n_rows, seed):
+    """Output rows U of the transposed aggregation (random local and halo rows
+    and the heaviest transpose rows), the transpose of the entries that reach
+    them, and the input rows V those entries read."""
+    nL, nT = part.n_local, part.n_total
+    rowptrT = np.concatenate([[0], np.cumsum(np.bincount(part.colidx, minlength=nT))])
+    U = sample_with_heavy(rowptrT, n_rows, seed)
+    sel = np.zeros(nT, bool)
+    sel[U] = True
+    keep = sel[part.colidx]
+    cnt = np.zeros(nL, np.int64)
+    row_of = np.repeat(np.arange(nL), np.diff(part.rowptr))
+    np.add.at(cnt, row_of[keep], 1)
+    sub_rowptr = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+    sub = synth.Partition(sub_rowptr, part.colidx[keep], nL, part.n_halo, part.deg, part.local_ids,
+                          part.halo_ids, part.n_table)
+    T = oracle.transpose(sub)
+    return U, T, np.unique(T[1]).astype(np.int64)
+
+
 @pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"{c[0]}-{c[1]}-L{c[2]}-grad_{c[3]}")
 def test_backward_layer(case):
     name, size, l, gd = case
@@ -254,19 +274,7 @@ def test_backward_layer(case):
     close(dWg[:, cols], dWr, tol, f"dW columns {cols}")
     # dH on output rows U (random local + halo rows and the heaviest transpose rows)
     if is_sampled(size, name):
-        rowptrT = np.concatenate([[0], np.cumsum(np.bincount(part.colidx, minlength=nT))])
-        U = sample_with_heavy(rowptrT, 600, SEED + 1)
-        sel = np.zeros(nT, bool)
-        sel[U] = True
-        keep = sel[part.colidx]
-        cnt = np.zeros(nL, np.int64)
-        row_of = np.repeat(np.arange(nL), np.diff(part.rowptr))
-        np.add.at(cnt, row_of[keep], 1)
-        sub_rowptr = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
-        sub = synth.Partition(sub_rowptr, part.colidx[keep], nL, part.n_halo, part.deg, part.local_ids,
-                              part.halo_ids, part.n_table)
-        T = oracle.transpose(sub)
-        V = np.unique(T[1]).astype(np.int64)
+        U, T, V = _sampled_transpose(part, 600, SEED + 1)
     else:
         U = np.arange(nT, dtype=np.int64)
         T = oracle.transpose(part)
@@ -754,6 +762,40 @@ def test_reordered_backward_matches_oracle(f_in, f_out, relu, halo):
     close(P.float().cpu().numpy(), Pr[:rows], TOL["bf16"], "P")
     close(dH.cpu().numpy(), dHr[:rows], TOL["bf16"], "dH")
     gnn.graph_destroy(g)
+
+
+@pytest.mark.parametrize("l", [1, 2])
+def test_reordered_backward_full_size_sampled(l):
+    # the bench partition's layers 2 and 1 in the other product order, in the launch configuration the bench's
+    # other_order step uses: dW on whole columns, P and dH on sampled output rows (local, halo, heaviest)
+    w, part, g = problem("rmat16m", "full")
+    f_in, f_out = w.widths[l], w.widths[l + 1]
+    relu = l < w.layers - 1
+    nL, nT = part.n_local, part.n_total
+    G_h = gen_matrix(nL, f_out, "f32", SEED, 200 + l)
+    Ho_h = gen_matrix(nL, f_out, "bf16", SEED, 300 + l)
+    Z_h = gen_matrix(nL, f_in, "bf16", SEED, 400 + l)
+    W = synth.glorot(f_in, f_out, SEED, synth.STREAM_WEIGHT + l)
+    dW = torch.full((f_in, f_out), float("nan"), dtype=torch.float32, device="cuda")
+    P = padded(nT, f_out, torch.bfloat16, "cuda")
+    dH = padded(nT, f_in, torch.float32, "cuda")
+    gnn.layer_backward_reordered(g, to_device(G_h, "f32", f_out), to_device(Ho_h, "bf16", f_out),
+                                 to_device(Z_h, "bf16", f_in), torch.from_numpy(W).cuda(), relu, dW, P, dH)
+    assert_ok(g)
+    tol = TOL["bf16"]
+    cols = sorted({0, f_out // 2, f_out - 1})
+    dWr = oracle.update_backward_dw_columns(G_h[:, :f_out], Ho_h[:, :f_out], Z_h[:, :f_in], relu, cols, True, False)
+    close(dW.cpu().numpy()[:, cols], dWr, tol, f"dW columns {cols}")
+    U, T, V = _sampled_transpose(part, 600, SEED + 2)
+    vmap = -np.ones(nL, np.int64)
+    vmap[V] = np.arange(V.shape[0])
+    Gw, How = oracle.widen(G_h[V][:, :f_out], False), oracle.widen(Ho_h[V][:, :f_out], True)
+    dY = oracle.round_bf16(Gw * (How > 0) if relu else Gw)  # the product operand dY, as the layer rounds it
+    Pr = oracle.round_bf16(oracle.aggregate_backward(part, T, dY, f_out, "gcn", rows=U, dmap=vmap,
+                                                     weights=oracle.gcn_dinv(part)))
+    Uc = torch.from_numpy(U).cuda()
+    close(P.index_select(0, Uc).float().cpu().numpy(), Pr, tol, "P")
+    close(to_host(dH.index_select(0, Uc)), Pr @ oracle.round_bf16(W.astype(np.float64)).T, tol, "dH")
 
 
 def test_reordered_backward_refuses_other_aggregations():
