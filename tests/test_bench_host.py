@@ -77,3 +77,21 @@ def test_cache_floor_matches_a_simulated_static_cache():
     assert full == fwd_b + bwd_b
     gathered = np.unique(part.colidx).shape[0]
     assert none[0] == fwd_b[0] - nT * w.widths[0] * elem + (part.nnz + nT - gathered) * w.widths[0] * elem
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    # the oracle arm on a tiny workload: one JSON line with the contract's keys and the oracle as its baseline
+    import json
+
+    bench.main(["--impl", "reference", "--workload", "er5k-tiny", "--steps", "2", "--warmup", "1",
+                "--ref-seconds", "0.05"])
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "er5k-tiny"
