@@ -109,6 +109,37 @@ def test_partition_epoch_passes_the_binding_checks(lib, agg, dtype, narrow, grad
     assert fwd in lib.calls
 
 
+@pytest.mark.parametrize("want_halo_grad", [True, False])
+def test_reordered_backward_passes_the_binding_checks(lib, want_halo_grad):
+    # layers l > 0 take the other product order, layer 0 the textbook backward (it has no input gradient)
+    m, part = _model("gcn", torch.bfloat16, widths=(12, 20, 16, 6))
+    m.set_reorder(True)
+    for l in range(m.L):
+        m.tables[l] = padded(part.n_table, m.widths[l], torch.bfloat16, "cpu")
+    m.forward()
+    m.loss_grad()
+    lib.calls.clear()
+    m.backward(want_halo_grad)
+    assert lib.calls == ["gnn_layer_backward_reordered", "gnn_layer_backward_reordered", "gnn_layer_backward"]
+    m.set_reorder(False)
+    lib.calls.clear()
+    m.backward(want_halo_grad)
+    assert lib.calls == ["gnn_layer_backward"] * 3
+
+
+def test_reordered_backward_needs_gcn_bf16_and_fp32_gradients(lib):
+    with pytest.raises(ValueError):
+        _model("sage", torch.bfloat16)[0].set_reorder(True)
+    with pytest.raises(ValueError):
+        _model("gcn", torch.float32)[0].set_reorder(True)
+    with pytest.raises(ValueError):
+        _model("gcn", torch.bfloat16, grad_dtype=torch.bfloat16)[0].set_reorder(True)
+    m, _ = _model("gcn", torch.bfloat16)
+    m.set_reorder(True)
+    with pytest.raises(ValueError):
+        m.set_grad_dtype(torch.bfloat16)
+
+
 @pytest.mark.parametrize("mode,sync_every", [("sync", 0), ("stale", 0), ("stale", 1)])
 def test_multi_partition_epoch_order(lib, mode, sync_every):
     parts, N = _parts(3)
